@@ -1,0 +1,280 @@
+"""fp64 CPU oracle for one sparse MoE layer forward -- TEST INFRASTRUCTURE.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never calls it and
+shares no code with it.
+
+This module is argument marshalling around ``moe_oracle.c`` (ctypes); all the
+arithmetic is in that C file, written as the plain definition in double
+precision.  Inputs are torch CPU tensors (float32 or bfloat16) or numpy
+arrays; outputs are numpy arrays (float64 for values, int32 for indices).
+"""
+import ctypes
+import math
+import os
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+_lib = None
+
+F32, BF16 = 0, 1
+
+
+def _load(path=None):
+    """Load liboracle.so (building it first if needed).  ``path`` loads another
+    build of the same source instead (used by the mutation tests)."""
+    global _lib
+    if _lib is None or path is not None:
+        path = path or _build.build()
+        lib = ctypes.CDLL(path)
+        vp, i32p, f64p, f32p = (ctypes.c_void_p, ctypes.c_void_p,
+                                ctypes.c_void_p, ctypes.c_void_p)
+        ci, cd = ctypes.c_int, ctypes.c_double
+        lib.oracle_router_logits.argtypes = [ci, ci, ci, ci, vp, vp, f32p, f64p, ci]
+        lib.oracle_topk_softmax.argtypes = [ci, ci, ci, f64p, i32p, f64p]
+        lib.oracle_capacity.argtypes = [cd, ci, ci, ci]
+        lib.oracle_group.argtypes = [ci, ci, ci, ci, i32p, i32p, i32p, i32p, i32p,
+                                     i32p, i32p]
+        lib.oracle_expert_rows.argtypes = [ci, ci, ci, vp, vp, vp, ci, vp, ci, f64p, ci]
+        lib.oracle_combine_rows.argtypes = [ci, ci, ci, i32p, f64p, f64p, f64p, f64p]
+        lib.oracle_moe_forward.argtypes = (
+            [ci] * 6 + [vp, vp, f32p, vp, vp, vp, ci, vp, vp, vp, cd, f64p, f64p,
+                        i32p, f64p, i32p, i32p, i32p, i32p, ci])
+        for name in ("oracle_router_logits", "oracle_topk_softmax", "oracle_capacity",
+                     "oracle_group", "oracle_expert_rows", "oracle_combine_rows",
+                     "oracle_moe_forward"):
+            getattr(lib, name).restype = ci
+        _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------------
+# marshalling helpers
+# --------------------------------------------------------------------------
+class _Buf:
+    """Keeps a contiguous CPU buffer alive and exposes its address + dtype code."""
+
+    def __init__(self, a):
+        if isinstance(a, torch.Tensor):
+            a = a.detach()
+            if a.device.type != "cpu":
+                a = a.cpu()
+            a = a.contiguous()
+            if a.dtype == torch.bfloat16:
+                self.dtype = BF16
+            elif a.dtype == torch.float32:
+                self.dtype = F32
+            else:
+                self.dtype = None
+            self.keep = a
+            self.ptr = a.data_ptr()
+        else:
+            a = np.ascontiguousarray(a)
+            self.dtype = F32 if a.dtype == np.float32 else None
+            self.keep = a
+            self.ptr = a.ctypes.data
+
+
+def _f32_or_none(b):
+    if b is None:
+        return None, None
+    if isinstance(b, torch.Tensor):
+        b = b.detach().cpu().float().contiguous().numpy()
+    b = np.ascontiguousarray(b, dtype=np.float32)
+    return b, b.ctypes.data
+
+
+def _i32(a):
+    if isinstance(a, torch.Tensor):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data
+
+
+def _check(rc, name):
+    if rc != 0:
+        raise RuntimeError(f"{name} failed with code {rc}")
+
+
+# --------------------------------------------------------------------------
+# stage functions
+# --------------------------------------------------------------------------
+def router_logits(x, W_g, bias=None, nthreads=None):
+    """logits[T,N] (fp64) = x[T,d] @ W_g[d,N] + bias[N]."""
+    lib = _load()
+    bx, bw = _Buf(x), _Buf(W_g)
+    assert bx.dtype is not None and bx.dtype == bw.dtype
+    T, d = bx.keep.shape
+    N = bw.keep.shape[1]
+    bb, pb = _f32_or_none(bias)
+    out = np.empty((T, N), dtype=np.float64)
+    _check(lib.oracle_router_logits(T, d, N, bx.dtype, bx.ptr, bw.ptr, pb, out.ctypes.data,
+                                    nthreads or default_threads()), "oracle_router_logits")
+    return out
+
+
+def topk_softmax(logits, k):
+    """(topk_idx[T,k] int32, topk_w[T,k] fp64) from fp64 logits[T,N]."""
+    lib = _load()
+    logits = np.ascontiguousarray(logits, dtype=np.float64)
+    T, N = logits.shape
+    idx = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    _check(lib.oracle_topk_softmax(T, N, k, logits.ctypes.data, idx.ctypes.data,
+                                   w.ctypes.data), "oracle_topk_softmax")
+    return idx, w
+
+
+def route(x, W_g, k, bias=None, nthreads=None):
+    logits = router_logits(x, W_g, bias, nthreads)
+    idx, w = topk_softmax(logits, k)
+    return logits, idx, w
+
+
+def capacity(cf, T, k, N) -> int:
+    return int(_load().oracle_capacity(float(cf), T, k, N))
+
+
+def group(topk_idx, N, capacity_rows=0):
+    """Grouping by expert.  Returns dict of counts, offsets, perm_token,
+    perm_slot, inv_pos, dropped (see moe_oracle.c, oracle_group)."""
+    lib = _load()
+    idx = _i32(topk_idx)
+    T, k = idx.shape
+    counts = np.empty(N, dtype=np.int32)
+    offsets = np.empty(N + 1, dtype=np.int32)
+    perm_token = np.full(T * k, -1, dtype=np.int32)
+    perm_slot = np.full(T * k, -1, dtype=np.int32)
+    inv_pos = np.empty((T, k), dtype=np.int32)
+    dropped = np.zeros(1, dtype=np.int32)
+    _check(lib.oracle_group(T, N, k, int(capacity_rows), idx.ctypes.data, counts.ctypes.data,
+                            offsets.ctypes.data, perm_token.ctypes.data,
+                            perm_slot.ctypes.data, inv_pos.ctypes.data,
+                            dropped.ctypes.data), "oracle_group")
+    A = int(offsets[N])
+    return dict(counts=counts, offsets=offsets, perm_token=perm_token[:A],
+                perm_slot=perm_slot[:A], inv_pos=inv_pos, dropped=int(dropped[0]))
+
+
+def expert_rows(W_gate_e, W_up_e, W_down_e, xrows, nthreads=None):
+    """out[R,d] (fp64) = SwiGLU expert (W_gate_e [d,f], W_up_e [d,f], W_down_e [f,d])
+    applied to each row of xrows [R,d]."""
+    lib = _load()
+    bg, bu, bd, bx = _Buf(W_gate_e), _Buf(W_up_e), _Buf(W_down_e), _Buf(xrows)
+    assert bg.dtype is not None and bg.dtype == bu.dtype == bd.dtype
+    d, f = bg.keep.shape
+    R = bx.keep.shape[0]
+    out = np.empty((R, d), dtype=np.float64)
+    _check(lib.oracle_expert_rows(d, f, bg.dtype, bg.ptr, bu.ptr, bd.ptr, R, bx.ptr,
+                                  bx.dtype, out.ctypes.data, nthreads or default_threads()),
+           "oracle_expert_rows")
+    return out
+
+
+def combine_rows(inv_pos_rows, topk_w_rows, expert_out, shared=None):
+    """y[R,d] = sum_j kept w[r,j] * expert_out[r,j,:] (+ shared[r,:])."""
+    lib = _load()
+    inv = _i32(inv_pos_rows)
+    w = np.ascontiguousarray(topk_w_rows, dtype=np.float64)
+    o = np.ascontiguousarray(expert_out, dtype=np.float64)
+    R, k, d = o.shape
+    sh = None if shared is None else np.ascontiguousarray(shared, dtype=np.float64)
+    y = np.empty((R, d), dtype=np.float64)
+    _check(lib.oracle_combine_rows(R, k, d, inv.ctypes.data, w.ctypes.data, o.ctypes.data,
+                                   _p(sh), y.ctypes.data), "oracle_combine_rows")
+    return y
+
+
+def moe_forward(x, W_g, W_gate, W_up, W_down, k, bias=None, Ws_gate=None, Ws_up=None,
+                Ws_down=None, capacity_factor=0.0, nthreads=None):
+    """Whole layer on all tokens with every weight in host memory (small cases).
+
+    Returns dict: y [T,d] fp64, logits, topk_idx, topk_w, counts, offsets,
+    inv_pos, dropped.
+    """
+    lib = _load()
+    bx, bg = _Buf(x), _Buf(W_g)
+    bwg, bwu, bwd = _Buf(W_gate), _Buf(W_up), _Buf(W_down)
+    dt = bx.dtype
+    assert dt is not None and all(b.dtype == dt for b in (bg, bwg, bwu, bwd))
+    T, d = bx.keep.shape
+    N, _, f = bwg.keep.shape
+    fs = 0
+    ps = (None, None, None)
+    keep = []
+    if Ws_gate is not None:
+        bsg, bsu, bsd = _Buf(Ws_gate), _Buf(Ws_up), _Buf(Ws_down)
+        assert bsg.dtype == dt == bsu.dtype == bsd.dtype
+        fs = bsg.keep.shape[1]
+        ps = (bsg.ptr, bsu.ptr, bsd.ptr)
+        keep += [bsg, bsu, bsd]
+    bb, pb = _f32_or_none(bias)
+    y = np.empty((T, d), dtype=np.float64)
+    logits = np.empty((T, N), dtype=np.float64)
+    idx = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    counts = np.empty(N, dtype=np.int32)
+    offsets = np.empty(N + 1, dtype=np.int32)
+    inv = np.empty((T, k), dtype=np.int32)
+    dropped = np.zeros(1, dtype=np.int32)
+    _check(lib.oracle_moe_forward(
+        T, d, f, N, k, dt, bx.ptr, bg.ptr, pb, bwg.ptr, bwu.ptr, bwd.ptr, fs, *ps,
+        float(capacity_factor), y.ctypes.data, logits.ctypes.data, idx.ctypes.data,
+        w.ctypes.data, counts.ctypes.data, offsets.ctypes.data, inv.ctypes.data,
+        dropped.ctypes.data, nthreads or default_threads()), "oracle_moe_forward")
+    return dict(y=y, logits=logits, topk_idx=idx, topk_w=w, counts=counts,
+                offsets=offsets, inv_pos=inv, dropped=int(dropped[0]))
+
+
+def forward_rows(x_rows, topk_idx_rows, topk_w_rows, inv_pos_rows, fetch_expert,
+                 shared=None, nthreads=None):
+    """Layer output for a subset of tokens, fetching one expert's weights at a time.
+
+    x_rows [R,d] (CPU tensor), topk_idx/topk_w/inv_pos rows [R,k] for those
+    tokens (routing and grouping already computed over ALL tokens, because
+    capacity drops depend on every earlier token), fetch_expert(e) -> (W_gate_e,
+    W_up_e, W_down_e) CPU tensors, shared = None or (Ws_gate, Ws_up, Ws_down).
+    Returns y [R,d] fp64.
+    """
+    idx = _i32(topk_idx_rows)
+    inv = _i32(inv_pos_rows)
+    R, k = idx.shape
+    d = x_rows.shape[1]
+    out = np.zeros((R, k, d), dtype=np.float64)
+    for e in sorted(set(int(v) for v in idx.ravel())):
+        rows, slots = np.nonzero((idx == e) & (inv >= 0))
+        if rows.size == 0:
+            continue
+        wg, wu, wd = fetch_expert(e)
+        o = expert_rows(wg, wu, wd, x_rows[torch.as_tensor(rows, dtype=torch.long)],
+                        nthreads)
+        out[rows, slots] = o
+    sh = None
+    if shared is not None:
+        sh = expert_rows(shared[0], shared[1], shared[2], x_rows, nthreads)
+    return combine_rows(inv, topk_w_rows, out, sh)
+
+
+def near_tie_tokens(logits, k, rel=1e-4):
+    """Boolean mask of tokens whose k-th and (k+1)-th largest logits differ by
+    less than rel * max(|l_k|, |l_k+1|) (the routing near-tie reading)."""
+    logits = np.asarray(logits, dtype=np.float64)
+    T, N = logits.shape
+    if k >= N:
+        return np.zeros(T, dtype=bool)
+    s = -np.sort(-np.where(np.isnan(logits), -np.inf, logits), axis=1)
+    a, b = s[:, k - 1], s[:, k]
+    scale = np.maximum(np.abs(a), np.abs(b))
+    return np.abs(a - b) < rel * scale
+
+

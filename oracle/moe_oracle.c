@@ -1,0 +1,405 @@
+/*
+ * moe_oracle.c -- plain, slow, fp64 CPU oracle for the forward pass of one
+ * sparse Mixture-of-Experts layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or calls
+ * this file: only the test suite, the smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code, header, table or helper with the CUDA
+ * library; the two meet only through the seeded input generator.
+ *
+ * Every step is the plain definition written out as loops, in double
+ * precision, from the exact input values (bf16 inputs are widened exactly; no
+ * intermediate is rounded).  Sources, by page title and section:
+ *
+ *   [MoE-Sharding]  "MoE 分片：混合專家模型的平行化策略" (optiversetech.com)
+ *   [MoE-Infer]     "MoE 推理：激活参数 vs 总参数与专家路由" (inference-learning-path)
+ *   [MoE-DSV4]      "大模型MoE混合专家架构原理与DeepSeek-V4工程实践解析" (yunthe.com)
+ *   [MoE-Primer]    "MoE 架构科普：为什么大模型要「混合专家」" (lidayun.com)
+ *   [MoE-Sparse]    "MoE稀疏激活原理与工程实践：揭秘大模型参数幻觉" (CSDN)
+ *
+ * Readings taken where the pages are silent or disagree (each one is repeated
+ * next to the function that applies it):
+ *   - gate weights are the softmax over the k selected logits (renormalised);
+ *   - top-k order is descending logit, equal logits -> lower expert id first,
+ *     NaN ranks below every number;
+ *   - the expert FFN is SwiGLU: (SiLU(x W_gate) * (x W_up)) W_down, no biases;
+ *   - capacity C = ceil(cf * T * k / N); an assignment is kept iff its 0-based
+ *     rank among the assignments of its expert, ordered by token index, is < C;
+ *     a dropped slot contributes zero and the kept weights are not renormalised;
+ *   - the optional shared expert is added with weight 1, outside the softmax.
+ *
+ * Parity pins for this file live in tests/test_oracle.py.  The fp64 values of
+ * the expert FFN have no printed worked example on the pages; they are pinned
+ * by closed-form special cases and invariants only.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+
+/* Widen element i of a float32 or bf16 array to double, exactly. */
+static double elem(const void *p, int dtype, size_t i) {
+  if (dtype == ORACLE_F32) return (double)((const float *)p)[i];
+  uint32_t bits = ((uint32_t)((const uint16_t *)p)[i]) << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* ------------------------------------------------------------------------- */
+/* A tiny static-partition thread pool: run fn(lo, hi, ctx) over [0, n).       */
+/* ------------------------------------------------------------------------- */
+typedef void (*range_fn)(long lo, long hi, void *ctx);
+typedef struct {
+  range_fn fn;
+  void *ctx;
+  long lo, hi;
+} range_job;
+
+static void *range_thread(void *p) {
+  range_job *j = (range_job *)p;
+  j->fn(j->lo, j->hi, j->ctx);
+  return NULL;
+}
+
+static void parallel_for(long n, int nthreads, range_fn fn, void *ctx) {
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  if (n < nthreads) nthreads = (int)(n > 0 ? n : 1);
+  if (nthreads == 1) {
+    fn(0, n, ctx);
+    return;
+  }
+  pthread_t th[256];
+  range_job jobs[256];
+  for (int i = 0; i < nthreads; ++i) {
+    jobs[i].fn = fn;
+    jobs[i].ctx = ctx;
+    jobs[i].lo = n * i / nthreads;
+    jobs[i].hi = n * (i + 1) / nthreads;
+    pthread_create(&th[i], NULL, range_thread, &jobs[i]);
+  }
+  for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Step 1: router linear layer.                                               */
+/* [MoE-Sharding] "動態 token 路由", step 2 (router scores every expert);      */
+/* [MoE-Infer] "深入原理" (router is a linear layer giving N gate logits);     */
+/* [MoE-DSV4] "MoE核心机制" (g(x) computed from W_g and x).                    */
+/*   logits[t,e] = sum_i x[t,i] * W_g[i,e] + bias[e]                          */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+  int d, N, dtype;
+  const void *x, *Wg;
+  const float *bias;
+  double *logits;
+} router_ctx;
+
+static void router_rows(long lo, long hi, void *p) {
+  router_ctx *c = (router_ctx *)p;
+  for (long t = lo; t < hi; ++t) {
+    for (int e = 0; e < c->N; ++e) {
+      double acc = 0.0;
+      for (int i = 0; i < c->d; ++i)
+        acc += elem(c->x, c->dtype, (size_t)t * c->d + i) *
+               elem(c->Wg, c->dtype, (size_t)i * c->N + e);
+      if (c->bias) acc += (double)c->bias[e];
+      c->logits[(size_t)t * c->N + e] = acc;
+    }
+  }
+}
+
+int oracle_router_logits(int T, int d, int N, int dtype, const void *x,
+                         const void *Wg, const float *bias, double *logits,
+                         int nthreads) {
+  if (T < 0 || d < 1 || N < 1 || !x || !Wg || !logits) return 1;
+  router_ctx c = {d, N, dtype, x, Wg, bias, logits};
+  parallel_for(T, nthreads, router_rows, &c);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Steps 2-3: top-k selection and softmax-normalised gate weights.            */
+/* [MoE-Infer] "代码" (top-k of the gate logits, then exp(l - max)/sum over   */
+/* the selected k) and "深入原理" ("top-k softmax gives the weights");         */
+/* [MoE-Sharding] "動態 token 路由", step 6 (0.6 / 0.4 worked example).        */
+/* Reading: order by logit descending, equal logits -> lower expert id; NaN   */
+/* ranks below every number.  Slot j holds the expert of rank j.              */
+/* ------------------------------------------------------------------------- */
+static double rank_key(double v) { return isnan(v) ? -INFINITY : v; }
+
+/* Does expert a (logit la) come before expert b (logit lb)? */
+static int ranks_before(double la, int a, double lb, int b) {
+  double ka = rank_key(la), kb = rank_key(lb);
+  if (ka != kb) return ka > kb;
+  return a < b;
+}
+
+int oracle_topk_softmax(int T, int N, int k, const double *logits,
+                        int32_t *topk_idx, double *topk_w) {
+  if (T < 0 || N < 1 || k < 1 || k > N || !logits || !topk_idx || !topk_w)
+    return 1;
+  char *taken = (char *)calloc((size_t)N, 1);
+  if (!taken) return 2;
+  for (int t = 0; t < T; ++t) {
+    const double *l = logits + (size_t)t * N;
+    memset(taken, 0, (size_t)N);
+    /* Selection: k rounds, each picking the best expert not yet taken. */
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      for (int e = 0; e < N; ++e) {
+        if (taken[e]) continue;
+        if (best < 0 || ranks_before(l[e], e, l[best], best)) best = e;
+      }
+      taken[best] = 1;
+      topk_idx[(size_t)t * k + j] = best;
+    }
+    /* Softmax over the k selected logits, shifted by the largest (slot 0). */
+    double lmax = l[topk_idx[(size_t)t * k]];
+    double denom = 0.0;
+    for (int j = 0; j < k; ++j)
+      denom += exp(l[topk_idx[(size_t)t * k + j]] - lmax);
+    for (int j = 0; j < k; ++j)
+      topk_w[(size_t)t * k + j] = exp(l[topk_idx[(size_t)t * k + j]] - lmax) / denom;
+  }
+  free(taken);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Capacity.  [MoE-Sparse] 2.2 "专家容量（Expert Capacity）的硬约束";          */
+/* [MoE-DSV4] "MoE训练中的负载均衡" (capacity factor caps tokens per expert). */
+/* The pages give no formula; reading: C = ceil(cf * T * k / N), cf <= 0     */
+/* meaning no limit (returned as 0).                                          */
+/* ------------------------------------------------------------------------- */
+int oracle_capacity(double cf, int T, int k, int N) {
+  if (!(cf > 0.0) || N < 1) return 0;
+  return (int)ceil(cf * (double)T * (double)k / (double)N);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Step 4-5: grouping tokens by expert ("token-level batching").             */
+/* [MoE-Sparse] 3.1 (tokens of a batch are regrouped by target expert id,    */
+/* e.g. {0:[t0,t1,t3], 1:[t2,t5], ...}); [MoE-Sharding] "動態 token 路由"     */
+/* step 3.  For e = 0..N-1 the list of tokens t (ascending) with e among      */
+/* their k experts; with capacity C > 0 only the first C of each list are     */
+/* kept.                                                                      */
+/*   counts[e]   = number of assignments routed to e (before capacity)        */
+/*   offsets[e]  = sum of kept counts of experts < e; offsets[N] = kept total */
+/*   perm_token[p] = token of kept row p; perm_slot[p] = its slot j           */
+/*   inv_pos[t,j]  = row p of assignment (t,j), or -1 when dropped            */
+/* ------------------------------------------------------------------------- */
+int oracle_group(int T, int N, int k, int capacity, const int32_t *topk_idx,
+                 int32_t *counts, int32_t *offsets, int32_t *perm_token,
+                 int32_t *perm_slot, int32_t *inv_pos, int32_t *dropped) {
+  if (T < 0 || N < 1 || k < 1 || capacity < 0 || !topk_idx || !counts ||
+      !offsets || !inv_pos)
+    return 1;
+  int32_t n_dropped = 0;
+  int32_t next = 0;
+  for (int e = 0; e < N; ++e) {
+    offsets[e] = next;
+    int32_t rank = 0;
+    for (int t = 0; t < T; ++t) {
+      for (int j = 0; j < k; ++j) {
+        if (topk_idx[(size_t)t * k + j] != e) continue;
+        if (capacity > 0 && rank >= capacity) {
+          inv_pos[(size_t)t * k + j] = -1;
+          ++n_dropped;
+        } else {
+          int32_t p = next + rank;
+          inv_pos[(size_t)t * k + j] = p;
+          if (perm_token) perm_token[p] = t;
+          if (perm_slot) perm_slot[p] = j;
+        }
+        ++rank;
+      }
+    }
+    counts[e] = rank;
+    next += (capacity > 0 && rank > capacity) ? capacity : rank;
+  }
+  offsets[N] = next;
+  /* Assignments whose expert id is outside [0, N) are in no list. */
+  for (long a = 0; a < (long)T * k; ++a)
+    if (topk_idx[a] < 0 || topk_idx[a] >= N) {
+      inv_pos[a] = -1;
+      ++n_dropped;
+    }
+  if (dropped) *dropped = n_dropped;
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Step 6: one expert's FFN on a set of rows, SwiGLU form.                    */
+/* [MoE-Sharding] "什麼是 MoE 模型" (an expert is two linear maps with an     */
+/* activation between) and step 4 (the expert runs only on its tokens).       */
+/* SwiGLU reading: g = x W_gate, u = x W_up, h = SiLU(g) * u with             */
+/* SiLU(z) = z / (1 + exp(-z)), out = h W_down.  Layouts: W_gate, W_up [d,f], */
+/* W_down [f,d], row-major.                                                   */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+  int d, f, dtype, x_dtype;
+  const void *Wg, *Wu, *Wd, *xrows;
+  double *out;
+} ffn_ctx;
+
+static void ffn_rows(long lo, long hi, void *p) {
+  ffn_ctx *c = (ffn_ctx *)p;
+  double *g = (double *)malloc(sizeof(double) * (size_t)c->f);
+  double *u = (double *)malloc(sizeof(double) * (size_t)c->f);
+  double *xr = (double *)malloc(sizeof(double) * (size_t)c->d);
+  if (!g || !u || !xr) {
+    free(g); free(u); free(xr);
+    return;
+  }
+  for (long r = lo; r < hi; ++r) {
+    for (int i = 0; i < c->d; ++i)
+      xr[i] = elem(c->xrows, c->x_dtype, (size_t)r * c->d + i);
+    for (int j = 0; j < c->f; ++j) g[j] = u[j] = 0.0;
+    for (int i = 0; i < c->d; ++i) {
+      double xi = xr[i];
+      for (int j = 0; j < c->f; ++j) {
+        g[j] += xi * elem(c->Wg, c->dtype, (size_t)i * c->f + j);
+        u[j] += xi * elem(c->Wu, c->dtype, (size_t)i * c->f + j);
+      }
+    }
+    double *o = c->out + (size_t)r * c->d;
+    for (int q = 0; q < c->d; ++q) o[q] = 0.0;
+    for (int j = 0; j < c->f; ++j) {
+      double h = g[j] / (1.0 + exp(-g[j])) * u[j];
+      for (int q = 0; q < c->d; ++q)
+        o[q] += h * elem(c->Wd, c->dtype, (size_t)j * c->d + q);
+    }
+  }
+  free(g); free(u); free(xr);
+}
+
+int oracle_expert_rows(int d, int f, int dtype, const void *W_gate_e,
+                       const void *W_up_e, const void *W_down_e, int R,
+                       const void *xrows, int x_dtype, double *out,
+                       int nthreads) {
+  if (d < 1 || f < 1 || R < 0 || !W_gate_e || !W_up_e || !W_down_e ||
+      (R > 0 && (!xrows || !out)))
+    return 1;
+  ffn_ctx c = {d, f, dtype, x_dtype, W_gate_e, W_up_e, W_down_e, xrows, out};
+  parallel_for(R, nthreads, ffn_rows, &c);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Step 7: gate-weighted combine back in token order.                         */
+/* [MoE-Sharding] "動態 token 路由", step 6; [MoE-Infer] "深入原理" (output = */
+/* weighted sum of its k experts); [MoE-DSV4] "MoE核心机制" (sum of g_i E_i). */
+/* For each row r: y[r] = sum over kept slots j of w[r,j] * o[r,j,:]          */
+/*                 (+ shared[r,:] with weight 1 when given).                  */
+/* expert_out is [R, k, d]: the output of slot j's expert on row r's token.   */
+/* ------------------------------------------------------------------------- */
+int oracle_combine_rows(int R, int k, int d, const int32_t *inv_pos_rows,
+                        const double *topk_w_rows, const double *expert_out,
+                        const double *shared, double *y) {
+  if (R < 0 || k < 1 || d < 1 || (R > 0 && (!inv_pos_rows || !topk_w_rows ||
+                                           !expert_out || !y)))
+    return 1;
+  for (long r = 0; r < R; ++r) {
+    double *yr = y + (size_t)r * d;
+    for (int q = 0; q < d; ++q) yr[q] = 0.0;
+    for (int j = 0; j < k; ++j) {
+      if (inv_pos_rows[(size_t)r * k + j] < 0) continue; /* dropped slot */
+      double w = topk_w_rows[(size_t)r * k + j];
+      const double *o = expert_out + ((size_t)r * k + j) * d;
+      for (int q = 0; q < d; ++q) yr[q] += w * o[q];
+    }
+    if (shared)
+      for (int q = 0; q < d; ++q) yr[q] += shared[(size_t)r * d + q];
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Whole layer, all tokens, weights resident in host memory (small cases).    */
+/* Composes steps 1-7 above.  Optional outputs may be NULL.                   */
+/* ------------------------------------------------------------------------- */
+int oracle_moe_forward(int T, int d, int f, int N, int k, int dtype,
+                       const void *x, const void *Wg, const float *bias,
+                       const void *W_gate, const void *W_up, const void *W_down,
+                       int fs, const void *Ws_gate, const void *Ws_up,
+                       const void *Ws_down, double capacity_factor, double *y,
+                       double *logits_out, int32_t *topk_idx_out,
+                       double *topk_w_out, int32_t *counts_out,
+                       int32_t *offsets_out, int32_t *inv_pos_out,
+                       int32_t *dropped_out, int nthreads) {
+  if (T < 1 || d < 1 || f < 1 || N < 1 || k < 1 || k > N || !x || !Wg ||
+      !W_gate || !W_up || !W_down || !y)
+    return 1;
+  if (fs > 0 && (!Ws_gate || !Ws_up || !Ws_down)) return 1;
+  size_t esz = dtype == ORACLE_F32 ? 4 : 2;
+  size_t TK = (size_t)T * k;
+  double *logits = (double *)malloc(sizeof(double) * (size_t)T * N);
+  int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * TK);
+  double *w = (double *)malloc(sizeof(double) * TK);
+  int32_t *counts = (int32_t *)malloc(sizeof(int32_t) * (size_t)N);
+  int32_t *offsets = (int32_t *)malloc(sizeof(int32_t) * ((size_t)N + 1));
+  int32_t *inv = (int32_t *)malloc(sizeof(int32_t) * TK);
+  double *o = (double *)malloc(sizeof(double) * TK * d);
+  double *sh = fs > 0 ? (double *)malloc(sizeof(double) * (size_t)T * d) : NULL;
+  int rc = 0;
+  if (!logits || !idx || !w || !counts || !offsets || !inv || !o ||
+      (fs > 0 && !sh)) {
+    rc = 2;
+    goto done;
+  }
+  oracle_router_logits(T, d, N, dtype, x, Wg, bias, logits, nthreads);
+  oracle_topk_softmax(T, N, k, logits, idx, w);
+  int C = oracle_capacity(capacity_factor, T, k, N);
+  int32_t dropped = 0;
+  oracle_group(T, N, k, C, idx, counts, offsets, NULL, NULL, inv, &dropped);
+  /* Expert outputs for every (t, j), one expert at a time, gathering its rows. */
+  memset(o, 0, sizeof(double) * TK * d);
+  for (int e = 0; e < N; ++e) {
+    int R = 0;
+    for (size_t a = 0; a < TK; ++a)
+      if (idx[a] == e && inv[a] >= 0) ++R;
+    if (R == 0) continue;
+    char *xr = (char *)malloc(esz * (size_t)R * d);
+    double *orow = (double *)malloc(sizeof(double) * (size_t)R * d);
+    size_t *which = (size_t *)malloc(sizeof(size_t) * (size_t)R);
+    if (!xr || !orow || !which) {
+      free(xr); free(orow); free(which);
+      rc = 2;
+      goto done;
+    }
+    int r = 0;
+    for (size_t a = 0; a < TK; ++a) {
+      if (idx[a] != e || inv[a] < 0) continue;
+      size_t t = a / (size_t)k;
+      memcpy(xr + esz * (size_t)r * d, (const char *)x + esz * t * d, esz * d);
+      which[r++] = a;
+    }
+    const char *wg = (const char *)W_gate + esz * (size_t)e * d * f;
+    const char *wu = (const char *)W_up + esz * (size_t)e * d * f;
+    const char *wd = (const char *)W_down + esz * (size_t)e * f * d;
+    oracle_expert_rows(d, f, dtype, wg, wu, wd, R, xr, dtype, orow, nthreads);
+    for (int q = 0; q < R; ++q)
+      memcpy(o + which[q] * d, orow + (size_t)q * d, sizeof(double) * d);
+    free(xr); free(orow); free(which);
+  }
+  if (fs > 0)
+    oracle_expert_rows(d, fs, dtype, Ws_gate, Ws_up, Ws_down, T, x, dtype, sh,
+                       nthreads);
+  oracle_combine_rows(T, k, d, inv, w, o, sh, y);
+  if (logits_out) memcpy(logits_out, logits, sizeof(double) * (size_t)T * N);
+  if (topk_idx_out) memcpy(topk_idx_out, idx, sizeof(int32_t) * TK);
+  if (topk_w_out) memcpy(topk_w_out, w, sizeof(double) * TK);
+  if (counts_out) memcpy(counts_out, counts, sizeof(int32_t) * (size_t)N);
+  if (offsets_out) memcpy(offsets_out, offsets, sizeof(int32_t) * ((size_t)N + 1));
+  if (inv_pos_out) memcpy(inv_pos_out, inv, sizeof(int32_t) * TK);
+  if (dropped_out) *dropped_out = dropped;
+done:
+  free(logits); free(idx); free(w); free(counts); free(offsets); free(inv);
+  free(o); free(sh);
+  return rc;
+}

@@ -1,0 +1,54 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a private copy of the oracle's C source (on
+the CPU, in a temporary directory), builds it, and runs the pin suite against
+that build in a subprocess: the suite has to fail.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+from conftest import ROOT
+
+SRC = os.path.join(ROOT, "oracle", "moe_oracle.c")
+
+# (name, exact text in the oracle, replacement)
+MUTANTS = [
+    ("silu_sign", "h = g[j] / (1.0 + exp(-g[j])) * u[j]", "h = g[j] / (1.0 + exp(g[j])) * u[j]"),
+    ("drop_up", "h = g[j] / (1.0 + exp(-g[j])) * u[j]", "h = g[j] / (1.0 + exp(-g[j]))"),
+    ("down_transposed", "elem(c->Wd, c->dtype, (size_t)j * c->d + q)",
+     "elem(c->Wd, c->dtype, (size_t)q * c->f + j)"),
+    ("gate_up_swapped", "g[j] += xi * elem(c->Wg", "g[j] += xi * elem(c->Wu"),
+    ("router_transposed", "elem(c->Wg, c->dtype, (size_t)i * c->N + e)",
+     "elem(c->Wg, c->dtype, (size_t)e * c->d + i)"),
+    ("router_no_bias", "if (c->bias) acc += (double)c->bias[e];", ""),
+    ("tie_break_reversed", "  return a < b;", "  return a > b;"),
+    ("nan_ranks_high", "isnan(v) ? -INFINITY : v", "isnan(v) ? INFINITY : v"),
+    ("softmax_wrong_index", "topk_w[(size_t)t * k + j] = exp(l[topk_idx[(size_t)t * k + j]] - lmax) / denom",
+     "topk_w[(size_t)t * k + j] = exp(l[j] - lmax) / denom"),
+    ("softmax_unnormalised", "- lmax) / denom;", "- lmax);"),
+    ("capacity_off_by_one", "capacity > 0 && rank >= capacity", "capacity > 0 && rank > capacity"),
+    ("capacity_floor", "return (int)ceil(cf", "return (int)floor(cf"),
+    ("combine_keeps_dropped", "if (inv_pos_rows[(size_t)r * k + j] < 0) continue; /* dropped slot */", ""),
+    ("combine_no_shared", "yr[q] += shared[(size_t)r * d + q];", ";"),
+    ("combine_unweighted", "yr[q] += w * o[q];", "yr[q] += o[q];"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
+    mut = src.replace(old, new)
+    csrc = tmp_path / "mut.c"
+    csrc.write_text(mut)
+    lib = tmp_path / "libmut.so"
+    subprocess.run(["gcc", "-O2", "-fPIC", "-shared", "-pthread", "-o", str(lib), str(csrc),
+                    "-lm"], check=True)
+    env = dict(os.environ, MOE_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle.py")],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"planted mistake '{name}' went unnoticed by the pins"
