@@ -1,0 +1,206 @@
+/*
+ * moe.h -- C ABI of libmoe.so: the forward pass of one sparse
+ * Mixture-of-Experts (MoE) layer on one NVIDIA B300 (sm_103a).
+ *
+ * The layer, per token t with hidden state x[t] (row of x[T,d]):
+ *   1. router logits   l[e] = x[t] . W_g[:,e] + b[e]          (e < N)
+ *   2. top-k           the k largest logits, descending, equal logits ->
+ *                      lower expert id; NaN ranks below every number
+ *   3. gate weights    w_j = softmax over the k selected logits
+ *   4. dispatch        tokens regrouped by expert, stable by token index,
+ *                      optionally capped at C rows per expert
+ *   5. expert FFN      SwiGLU: o = (SiLU(x W_gate[e]) * (x W_up[e])) W_down[e]
+ *   6. combine         y[t] = sum over kept slots j of w_j * o_j
+ *                      (+ the always-on shared expert's output, weight 1)
+ *
+ * Sources, by page title and section:
+ *   steps 1-3: "MoE 分片：混合專家模型的平行化策略", section 動態 token 路由,
+ *              steps 2 and 6; "MoE 推理：激活参数 vs 总参数与专家路由",
+ *              sections 深入原理 and 代码; "大模型MoE混合专家架构原理与
+ *              DeepSeek-V4工程实践解析", section MoE核心机制.
+ *   step 4:    "MoE稀疏激活原理与工程实践", 3.1 (token-level batching: regroup
+ *              a batch's tokens by target expert id) and 2.2 (expert capacity).
+ *   step 5:    "MoE 分片", section 什麼是 MoE 模型 (an expert is two linear
+ *              maps with an activation between) and step 4; the SwiGLU form
+ *              (gate, up, SiLU, down) is this library's reading.
+ *   step 6:    "MoE 分片", step 6; "MoE 架构科普", section 专家粒度 (shared
+ *              experts every token passes through).
+ *
+ * Conventions for every entry point:
+ *   - All pointers to tensors are DEVICE pointers unless the name says host.
+ *     Every tensor is row-major and contiguous; base addresses are 16-byte
+ *     aligned; d and f (and fs) are multiples of 8.  The caller owns every
+ *     buffer, including the workspace; the library allocates no device memory
+ *     and keeps no per-call state.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Every call only enqueues work on it; none synchronises the host, and
+ *     none reads device results back to the host.
+ *   - Argument errors are found on the host and returned synchronously with
+ *     nothing enqueued.  A failed kernel launch returns MOE_ERR_CUDA.
+ *   - Errors found on the device (bad expert ids, NaN logits, a bounded wait
+ *     that gave up) are OR-ed as MOE_DEV_* bits into *device_status when that
+ *     pointer is non-NULL; the affected rows are skipped.  The caller reads it
+ *     after synchronising.  No kernel traps, asserts or waits without bound.
+ *   - moe_last_error() gives a one-line description of the last failure on
+ *     the calling host thread.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* a size, pointer or alignment the call rejects   */
+  MOE_ERR_UNSUPPORTED = 2, /* valid, but outside what the kernels implement   */
+  MOE_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than *_workspace_size */
+  MOE_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed     */
+  MOE_ERR_DEVICE = 5       /* no usable CUDA device / wrong architecture      */
+} moe_status_t;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+
+/* Bits OR-ed into *device_status by the kernels. */
+#define MOE_DEV_BAD_EXPERT_ID 0x1 /* an expert id outside [0,N) reached moe_permute */
+#define MOE_DEV_NAN_LOGIT 0x2     /* a router logit was NaN (ranked last)           */
+#define MOE_DEV_TIMEOUT 0x4       /* a bounded on-chip wait gave up; output invalid */
+#define MOE_DEV_BAD_TILE 0x8      /* grouped-GEMM tile outside the expert layout     */
+
+const char *moe_status_string(moe_status_t s);
+const char *moe_last_error(void);
+/* Library version, e.g. "moe63 1.0 sm_103a". */
+const char *moe_version(void);
+/* Kernel launches this process has enqueued through the library so far
+ * (all entry points, all threads); for counting launches per call. */
+uint64_t moe_launch_counter(void);
+
+/* Capacity in rows per expert for a capacity factor: ceil(cf * T * k / N),
+ * computed in double precision; 0 (no limit) when cf <= 0.  Capacity reading:
+ * "MoE稀疏激活原理与工程实践", 2.2 -- the page caps each expert's queue but
+ * gives no formula; C = factor x the even-split load is this library's. */
+int moe_capacity(float capacity_factor, int T, int k, int N);
+
+/* ---------------------------------------------------------------------------
+ * Step 1-3: router GEMM, top-k and softmax over the selected k.
+ *   x [T,d] (dtype), W_g [d,N] (dtype), bias [N] fp32 or NULL.
+ *   logits [T,N] fp32 output, or NULL to skip writing it.
+ *   topk_idx [T,k] int32, topk_w [T,k] fp32 outputs (slot order = rank order).
+ * Requires 1 <= k <= N <= 256, k <= 32, T >= 0, d >= 8, d % 8 == 0.
+ * fp32 accumulation; the softmax is exp(l_j - l_0) / sum_j' exp(l_j' - l_0).
+ * ------------------------------------------------------------------------- */
+moe_status_t moe_router_topk(const void *x, const void *W_g, const float *bias,
+                             moe_dtype_t dtype, int T, int d, int N, int k,
+                             float *logits, int32_t *topk_idx, float *topk_w,
+                             int32_t *device_status, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Step 4: dispatch.  Regroups the T*k assignments by expert, stable by token
+ * index, and gathers the token rows.
+ *   topk_idx [T,k] int32; topk_w [T,k] fp32 or NULL (then row_scale unused).
+ *   capacity: rows kept per expert (0 = no limit); an assignment is kept iff
+ *   its 0-based rank among its expert's assignments, by token index, is below
+ *   the capacity.
+ * Outputs (device):
+ *   counts [N]      assignments routed to each expert, before capacity
+ *   offsets [N+1]   exclusive prefix sum of KEPT rows; offsets[N] = kept total A
+ *   perm_token [T*k] token of row p (p < A)
+ *   row_scale [T*k] gate weight of row p, or NULL
+ *   inv_pos [T,k]   row p of assignment (t,j), -1 if dropped
+ *   x_perm [T*k,d]  x[perm_token[p]] for p < A (dtype), or NULL to skip
+ *   dropped         scalar int32: assignments dropped, or NULL
+ * An expert id outside [0,N) sets MOE_DEV_BAD_EXPERT_ID and that assignment
+ * is treated as dropped.  Workspace: moe_permute_workspace_size(T, N, k).
+ * ------------------------------------------------------------------------- */
+size_t moe_permute_workspace_size(int T, int N, int k);
+moe_status_t moe_permute(const int32_t *topk_idx, const float *topk_w,
+                         const void *x, moe_dtype_t dtype, int T, int d, int N,
+                         int k, int capacity, int32_t *counts, int32_t *offsets,
+                         int32_t *perm_token, float *row_scale,
+                         int32_t *inv_pos, void *x_perm, int32_t *dropped,
+                         int32_t *device_status, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Step 5: grouped expert FFN (SwiGLU) over permuted rows.
+ *   x_perm [A_max,d] (dtype): rows of expert e are offsets[e]..offsets[e+1]-1.
+ *   offsets [N+1] device int32 (from moe_permute); offsets[N] <= A_max.
+ *   row_scale [A_max] fp32 or NULL: each output row is multiplied by it.
+ *   W_gate, W_up [N,d,f]; W_down [N,f,d] (dtype).
+ *   y_perm [A_max,d] (dtype) output: row_scale[p] * SwiGLU_e(x_perm[p]).
+ * bf16 runs on tcgen05 tensor cores (fp32 accumulation in tensor memory; the
+ * hidden activation h is rounded to bf16 between the two GEMMs); fp32 runs
+ * on the CUDA cores in fp32.  Workspace: moe_expert_ffn_workspace_size().
+ * ------------------------------------------------------------------------- */
+size_t moe_expert_ffn_workspace_size(int A_max, int d, int f, int N,
+                                     moe_dtype_t dtype);
+moe_status_t moe_expert_ffn(const void *x_perm, const int32_t *offsets,
+                            const float *row_scale, int A_max, int d, int f,
+                            int N, moe_dtype_t dtype, const void *W_gate,
+                            const void *W_up, const void *W_down, void *y_perm,
+                            int32_t *device_status, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Step 6: combine.  y[t] = sum_{j<k, inv_pos[t,j] >= 0} y_perm[inv_pos[t,j]]
+ *                          (+ shared_y[t]), summed in fp32 in that order.
+ *   y_perm [*,d] and shared_y [T,d] (NULL = none) in y_perm_dtype;
+ *   y [T,d] in y_dtype (fp32 or bf16, rounded once at the end).
+ * ------------------------------------------------------------------------- */
+moe_status_t moe_combine(const void *y_perm, moe_dtype_t y_perm_dtype,
+                         const int32_t *inv_pos, int T, int k, int d,
+                         const void *shared_y, void *y, moe_dtype_t y_dtype,
+                         void *stream);
+
+/* ---------------------------------------------------------------------------
+ * The whole layer in one call: steps 1-6 plus the optional shared expert.
+ * Optional outputs may be NULL (then workspace holds them).
+ * ------------------------------------------------------------------------- */
+typedef struct moe_forward_args {
+  int T, d, f, N, k;
+  moe_dtype_t dtype;          /* x and every weight                          */
+  const void *x;              /* [T,d]                                       */
+  const void *W_g;            /* [d,N]                                       */
+  const float *router_bias;   /* [N] fp32, or NULL                           */
+  const void *W_gate;         /* [N,d,f]                                     */
+  const void *W_up;           /* [N,d,f]                                     */
+  const void *W_down;         /* [N,f,d]                                     */
+  int fs;                     /* shared-expert hidden dim, 0 = no shared     */
+  const void *Ws_gate;        /* [d,fs]                                      */
+  const void *Ws_up;          /* [d,fs]                                      */
+  const void *Ws_down;        /* [fs,d]                                      */
+  float capacity_factor;      /* <= 0: no capacity limit                     */
+  void *y;                    /* [T,d] output                                */
+  moe_dtype_t y_dtype;        /* MOE_F32 (default) or MOE_BF16               */
+  float *logits;              /* [T,N] optional output                       */
+  int32_t *topk_idx;          /* [T,k] optional output                       */
+  float *topk_w;              /* [T,k] optional output                       */
+  int32_t *counts;            /* [N]   optional output                       */
+  int32_t *offsets;           /* [N+1] optional output                       */
+  int32_t *inv_pos;           /* [T,k] optional output                       */
+  int32_t *dropped;           /* scalar optional output                      */
+  int32_t *device_status;     /* scalar, OR-ed MOE_DEV_* bits, optional      */
+} moe_forward_args;
+
+size_t moe_forward_workspace_size(const moe_forward_args *args);
+moe_status_t moe_forward(const moe_forward_args *args, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
+/* The same call with x read from, and y written to, HOST memory: enqueues
+ * the host->device copy of x_host into args->x, the layer, and the
+ * device->host copy of args->y into y_host on `stream`.  args->x and args->y
+ * are the device staging buffers.  Pinned host memory makes the copies
+ * asynchronous; the caller synchronises the stream before reading y_host. */
+moe_status_t moe_forward_host_io(const moe_forward_args *args,
+                                 const void *x_host, void *y_host,
+                                 void *workspace, size_t workspace_bytes,
+                                 void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

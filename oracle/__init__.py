@@ -244,24 +244,32 @@ def forward_rows(x_rows, topk_idx_rows, topk_w_rows, inv_pos_rows, fetch_expert,
     tokens (routing and grouping already computed over ALL tokens, because
     capacity drops depend on every earlier token), fetch_expert(e) -> (W_gate_e,
     W_up_e, W_down_e) CPU tensors, shared = None or (Ws_gate, Ws_up, Ws_down).
+    Experts are evaluated concurrently (each call releases the GIL).
     Returns y [R,d] fp64.
     """
+    import concurrent.futures as cf
     idx = _i32(topk_idx_rows)
     inv = _i32(inv_pos_rows)
     R, k = idx.shape
     d = x_rows.shape[1]
     out = np.zeros((R, k, d), dtype=np.float64)
-    for e in sorted(set(int(v) for v in idx.ravel())):
+    experts = sorted(set(int(v) for v in idx[inv >= 0].ravel()))
+    cores = nthreads or default_threads()
+    workers = max(1, min(cores, len(experts)))
+    per_call = max(1, cores // workers)
+
+    def run(e):
         rows, slots = np.nonzero((idx == e) & (inv >= 0))
-        if rows.size == 0:
-            continue
         wg, wu, wd = fetch_expert(e)
-        o = expert_rows(wg, wu, wd, x_rows[torch.as_tensor(rows, dtype=torch.long)],
-                        nthreads)
-        out[rows, slots] = o
+        o = expert_rows(wg, wu, wd, x_rows[torch.as_tensor(rows, dtype=torch.long)], per_call)
+        return rows, slots, o
+
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        for rows, slots, o in ex.map(run, experts):
+            out[rows, slots] = o
     sh = None
     if shared is not None:
-        sh = expert_rows(shared[0], shared[1], shared[2], x_rows, nthreads)
+        sh = expert_rows(shared[0], shared[1], shared[2], x_rows, cores)
     return combine_rows(inv, topk_w_rows, out, sh)
 
 

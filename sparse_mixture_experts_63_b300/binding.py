@@ -1,0 +1,295 @@
+"""ctypes binding to libmoe.so -- argument marshalling only.
+
+Every function here has the name of the C entry point it calls (see
+include/moe.h), takes torch CUDA tensors, passes their device addresses and
+sizes, and enqueues on torch's current CUDA stream.  No step of the layer runs
+in Python or on the CPU: if libmoe.so is missing or the device is not a
+B300, the calls raise.
+"""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+MOE_F32, MOE_BF16 = 0, 1
+MOE_DEV_BAD_EXPERT_ID, MOE_DEV_NAN_LOGIT, MOE_DEV_TIMEOUT, MOE_DEV_BAD_TILE = 1, 2, 4, 8
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+          3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE"}
+
+# Every symbol the header declares.
+EXPORTS = ("moe_status_string", "moe_last_error", "moe_version", "moe_launch_counter",
+           "moe_capacity",
+           "moe_router_topk", "moe_permute_workspace_size", "moe_permute",
+           "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
+           "moe_forward_workspace_size", "moe_forward", "moe_forward_host_io")
+
+
+class MoEError(RuntimeError):
+    def __init__(self, name, code, msg):
+        super().__init__(f"{name} -> {STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class moe_forward_args(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("d", ctypes.c_int), ("f", ctypes.c_int),
+                ("N", ctypes.c_int), ("k", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("x", ctypes.c_void_p), ("W_g", ctypes.c_void_p),
+                ("router_bias", ctypes.c_void_p), ("W_gate", ctypes.c_void_p),
+                ("W_up", ctypes.c_void_p), ("W_down", ctypes.c_void_p),
+                ("fs", ctypes.c_int), ("Ws_gate", ctypes.c_void_p),
+                ("Ws_up", ctypes.c_void_p), ("Ws_down", ctypes.c_void_p),
+                ("capacity_factor", ctypes.c_float), ("y", ctypes.c_void_p),
+                ("y_dtype", ctypes.c_int), ("logits", ctypes.c_void_p),
+                ("topk_idx", ctypes.c_void_p), ("topk_w", ctypes.c_void_p),
+                ("counts", ctypes.c_void_p), ("offsets", ctypes.c_void_p),
+                ("inv_pos", ctypes.c_void_p), ("dropped", ctypes.c_void_p),
+                ("device_status", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libmoe.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libmoe.so not built ({LIB_PATH}); run "
+                               "python -m sparse_mixture_experts_63_b300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, ci, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_status_string.argtypes = [ci]
+        L.moe_last_error.restype = ctypes.c_char_p
+        L.moe_version.restype = ctypes.c_char_p
+        L.moe_launch_counter.restype = ctypes.c_uint64
+        L.moe_capacity.argtypes = [ctypes.c_float, ci, ci, ci]
+        L.moe_capacity.restype = ci
+        L.moe_router_topk.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp]
+        L.moe_permute_workspace_size.argtypes = [ci, ci, ci]
+        L.moe_permute_workspace_size.restype = sz
+        L.moe_permute.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp,
+                                  vp, vp, vp, sz, vp]
+        L.moe_expert_ffn_workspace_size.argtypes = [ci, ci, ci, ci, ci]
+        L.moe_expert_ffn_workspace_size.restype = sz
+        L.moe_expert_ffn.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp,
+                                     sz, vp]
+        L.moe_combine.argtypes = [vp, ci, vp, ci, ci, ci, vp, vp, ci, vp]
+        L.moe_forward_workspace_size.argtypes = [ctypes.POINTER(moe_forward_args)]
+        L.moe_forward_workspace_size.restype = sz
+        L.moe_forward.argtypes = [ctypes.POINTER(moe_forward_args), vp, sz, vp]
+        L.moe_forward_host_io.argtypes = [ctypes.POINTER(moe_forward_args), vp, vp, vp, sz, vp]
+        for n in ("moe_router_topk", "moe_permute", "moe_expert_ffn", "moe_combine",
+                  "moe_forward", "moe_forward_host_io"):
+            getattr(L, n).restype = ci
+        _lib = L
+    return _lib
+
+
+def _check(name, code):
+    if code != 0:
+        raise MoEError(name, code, lib().moe_last_error().decode())
+
+
+def _p(t):
+    return None if t is None else t.data_ptr()
+
+
+def _dt(t):
+    if t.dtype == torch.bfloat16:
+        return MOE_BF16
+    if t.dtype == torch.float32:
+        return MOE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+# ---------------------------------------------------------------------------
+def moe_version() -> str:
+    return lib().moe_version().decode()
+
+
+def moe_launch_counter() -> int:
+    return int(lib().moe_launch_counter())
+
+
+def moe_capacity(capacity_factor, T, k, N) -> int:
+    return int(lib().moe_capacity(float(capacity_factor), T, k, N))
+
+
+def moe_router_topk(x, W_g, k, bias=None, logits=None, topk_idx=None, topk_w=None,
+                    device_status=None, stream=None):
+    """Returns (topk_idx [T,k] int32, topk_w [T,k] fp32); fills logits if given."""
+    _cuda(x, W_g, bias, logits)
+    T, d = x.shape
+    N = W_g.shape[1]
+    if topk_idx is None:
+        topk_idx = torch.empty((T, k), dtype=torch.int32, device=x.device)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=x.device)
+    _check("moe_router_topk", lib().moe_router_topk(
+        _p(x), _p(W_g), _p(bias), _dt(x), T, d, N, k, _p(logits), _p(topk_idx), _p(topk_w),
+        _p(device_status), _stream(stream)))
+    return topk_idx, topk_w
+
+
+def moe_permute(topk_idx, N, x=None, topk_w=None, capacity=0, gather=True,
+                device_status=None, stream=None, A_max=None):
+    """Returns dict counts, offsets, perm_token, row_scale, inv_pos, x_perm, dropped."""
+    _cuda(topk_idx, x, topk_w)
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    d = x.shape[1] if x is not None else 0
+    A = T * k if A_max is None else A_max
+    out = dict(counts=torch.empty(N, dtype=torch.int32, device=dev),
+               offsets=torch.empty(N + 1, dtype=torch.int32, device=dev),
+               perm_token=torch.empty(max(T * k, 1), dtype=torch.int32, device=dev),
+               row_scale=(torch.empty(max(T * k, 1), dtype=torch.float32, device=dev)
+                          if topk_w is not None else None),
+               inv_pos=torch.empty((T, k), dtype=torch.int32, device=dev),
+               x_perm=(torch.empty((max(A, 1), d), dtype=x.dtype, device=dev)
+                       if (gather and x is not None) else None),
+               dropped=torch.zeros(1, dtype=torch.int32, device=dev))
+    ws_bytes = lib().moe_permute_workspace_size(T, N, k)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    _check("moe_permute", lib().moe_permute(
+        _p(topk_idx), _p(topk_w), _p(x), _dt(x) if x is not None else MOE_BF16, T, d, N, k,
+        int(capacity), _p(out["counts"]), _p(out["offsets"]), _p(out["perm_token"]),
+        _p(out["row_scale"]), _p(out["inv_pos"]), _p(out["x_perm"]), _p(out["dropped"]),
+        _p(device_status), _p(ws), ws_bytes, _stream(stream)))
+    return out
+
+
+def moe_expert_ffn(x_perm, offsets, W_gate, W_up, W_down, row_scale=None, y_perm=None,
+                   device_status=None, stream=None, A_max=None):
+    """y_perm [A_max,d] = row_scale * SwiGLU_e(x_perm) for each expert's rows."""
+    _cuda(x_perm, offsets, W_gate, W_up, W_down, row_scale, y_perm)
+    A = x_perm.shape[0] if A_max is None else A_max
+    d = x_perm.shape[1]
+    N, _, f = W_gate.shape
+    if y_perm is None:
+        y_perm = torch.empty((max(A, 1), d), dtype=x_perm.dtype, device=x_perm.device)
+    ws_bytes = lib().moe_expert_ffn_workspace_size(A, d, f, N, _dt(x_perm))
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=x_perm.device)
+    _check("moe_expert_ffn", lib().moe_expert_ffn(
+        _p(x_perm), _p(offsets), _p(row_scale), A, d, f, N, _dt(x_perm), _p(W_gate),
+        _p(W_up), _p(W_down), _p(y_perm), _p(device_status), _p(ws), ws_bytes,
+        _stream(stream)))
+    return y_perm
+
+
+def moe_combine(y_perm, inv_pos, shared_y=None, y=None, y_dtype=torch.float32, stream=None):
+    _cuda(y_perm, inv_pos, shared_y, y)
+    T, k = inv_pos.shape
+    d = y_perm.shape[1]
+    if y is None:
+        y = torch.empty((T, d), dtype=y_dtype, device=y_perm.device)
+    _check("moe_combine", lib().moe_combine(
+        _p(y_perm), _dt(y_perm), _p(inv_pos), T, k, d, _p(shared_y), _p(y), _dt(y),
+        _stream(stream)))
+    return y
+
+
+def make_forward_args(x, W_g, W_gate, W_up, W_down, k, y, bias=None, Ws_gate=None,
+                      Ws_up=None, Ws_down=None, capacity_factor=0.0, outputs=None,
+                      device_status=None):
+    _cuda(x, W_g, W_gate, W_up, W_down, y, bias, Ws_gate, Ws_up, Ws_down)
+    T, d = x.shape
+    N, _, f = W_gate.shape
+    o = outputs or {}
+    a = moe_forward_args()
+    a.T, a.d, a.f, a.N, a.k, a.dtype = T, d, f, N, k, _dt(x)
+    a.x, a.W_g, a.router_bias = _p(x), _p(W_g), _p(bias)
+    a.W_gate, a.W_up, a.W_down = _p(W_gate), _p(W_up), _p(W_down)
+    a.fs = 0 if Ws_gate is None else Ws_gate.shape[1]
+    a.Ws_gate, a.Ws_up, a.Ws_down = _p(Ws_gate), _p(Ws_up), _p(Ws_down)
+    a.capacity_factor = float(capacity_factor)
+    a.y, a.y_dtype = _p(y), _dt(y)
+    for key in ("logits", "topk_idx", "topk_w", "counts", "offsets", "inv_pos", "dropped"):
+        setattr(a, key, _p(o.get(key)))
+    a.device_status = _p(device_status)
+    return a
+
+
+def moe_forward_workspace_size(args) -> int:
+    n = lib().moe_forward_workspace_size(ctypes.byref(args))
+    if n == 0:
+        raise MoEError("moe_forward_workspace_size", 1, lib().moe_last_error().decode())
+    return n
+
+
+def moe_forward(args, workspace, stream=None):
+    _check("moe_forward", lib().moe_forward(ctypes.byref(args), _p(workspace),
+                                            workspace.numel(), _stream(stream)))
+
+
+def moe_forward_host_io(args, x_host, y_host, workspace, stream=None):
+    if x_host.is_cuda or y_host.is_cuda:
+        raise ValueError("x_host / y_host must be host tensors")
+    _check("moe_forward_host_io", lib().moe_forward_host_io(
+        ctypes.byref(args), _p(x_host), _p(y_host), _p(workspace), workspace.numel(),
+        _stream(stream)))
+
+
+class MoELayer:
+    """Convenience holder: the layer's weights plus a reusable workspace.
+
+    ``layer(x)`` returns y [T,d] (fp32 by default) and keeps the routing
+    outputs of the last call in ``layer.last``.
+    """
+
+    def __init__(self, W_g, W_gate, W_up, W_down, k, bias=None, Ws_gate=None, Ws_up=None,
+                 Ws_down=None, capacity_factor=0.0, y_dtype=torch.float32):
+        self.W_g, self.W_gate, self.W_up, self.W_down = W_g, W_gate, W_up, W_down
+        self.k, self.bias, self.cf, self.y_dtype = k, bias, capacity_factor, y_dtype
+        self.Ws_gate, self.Ws_up, self.Ws_down = Ws_gate, Ws_up, Ws_down
+        self._ws = None
+        self.last = None
+
+    def outputs_for(self, T, device, logits=False):
+        N = self.W_gate.shape[0]
+        k = self.k
+        o = dict(topk_idx=torch.empty((T, k), dtype=torch.int32, device=device),
+                 topk_w=torch.empty((T, k), dtype=torch.float32, device=device),
+                 counts=torch.empty(N, dtype=torch.int32, device=device),
+                 offsets=torch.empty(N + 1, dtype=torch.int32, device=device),
+                 inv_pos=torch.empty((T, k), dtype=torch.int32, device=device),
+                 dropped=torch.zeros(1, dtype=torch.int32, device=device),
+                 device_status=torch.zeros(1, dtype=torch.int32, device=device))
+        if logits:
+            o["logits"] = torch.empty((T, N), dtype=torch.float32, device=device)
+        return o
+
+    def args(self, x, y, outputs):
+        return make_forward_args(x, self.W_g, self.W_gate, self.W_up, self.W_down, self.k, y,
+                                 bias=self.bias, Ws_gate=self.Ws_gate, Ws_up=self.Ws_up,
+                                 Ws_down=self.Ws_down, capacity_factor=self.cf,
+                                 outputs=outputs, device_status=outputs.get("device_status"))
+
+    def workspace(self, args, device):
+        n = moe_forward_workspace_size(args)
+        if self._ws is None or self._ws.numel() < n:
+            self._ws = torch.empty(n, dtype=torch.uint8, device=device)
+        return self._ws
+
+    def __call__(self, x, logits=False, stream=None):
+        T, d = x.shape
+        y = torch.empty((T, d), dtype=self.y_dtype, device=x.device)
+        o = self.outputs_for(T, x.device, logits)
+        a = self.args(x, y, o)
+        moe_forward(a, self.workspace(a, x.device), stream)
+        self.last = o
+        return y

@@ -1,0 +1,374 @@
+// libmoe.so entry points: argument checks, workspace layout and launch order.
+// Every compute step runs in the kernels of the other translation units; this
+// file only validates, carves the caller's workspace and enqueues launches.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+static thread_local char g_err[512] = "";
+static std::atomic<uint64_t> g_launches{0};
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+void set_error(const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+}
+
+namespace {
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t esize(moe_dtype_t t) { return t == MOE_BF16 ? 2 : 4; }
+inline bool dtype_ok(moe_dtype_t t) { return t == MOE_F32 || t == MOE_BF16; }
+
+#define CHECK_ARG(cond, ...)              \
+  do {                                    \
+    if (!(cond)) {                        \
+      ::moe::set_error(__VA_ARGS__);      \
+      return MOE_ERR_INVALID_ARG;         \
+    }                                     \
+  } while (0)
+
+// The kernels are built for sm_103a only.
+moe_status_t check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    set_error("no CUDA device");
+    return MOE_ERR_DEVICE;
+  }
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) {
+    set_error("device %d is sm_%d%d; libmoe is built for sm_103a (B300) only", dev, major,
+              minor);
+    return MOE_ERR_DEVICE;
+  }
+  return MOE_OK;
+}
+
+// Sub-allocator over the caller's workspace (256-byte aligned slices).
+struct Carve {
+  char *base;
+  size_t used = 0;
+  explicit Carve(void *b) : base(static_cast<char *>(b)) {}
+  template <typename T>
+  T *take(size_t count) {
+    size_t off = used;
+    used = align_up(used + count * sizeof(T), 256);
+    return base ? reinterpret_cast<T *>(base + off) : nullptr;
+  }
+  void *take_bytes(size_t bytes) {
+    size_t off = used;
+    used = align_up(used + bytes, 256);
+    return base ? base + off : nullptr;
+  }
+};
+
+__global__ void set_shared_offsets(int32_t *off, int T) {
+  off[0] = 0;
+  off[1] = T;
+}
+
+long routed_rows_max(int T, int N, int k, int capacity) {
+  long a = (long)T * k;
+  if (capacity > 0 && (long)N * capacity < a) a = (long)N * capacity;
+  return a;
+}
+
+struct ForwardLayout {
+  int32_t *topk_idx, *counts, *offsets, *inv_pos, *perm_token, *dropped, *sh_offsets;
+  float *topk_w, *row_scale;
+  void *x_perm, *y_perm, *ffn_ws, *perm_ws, *ys, *sh_ffn_ws;
+  size_t bytes;
+};
+
+ForwardLayout layout_forward(const moe_forward_args *a, void *ws) {
+  ForwardLayout L{};
+  Carve c(ws);
+  const int cap = moe_capacity(a->capacity_factor, a->T, a->k, a->N);
+  const long A_max = routed_rows_max(a->T, a->N, a->k, cap);
+  const size_t tk = (size_t)a->T * a->k;
+  const size_t es = esize(a->dtype);
+  L.topk_idx = a->topk_idx ? a->topk_idx : c.take<int32_t>(tk);
+  L.topk_w = a->topk_w ? a->topk_w : c.take<float>(tk);
+  L.counts = a->counts ? a->counts : c.take<int32_t>(a->N);
+  L.offsets = a->offsets ? a->offsets : c.take<int32_t>(a->N + 1);
+  L.inv_pos = a->inv_pos ? a->inv_pos : c.take<int32_t>(tk);
+  L.dropped = a->dropped ? a->dropped : c.take<int32_t>(1);
+  L.perm_token = c.take<int32_t>(tk);
+  L.row_scale = c.take<float>(tk);
+  L.x_perm = c.take_bytes((size_t)A_max * a->d * es);
+  L.y_perm = c.take_bytes((size_t)A_max * a->d * es);
+  L.ffn_ws = c.take_bytes(ffn_workspace_bytes((int)A_max, a->d, a->f, a->N, a->dtype));
+  L.perm_ws = c.take_bytes(permute_workspace_bytes(a->T, a->N, a->k));
+  if (a->fs > 0) {
+    L.sh_offsets = c.take<int32_t>(2);
+    L.ys = c.take_bytes((size_t)a->T * a->d * es);
+    L.sh_ffn_ws = c.take_bytes(ffn_workspace_bytes(a->T, a->d, a->fs, 1, a->dtype));
+  }
+  L.bytes = c.used;
+  return L;
+}
+
+moe_status_t validate_router(const void *x, const void *W_g, moe_dtype_t dtype, int T, int d,
+                             int N, int k, const int32_t *topk_idx, const float *topk_w) {
+  CHECK_ARG(dtype_ok(dtype), "dtype %d is not MOE_F32 or MOE_BF16", (int)dtype);
+  CHECK_ARG(T >= 0 && d >= 8 && N >= 1, "bad sizes T=%d d=%d N=%d", T, d, N);
+  CHECK_ARG(k >= 1 && k <= N, "k=%d must satisfy 1 <= k <= N=%d", k, N);
+  CHECK_ARG(d % 8 == 0, "d=%d must be a multiple of 8", d);
+  if (N > 256 || k > 32) {
+    set_error("router supports N <= 256 and k <= 32 (got N=%d k=%d)", N, k);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  CHECK_ARG(T == 0 || (x && W_g && topk_idx && topk_w), "required pointer is NULL");
+  CHECK_ARG(aligned16(x), "x must be 16-byte aligned");
+  return MOE_OK;
+}
+
+moe_status_t validate_ffn(const void *x_perm, const int32_t *offsets, int A_max, int d, int f,
+                          int N, moe_dtype_t dtype, const void *Wg, const void *Wu,
+                          const void *Wd, const void *y_perm) {
+  CHECK_ARG(dtype_ok(dtype), "dtype %d is not MOE_F32 or MOE_BF16", (int)dtype);
+  CHECK_ARG(A_max >= 0 && d >= 8 && f >= 8 && N >= 1, "bad sizes A_max=%d d=%d f=%d N=%d",
+            A_max, d, f, N);
+  CHECK_ARG(d % 8 == 0 && f % 8 == 0, "d=%d and f=%d must be multiples of 8", d, f);
+  CHECK_ARG(offsets && Wg && Wu && Wd, "required pointer is NULL");
+  CHECK_ARG(A_max == 0 || (x_perm && y_perm), "x_perm / y_perm is NULL");
+  CHECK_ARG(aligned16(x_perm) && aligned16(y_perm) && aligned16(Wg) && aligned16(Wu) &&
+                aligned16(Wd),
+            "tensors must be 16-byte aligned");
+  return MOE_OK;
+}
+
+}  // namespace
+
+size_t ffn_workspace_bytes(int A_max, int d, int f, int N, moe_dtype_t dtype) {
+  (void)d;
+  (void)N;
+  // h [A_max, f] in the layer dtype.
+  return align_up((size_t)A_max * f * esize(dtype), 256);
+}
+
+moe_status_t launch_expert_ffn(const void *x_perm, const int32_t *offsets, const float *row_scale,
+                               int A_max, int d, int f, int N, moe_dtype_t dtype,
+                               const void *W_gate, const void *W_up, const void *W_down,
+                               void *y_perm, int32_t *device_status, void *workspace,
+                               cudaStream_t stream) {
+  void *h = workspace;
+  return launch_ffn_simt(x_perm, offsets, row_scale, A_max, d, f, N, dtype, W_gate, W_up,
+                         W_down, h, y_perm, device_status, stream);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char *moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE: return "unsupported or missing device";
+  }
+  return "unknown status";
+}
+
+const char *moe_last_error(void) { return g_err; }
+
+const char *moe_version(void) { return "moe63 1.0 sm_103a"; }
+
+uint64_t moe_launch_counter(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int moe_capacity(float capacity_factor, int T, int k, int N) {
+  if (!(capacity_factor > 0.f) || N < 1) return 0;
+  return (int)ceil((double)capacity_factor * (double)T * (double)k / (double)N);
+}
+
+moe_status_t moe_router_topk(const void *x, const void *W_g, const float *bias,
+                             moe_dtype_t dtype, int T, int d, int N, int k, float *logits,
+                             int32_t *topk_idx, float *topk_w, int32_t *device_status,
+                             void *stream) {
+  moe_status_t s = validate_router(x, W_g, dtype, T, d, N, k, topk_idx, topk_w);
+  if (s != MOE_OK) return s;
+  if ((s = check_device()) != MOE_OK) return s;
+  return launch_router_topk(x, W_g, bias, dtype, T, d, N, k, logits, topk_idx, topk_w,
+                            device_status, static_cast<cudaStream_t>(stream));
+}
+
+size_t moe_permute_workspace_size(int T, int N, int k) {
+  if (T < 0 || N < 1 || k < 1) return 0;
+  return permute_workspace_bytes(T, N, k);
+}
+
+moe_status_t moe_permute(const int32_t *topk_idx, const float *topk_w, const void *x,
+                         moe_dtype_t dtype, int T, int d, int N, int k, int capacity,
+                         int32_t *counts, int32_t *offsets, int32_t *perm_token,
+                         float *row_scale, int32_t *inv_pos, void *x_perm, int32_t *dropped,
+                         int32_t *device_status, void *workspace, size_t workspace_bytes,
+                         void *stream) {
+  CHECK_ARG(dtype_ok(dtype), "dtype %d is not MOE_F32 or MOE_BF16", (int)dtype);
+  CHECK_ARG(T >= 0 && N >= 1 && k >= 1 && k <= N && capacity >= 0,
+            "bad sizes T=%d N=%d k=%d capacity=%d", T, N, k, capacity);
+  CHECK_ARG(counts && offsets && perm_token && inv_pos && (T == 0 || topk_idx),
+            "required pointer is NULL");
+  CHECK_ARG(!row_scale || topk_w, "row_scale needs topk_w");
+  if (x_perm) {
+    CHECK_ARG(x && d >= 8 && d % 8 == 0, "x_perm needs x and d %% 8 == 0 (d=%d)", d);
+    CHECK_ARG(aligned16(x) && aligned16(x_perm), "x / x_perm must be 16-byte aligned");
+  }
+  if (N > 1024) {
+    set_error("moe_permute supports N <= 1024");
+    return MOE_ERR_UNSUPPORTED;
+  }
+  size_t need = permute_workspace_bytes(T, N, k);
+  if (need > 0 && (!workspace || workspace_bytes < need)) {
+    set_error("moe_permute: workspace %zu bytes, needs %zu", workspace_bytes, need);
+    return MOE_ERR_WORKSPACE;
+  }
+  moe_status_t s = check_device();
+  if (s != MOE_OK) return s;
+  return launch_permute(topk_idx, topk_w, x, dtype, T, d, N, k, capacity, counts, offsets,
+                        perm_token, row_scale, inv_pos, x_perm, dropped, device_status,
+                        workspace, static_cast<cudaStream_t>(stream));
+}
+
+size_t moe_expert_ffn_workspace_size(int A_max, int d, int f, int N, moe_dtype_t dtype) {
+  if (A_max < 0 || d < 1 || f < 1 || N < 1 || !dtype_ok(dtype)) return 0;
+  return ffn_workspace_bytes(A_max, d, f, N, dtype);
+}
+
+moe_status_t moe_expert_ffn(const void *x_perm, const int32_t *offsets, const float *row_scale,
+                            int A_max, int d, int f, int N, moe_dtype_t dtype,
+                            const void *W_gate, const void *W_up, const void *W_down,
+                            void *y_perm, int32_t *device_status, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+  moe_status_t s = validate_ffn(x_perm, offsets, A_max, d, f, N, dtype, W_gate, W_up, W_down,
+                                y_perm);
+  if (s != MOE_OK) return s;
+  size_t need = ffn_workspace_bytes(A_max, d, f, N, dtype);
+  if (need > 0 && (!workspace || workspace_bytes < need)) {
+    set_error("moe_expert_ffn: workspace %zu bytes, needs %zu", workspace_bytes, need);
+    return MOE_ERR_WORKSPACE;
+  }
+  if ((s = check_device()) != MOE_OK) return s;
+  return launch_expert_ffn(x_perm, offsets, row_scale, A_max, d, f, N, dtype, W_gate, W_up,
+                           W_down, y_perm, device_status, workspace,
+                           static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_combine(const void *y_perm, moe_dtype_t y_perm_dtype, const int32_t *inv_pos,
+                         int T, int k, int d, const void *shared_y, void *y, moe_dtype_t y_dtype,
+                         void *stream) {
+  CHECK_ARG(dtype_ok(y_perm_dtype) && dtype_ok(y_dtype), "bad dtype");
+  CHECK_ARG(T >= 0 && k >= 1 && d >= 8 && d % 8 == 0, "bad sizes T=%d k=%d d=%d", T, k, d);
+  CHECK_ARG(T == 0 || (y_perm && inv_pos && y), "required pointer is NULL");
+  CHECK_ARG(aligned16(y_perm) && aligned16(shared_y) && aligned16(y),
+            "tensors must be 16-byte aligned");
+  moe_status_t s = check_device();
+  if (s != MOE_OK) return s;
+  return launch_combine(y_perm, y_perm_dtype, inv_pos, T, k, d, shared_y, y, y_dtype,
+                        static_cast<cudaStream_t>(stream));
+}
+
+static moe_status_t validate_forward(const moe_forward_args *a) {
+  CHECK_ARG(a, "args is NULL");
+  CHECK_ARG(dtype_ok(a->dtype) && dtype_ok(a->y_dtype), "bad dtype");
+  CHECK_ARG(a->T >= 1 && a->d >= 8 && a->f >= 8 && a->N >= 1, "bad sizes T=%d d=%d f=%d N=%d",
+            a->T, a->d, a->f, a->N);
+  CHECK_ARG(a->k >= 1 && a->k <= a->N, "k=%d must satisfy 1 <= k <= N=%d", a->k, a->N);
+  CHECK_ARG(a->d % 8 == 0 && a->f % 8 == 0, "d=%d and f=%d must be multiples of 8", a->d, a->f);
+  CHECK_ARG(a->fs >= 0 && a->fs % 8 == 0, "fs=%d must be a non-negative multiple of 8", a->fs);
+  CHECK_ARG(a->x && a->W_g && a->W_gate && a->W_up && a->W_down && a->y,
+            "required pointer is NULL");
+  CHECK_ARG(a->fs == 0 || (a->Ws_gate && a->Ws_up && a->Ws_down), "shared weights are NULL");
+  CHECK_ARG(aligned16(a->x) && aligned16(a->y) && aligned16(a->W_gate) && aligned16(a->W_up) &&
+                aligned16(a->W_down) && aligned16(a->Ws_gate) && aligned16(a->Ws_up) &&
+                aligned16(a->Ws_down),
+            "tensors must be 16-byte aligned");
+  CHECK_ARG((long)a->T * a->k < (1L << 31) - 1, "T*k too large");
+  if (a->N > 256 || a->k > 32) {
+    set_error("N <= 256 and k <= 32 are supported (got N=%d k=%d)", a->N, a->k);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+size_t moe_forward_workspace_size(const moe_forward_args *args) {
+  if (validate_forward(args) != MOE_OK) return 0;
+  return layout_forward(args, nullptr).bytes;
+}
+
+moe_status_t moe_forward(const moe_forward_args *a, void *workspace, size_t workspace_bytes,
+                         void *stream_) {
+  moe_status_t s = validate_forward(a);
+  if (s != MOE_OK) return s;
+  ForwardLayout need = layout_forward(a, nullptr);
+  if (!workspace || workspace_bytes < need.bytes) {
+    set_error("moe_forward: workspace %zu bytes, needs %zu", workspace_bytes, need.bytes);
+    return MOE_ERR_WORKSPACE;
+  }
+  if (!aligned16(workspace)) {
+    set_error("workspace must be 16-byte aligned");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if ((s = check_device()) != MOE_OK) return s;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  ForwardLayout L = layout_forward(a, workspace);
+  const int cap = moe_capacity(a->capacity_factor, a->T, a->k, a->N);
+  const int A_max = (int)routed_rows_max(a->T, a->N, a->k, cap);
+
+  s = launch_router_topk(a->x, a->W_g, a->router_bias, a->dtype, a->T, a->d, a->N, a->k,
+                         a->logits, L.topk_idx, L.topk_w, a->device_status, stream);
+  if (s != MOE_OK) return s;
+  s = launch_permute(L.topk_idx, L.topk_w, a->x, a->dtype, a->T, a->d, a->N, a->k, cap,
+                     L.counts, L.offsets, L.perm_token, L.row_scale, L.inv_pos, L.x_perm,
+                     L.dropped, a->device_status, L.perm_ws, stream);
+  if (s != MOE_OK) return s;
+  s = launch_expert_ffn(L.x_perm, L.offsets, L.row_scale, A_max, a->d, a->f, a->N, a->dtype,
+                        a->W_gate, a->W_up, a->W_down, L.y_perm, a->device_status, L.ffn_ws,
+                        stream);
+  if (s != MOE_OK) return s;
+  if (a->fs > 0) {
+    set_shared_offsets<<<1, 1, 0, stream>>>(L.sh_offsets, a->T);
+    MOE_LAUNCH_CHECK();
+    s = launch_expert_ffn(a->x, L.sh_offsets, nullptr, a->T, a->d, a->fs, 1, a->dtype,
+                          a->Ws_gate, a->Ws_up, a->Ws_down, L.ys, a->device_status,
+                          L.sh_ffn_ws, stream);
+    if (s != MOE_OK) return s;
+  }
+  return launch_combine(L.y_perm, a->dtype, L.inv_pos, a->T, a->k, a->d,
+                        a->fs > 0 ? L.ys : nullptr, a->y, a->y_dtype, stream);
+}
+
+moe_status_t moe_forward_host_io(const moe_forward_args *a, const void *x_host, void *y_host,
+                                 void *workspace, size_t workspace_bytes, void *stream_) {
+  moe_status_t s = validate_forward(a);
+  if (s != MOE_OK) return s;
+  CHECK_ARG(x_host && y_host, "host buffers are NULL");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const size_t xb = (size_t)a->T * a->d * esize(a->dtype);
+  const size_t yb = (size_t)a->T * a->d * esize(a->y_dtype);
+  MOE_CUDA_TRY(cudaMemcpyAsync(const_cast<void *>(a->x), x_host, xb, cudaMemcpyHostToDevice,
+                               stream));
+  s = moe_forward(a, workspace, workspace_bytes, stream_);
+  if (s != MOE_OK) return s;
+  MOE_CUDA_TRY(cudaMemcpyAsync(y_host, a->y, yb, cudaMemcpyDeviceToHost, stream));
+  return MOE_OK;
+}
+
+}  // extern "C"

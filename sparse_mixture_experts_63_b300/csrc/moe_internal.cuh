@@ -1,0 +1,104 @@
+// Internal declarations shared by the CUDA translation units of libmoe.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Records a one-line description of the last failure (thread-local).
+void set_error(const char *fmt, ...);
+// Counts one enqueued kernel launch (read by moe_launch_counter()).
+void count_launch();
+
+#define MOE_CUDA_TRY(expr)                                                     \
+  do {                                                                         \
+    cudaError_t err_ = (expr);                                                 \
+    if (err_ != cudaSuccess) {                                                 \
+      ::moe::set_error("%s: %s (%s:%d)", #expr, cudaGetErrorString(err_),      \
+                       __FILE__, __LINE__);                                    \
+      return MOE_ERR_CUDA;                                                     \
+    }                                                                          \
+  } while (0)
+
+#define MOE_LAUNCH_CHECK()                                                     \
+  do {                                                                         \
+    ::moe::count_launch();                                                     \
+    cudaError_t err_ = cudaGetLastError();                                     \
+    if (err_ != cudaSuccess) {                                                 \
+      ::moe::set_error("kernel launch: %s (%s:%d)", cudaGetErrorString(err_),  \
+                       __FILE__, __LINE__);                                    \
+      return MOE_ERR_CUDA;                                                     \
+    }                                                                          \
+  } while (0)
+
+// ---- element helpers --------------------------------------------------------
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// Loads 8 consecutive elements (16 B for bf16, 32 B for fp32) as fp32.
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8]) {
+  uint4 q = *reinterpret_cast<const uint4 *>(p);
+  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&q);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __bfloat1622float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
+  float4 a = *reinterpret_cast<const float4 *>(p);
+  float4 b = *reinterpret_cast<const float4 *>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+__device__ __forceinline__ void report(int32_t *status, int32_t bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// ---- launchers (each returns MOE_OK or an error; never synchronises) --------
+moe_status_t launch_router_topk(const void *x, const void *W_g, const float *bias,
+                                moe_dtype_t dtype, int T, int d, int N, int k,
+                                float *logits, int32_t *topk_idx, float *topk_w,
+                                int32_t *device_status, cudaStream_t stream);
+
+size_t permute_workspace_bytes(int T, int N, int k);
+moe_status_t launch_permute(const int32_t *topk_idx, const float *topk_w, const void *x,
+                            moe_dtype_t dtype, int T, int d, int N, int k, int capacity,
+                            int32_t *counts, int32_t *offsets, int32_t *perm_token,
+                            float *row_scale, int32_t *inv_pos, void *x_perm,
+                            int32_t *dropped, int32_t *device_status, void *workspace,
+                            cudaStream_t stream);
+
+size_t ffn_workspace_bytes(int A_max, int d, int f, int N, moe_dtype_t dtype);
+moe_status_t launch_expert_ffn(const void *x_perm, const int32_t *offsets,
+                               const float *row_scale, int A_max, int d, int f, int N,
+                               moe_dtype_t dtype, const void *W_gate, const void *W_up,
+                               const void *W_down, void *y_perm, int32_t *device_status,
+                               void *workspace, cudaStream_t stream);
+
+moe_status_t launch_combine(const void *y_perm, moe_dtype_t y_perm_dtype,
+                            const int32_t *inv_pos, int T, int k, int d,
+                            const void *shared_y, void *y, moe_dtype_t y_dtype,
+                            cudaStream_t stream);
+
+// fp32 SIMT grouped SwiGLU FFN (any dtype; the fp32 layer's path).
+moe_status_t launch_ffn_simt(const void *x_perm, const int32_t *offsets,
+                             const float *row_scale, int A_max, int d, int f, int N,
+                             moe_dtype_t dtype, const void *W_gate, const void *W_up,
+                             const void *W_down, void *h, void *y_perm,
+                             int32_t *device_status, cudaStream_t stream);
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace moe

@@ -1,0 +1,211 @@
+// Dispatch: regroup the T*k (token, slot) assignments by expert, stable by
+// token index, with an optional per-expert capacity, and gather the rows.
+//
+// Source: "MoE稀疏激活原理与工程实践", 3.1 (token-level batching: the batch's
+// tokens are regrouped by target expert id, {0:[t0,t1,t3], 1:[t2,t5], ...},
+// before each expert runs) and 2.2 (a per-expert queue with a hard capacity);
+// "MoE 分片：混合專家模型的平行化策略", section 動態 token 路由, step 3.
+//
+// Deterministic without inter-CTA waits, in four launches:
+//   1. hist:    CTA b counts its chunk's assignments per expert -> hist[b][e]
+//   2. scan:    one CTA: per expert, prefix over chunks (chunk_base[b][e]),
+//               counts[e], kept[e] = min(counts[e], C), offsets = exclusive
+//               scan of kept, dropped.
+//   3. scatter: CTA b re-reads its chunk; the rank of an assignment inside the
+//               chunk (stable by token) comes from warp match + per-warp counts;
+//               rank = chunk_base + in-chunk rank; kept iff rank < C.
+//   4. gather:  x_perm[p] = x[perm_token[p]], 16-byte vector copies.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kChunkTokens = 256;  // tokens per chunk (CTA) in hist / scatter
+constexpr int kThreads = 256;
+constexpr int kMaxN = 1024;
+
+__global__ void __launch_bounds__(kThreads) permute_hist(const int32_t *__restrict__ topk_idx,
+                                                         int T, int N, int k,
+                                                         int32_t *__restrict__ hist,
+                                                         int32_t *status) {
+  extern __shared__ int32_t sh_hist[];  // [N]
+  for (int e = threadIdx.x; e < N; e += blockDim.x) sh_hist[e] = 0;
+  __syncthreads();
+  const long a0 = (long)blockIdx.x * kChunkTokens * k;
+  const long a1 = min((long)T * k, a0 + (long)kChunkTokens * k);
+  bool bad = false;
+  for (long a = a0 + threadIdx.x; a < a1; a += blockDim.x) {
+    int e = topk_idx[a];
+    if (e >= 0 && e < N)
+      atomicAdd(&sh_hist[e], 1);
+    else
+      bad = true;
+  }
+  if (bad) report(status, MOE_DEV_BAD_EXPERT_ID);
+  __syncthreads();
+  for (int e = threadIdx.x; e < N; e += blockDim.x) hist[(size_t)blockIdx.x * N + e] = sh_hist[e];
+}
+
+// One CTA of kMaxN threads; thread e owns expert e.
+__global__ void __launch_bounds__(kMaxN) permute_scan(int32_t *__restrict__ hist, int nchunks,
+                                                      int T, int N, int k, int capacity,
+                                                      int32_t *__restrict__ counts,
+                                                      int32_t *__restrict__ offsets,
+                                                      int32_t *__restrict__ dropped) {
+  __shared__ int32_t warp_sums[kMaxN / 32];
+  const int e = threadIdx.x;
+  int32_t total = 0;
+  if (e < N) {
+    for (int b = 0; b < nchunks; ++b) {
+      int32_t c = hist[(size_t)b * N + e];
+      hist[(size_t)b * N + e] = total;  // becomes chunk_base[b][e]
+      total += c;
+    }
+    counts[e] = total;
+  }
+  int32_t kept = (e < N) ? ((capacity > 0 && total > capacity) ? capacity : total) : 0;
+  // Block-wide exclusive scan of kept.
+  const int lane = e % 32, w = e / 32;
+  int32_t incl = kept;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_sums[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int32_t s = warp_sums[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      int32_t o = __shfl_up_sync(0xffffffffu, s, off);
+      if (lane >= off) s += o;
+    }
+    warp_sums[lane] = s;  // inclusive over warps
+  }
+  __syncthreads();
+  int32_t excl = incl - kept + (w > 0 ? warp_sums[w - 1] : 0);
+  if (e < N) offsets[e] = excl;
+  if (e == N - 1) {
+    offsets[N] = excl + kept;
+    if (dropped) *dropped = (int32_t)((long)T * k - (excl + kept));
+  }
+}
+
+// CTA b: assignments of tokens [b*256, (b+1)*256).  Processed in rounds of
+// kThreads consecutive assignments (token-major, so order = token order).
+__global__ void __launch_bounds__(kThreads) permute_scatter(
+    const int32_t *__restrict__ topk_idx, const float *__restrict__ topk_w, int T, int N, int k,
+    int capacity, const int32_t *__restrict__ chunk_base, const int32_t *__restrict__ offsets,
+    int32_t *__restrict__ perm_token, float *__restrict__ row_scale, int32_t *__restrict__ inv_pos) {
+  extern __shared__ int32_t sm[];
+  int32_t *running = sm;                  // [N] rows of each expert seen in earlier rounds
+  int32_t *warp_cnt = sm + N;             // [8][N] per-warp counts of this round
+  constexpr int kWarps = kThreads / 32;
+  for (int e = threadIdx.x; e < N; e += blockDim.x) running[e] = 0;
+  const long a0 = (long)blockIdx.x * kChunkTokens * k;
+  const long a1 = min((long)T * k, a0 + (long)kChunkTokens * k);
+  const int lane = threadIdx.x % 32, w = threadIdx.x / 32;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (long base = a0; base < a1; base += kThreads) {
+    for (int q = threadIdx.x; q < kWarps * N; q += blockDim.x) warp_cnt[q] = 0;
+    __syncthreads();
+    const long a = base + threadIdx.x;
+    int e = (a < a1) ? topk_idx[a] : -1;
+    const bool valid = (e >= 0 && e < N);
+    const int key = valid ? e : -1 - (int)(threadIdx.x);  // invalid lanes match nobody
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    const int rank_in_warp = __popc(peers & lt_mask);
+    const bool last_of_group = (peers >> lane) == 1u;  // highest lane of its group
+    if (valid && last_of_group) warp_cnt[w * N + e] = rank_in_warp + 1;
+    __syncthreads();
+    if (valid) {
+      int32_t r = running[e] + rank_in_warp;
+      for (int w2 = 0; w2 < w; ++w2) r += warp_cnt[w2 * N + e];
+      r += chunk_base[(size_t)blockIdx.x * N + e];
+      if (capacity > 0 && r >= capacity) {
+        inv_pos[a] = -1;
+      } else {
+        int32_t p = offsets[e] + r;
+        inv_pos[a] = p;
+        perm_token[p] = (int32_t)(a / k);
+        if (row_scale) row_scale[p] = topk_w[a];
+      }
+    } else if (a < a1) {
+      inv_pos[a] = -1;
+    }
+    __syncthreads();
+    for (int q = threadIdx.x; q < N; q += blockDim.x) {
+      int32_t s = 0;
+      for (int w2 = 0; w2 < kWarps; ++w2) s += warp_cnt[w2 * N + q];
+      running[q] += s;
+    }
+    __syncthreads();
+  }
+}
+
+// One warp per row p < offsets[N]; grid-stride over rows.
+template <typename VecT>
+__global__ void __launch_bounds__(256) permute_gather(const VecT *__restrict__ x,
+                                                      const int32_t *__restrict__ perm_token,
+                                                      const int32_t *__restrict__ offsets, int N,
+                                                      int vecs_per_row, VecT *__restrict__ x_perm) {
+  const int A = offsets[N];
+  const int lane = threadIdx.x % 32;
+  const int warps = blockDim.x / 32;
+  for (int p = blockIdx.x * warps + threadIdx.x / 32; p < A; p += gridDim.x * warps) {
+    const VecT *src = x + (size_t)perm_token[p] * vecs_per_row;
+    VecT *dst = x_perm + (size_t)p * vecs_per_row;
+    for (int v = lane; v < vecs_per_row; v += 32) dst[v] = __ldg(src + v);
+  }
+}
+
+}  // namespace
+
+size_t permute_workspace_bytes(int T, int N, int k) {
+  (void)k;
+  size_t nchunks = (size_t)(T + kChunkTokens - 1) / kChunkTokens;
+  return align_up(nchunks * (size_t)N * sizeof(int32_t), 256);
+}
+
+moe_status_t launch_permute(const int32_t *topk_idx, const float *topk_w, const void *x,
+                            moe_dtype_t dtype, int T, int d, int N, int k, int capacity,
+                            int32_t *counts, int32_t *offsets, int32_t *perm_token,
+                            float *row_scale, int32_t *inv_pos, void *x_perm, int32_t *dropped,
+                            int32_t *device_status, void *workspace, cudaStream_t stream) {
+  if (N > kMaxN) {
+    set_error("moe_permute: N=%d above %d", N, kMaxN);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  int32_t *hist = static_cast<int32_t *>(workspace);
+  const int nchunks = (T + kChunkTokens - 1) / kChunkTokens;
+  if (nchunks > 0) {
+    permute_hist<<<nchunks, kThreads, N * sizeof(int32_t), stream>>>(topk_idx, T, N, k, hist,
+                                                                     device_status);
+    MOE_LAUNCH_CHECK();
+  }
+  permute_scan<<<1, kMaxN, 0, stream>>>(hist, nchunks, T, N, k, capacity, counts, offsets,
+                                        dropped);
+  MOE_LAUNCH_CHECK();
+  if (nchunks > 0) {
+    size_t smem = (size_t)N * (1 + kThreads / 32) * sizeof(int32_t);
+    permute_scatter<<<nchunks, kThreads, smem, stream>>>(topk_idx, topk_w, T, N, k, capacity,
+                                                         hist, offsets, perm_token, row_scale,
+                                                         inv_pos);
+    MOE_LAUNCH_CHECK();
+  }
+  if (x_perm && T > 0) {
+    const size_t row_bytes = (size_t)d * (dtype == MOE_BF16 ? 2 : 4);
+    const int vecs = (int)(row_bytes / 16);
+    long A_max = (long)T * k;
+    long grid = (A_max + 7) / 8;
+    if (grid > 148L * 16) grid = 148L * 16;
+    permute_gather<uint4><<<(int)grid, 256, 0, stream>>>(
+        static_cast<const uint4 *>(x), perm_token, offsets, N, vecs,
+        static_cast<uint4 *>(x_perm));
+    MOE_LAUNCH_CHECK();
+  }
+  return MOE_OK;
+}
+
+}  // namespace moe

@@ -1,0 +1,107 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point include/moe.h declares, and rejects bad arguments on the
+host with the documented status codes before touching any device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+from sparse_mixture_experts_63_b300 import binding as B
+from sparse_mixture_experts_63_b300 import build as build_mod
+import oracle
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.lib()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_what_binding_lists():
+    assert header_functions() == sorted(B.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version(lib):
+    assert "sm_103a" in B.moe_version()
+
+
+def test_capacity_matches_oracle(lib):
+    for cf, T, k, N in [(1.25, 4096, 2, 128), (1.0, 10, 1, 3), (0.0, 5, 2, 4),
+                        (-1.0, 5, 2, 4), (1.1, 1000, 2, 7), (2.0, 1, 1, 1)]:
+        assert B.moe_capacity(cf, T, k, N) == oracle.capacity(cf, T, k, N)
+
+
+def _args(**kw):
+    a = B.moe_forward_args()
+    a.T, a.d, a.f, a.N, a.k, a.dtype = 16, 64, 128, 8, 2, B.MOE_BF16
+    for n in ("x", "W_g", "W_gate", "W_up", "W_down", "y"):
+        setattr(a, n, 4096)          # a fake, aligned address: never dereferenced
+    a.y_dtype = B.MOE_F32
+    for key, v in kw.items():
+        setattr(a, key, v)
+    return a
+
+
+@pytest.mark.parametrize("bad", [dict(k=0), dict(k=9), dict(T=0), dict(d=60), dict(f=100),
+                                 dict(N=0), dict(x=None), dict(W_down=None), dict(y=None),
+                                 dict(x=4100), dict(dtype=7), dict(fs=16)])
+def test_forward_rejects_bad_arguments(lib, bad):
+    a = _args(**bad)
+    assert lib.moe_forward_workspace_size(ctypes.byref(a)) == 0
+    rc = lib.moe_forward(ctypes.byref(a), ctypes.c_void_p(4096), 1 << 40, None)
+    assert rc == 1, lib.moe_last_error()
+
+
+def test_forward_unsupported_sizes(lib):
+    a = _args(N=300, k=2)
+    assert lib.moe_forward(ctypes.byref(a), ctypes.c_void_p(4096), 1 << 40, None) == 2
+
+
+def test_forward_workspace_too_small(lib):
+    a = _args()
+    need = lib.moe_forward_workspace_size(ctypes.byref(a))
+    assert need > 0
+    assert lib.moe_forward(ctypes.byref(a), ctypes.c_void_p(4096), need - 1, None) == 3
+    assert lib.moe_forward(ctypes.byref(a), None, need, None) == 3
+
+
+def test_workspace_size_grows_with_shared_expert(lib):
+    a = _args()
+    b = _args(fs=64, Ws_gate=4096, Ws_up=4096, Ws_down=4096)
+    assert lib.moe_forward_workspace_size(ctypes.byref(b)) > lib.moe_forward_workspace_size(
+        ctypes.byref(a))
+
+
+def test_stage_entry_points_reject_bad_arguments(lib):
+    # router: k > N, misaligned x
+    assert lib.moe_router_topk(4096, 4096, None, 1, 4, 64, 8, 9, None, 4096, 4096, None,
+                               None) == 1
+    assert lib.moe_router_topk(4098, 4096, None, 1, 4, 64, 8, 2, None, 4096, 4096, None,
+                               None) == 1
+    assert lib.moe_router_topk(4096, 4096, None, 1, 4, 64, 300, 2, None, 4096, 4096, None,
+                               None) == 2
+    # permute: negative capacity, workspace too small
+    assert lib.moe_permute(4096, None, None, 1, 4, 64, 8, 2, -1, 4096, 4096, 4096, None, 4096,
+                           None, None, None, 4096, 1 << 20, None) == 1
+    assert lib.moe_permute(4096, None, None, 1, 4, 64, 8, 2, 0, 4096, 4096, 4096, None, 4096,
+                           None, None, None, None, 0, None) == 3
+    # expert ffn: f not a multiple of 8
+    assert lib.moe_expert_ffn(4096, 4096, None, 8, 64, 100, 8, 1, 4096, 4096, 4096, 4096, None,
+                              4096, 1 << 30, None) == 1
+    # combine: d not a multiple of 8
+    assert lib.moe_combine(4096, 1, 4096, 4, 2, 60, None, 4096, 0, None) == 1
+    assert "d=60" in B.lib().moe_last_error().decode()

@@ -1,0 +1,229 @@
+"""GPU parity: every stage and the whole layer, through the C ABI, against the
+fp64 CPU oracle, on seeded synthetic layers.
+
+Reduced layers span several tiles and ragged tails and are checked on every
+row; the five full-size workloads (the launch configuration the benchmark
+times) are checked on all tokens for routing and grouping and on sampled rows
+for the layer output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_mixture_experts_63_b300 import binding as B
+from sparse_mixture_experts_63_b300.configs import CONFIGS, MoEConfig
+from sparse_mixture_experts_63_b300.inputs import make_inputs
+
+import parity
+
+pytestmark = pytest.mark.gpu
+
+REDUCED = {
+    "tiny": CONFIGS["tiny"],
+    "mixtral_small": MoEConfig("mixtral_small", T=300, d=512, f=1024, N=8, k=2, bias_std=0.5,
+                               seed=31),
+    "deepseek_small": MoEConfig("deepseek_small", T=200, d=256, f=256, N=256, k=8, fs=256,
+                                seed=41),
+    "capacity_small": MoEConfig("capacity_small", T=512, d=256, f=192, N=32, k=2, cf=1.25,
+                                bias_std=1.0, seed=51),
+    "f32_wide": MoEConfig("f32_wide", T=129, d=128, f=72, N=16, k=3, bias_std=0.3, dtype="f32",
+                          seed=61),
+    "one_token": MoEConfig("one_token", T=1, d=64, f=64, N=8, k=2, seed=71),
+    "three_tokens_shared": MoEConfig("three_tokens_shared", T=3, d=128, f=128, N=16, k=4,
+                                     fs=64, seed=72),
+    "ragged_257": MoEConfig("ragged_257", T=257, d=136, f=200, N=8, k=2, seed=73),
+    "k_equals_n": MoEConfig("k_equals_n", T=64, d=64, f=64, N=4, k=4, seed=74),
+}
+
+
+def _cuda():
+    return torch.device("cuda")
+
+
+@pytest.mark.parametrize("name", list(REDUCED))
+def test_layer_reduced(name):
+    inp = make_inputs(REDUCED[name], device=_cuda())
+    res = parity.check_layer(inp)
+    print(name, res)
+
+
+@pytest.mark.parametrize("name,rows", [("mixtral_decode", None), ("capacity", 512),
+                                       ("mixtral_prefill", 48), ("deepseek", 24)])
+def test_layer_full_size(name, rows):
+    cfg = CONFIGS[name]
+    inp = make_inputs(cfg, device=_cuda())
+    sel = None
+    if rows is not None:
+        sel = np.sort(np.random.default_rng(cfg.seed).choice(cfg.T, size=rows, replace=False))
+        sel[0], sel[-1] = 0, cfg.T - 1
+    res = parity.check_layer(inp, rows=sel)
+    print(name, res)
+    del inp
+    torch.cuda.empty_cache()
+
+
+def test_bf16_output_variant():
+    inp = make_inputs(REDUCED["mixtral_small"], device=_cuda())
+    y32, _ = parity.run_forward(inp, y_dtype=torch.float32)
+    y16, _ = parity.run_forward(inp, y_dtype=torch.bfloat16)
+    assert torch.equal(y16, y32.to(torch.bfloat16))
+
+
+# --------------------------------------------------------------- stages ----
+@pytest.mark.parametrize("name", ["tiny", "mixtral_small", "deepseek_small", "capacity_small",
+                                  "f32_wide"])
+def test_router_stage(name):
+    cfg = REDUCED[name]
+    inp = make_inputs(cfg, device=_cuda())
+    logits = torch.empty((cfg.T, cfg.N), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    idx, w = B.moe_router_topk(inp.x, inp.W_g, cfg.k, bias=inp.bias, logits=logits,
+                               device_status=status)
+    torch.cuda.synchronize()
+    lo = oracle.router_logits(inp.x.cpu(), inp.W_g.cpu(),
+                              None if inp.bias is None else inp.bias.cpu())
+    rep = parity.check_routing(lo, idx.cpu().numpy(), w.cpu().numpy(), cfg.k)
+    assert not rep.unexplained and rep.w_max_rel <= parity.W_REL
+    assert int(status.item()) == 0
+    # fp32 logits against fp64: within a few ulps of the accumulation bound
+    assert np.abs(logits.cpu().double().numpy() - lo).max() < 1e-4
+
+
+def test_router_ties_and_nan():
+    """Exact ties go to the lower expert id; NaN logits rank last and are flagged."""
+    T, d, N, k = 4, 64, 8, 3
+    x = torch.zeros((T, d), dtype=torch.float32, device="cuda")
+    Wg = torch.zeros((d, N), dtype=torch.float32, device="cuda")
+    bias = torch.tensor([1.0, 2.0, 2.0, 0.5, 2.0, -1.0, 0.0, 3.0], device="cuda")
+    idx, w = B.moe_router_topk(x, Wg, k, bias=bias)
+    torch.cuda.synchronize()
+    assert idx.cpu().tolist() == [[7, 1, 2]] * T
+    bias2 = torch.tensor([float("nan"), 2.0, 2.0, 0.5, 2.0, -1.0, 0.0, 3.0], device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    idx2, _ = B.moe_router_topk(x, Wg, 8, bias=bias2, device_status=status)
+    torch.cuda.synchronize()
+    assert idx2.cpu().tolist()[0] == [7, 1, 2, 4, 3, 6, 5, 0]
+    assert int(status.item()) & B.MOE_DEV_NAN_LOGIT
+
+
+@pytest.mark.parametrize("T,N,k,cap,skew", [(1000, 8, 2, 0, 0.0), (2049, 256, 8, 0, 0.5),
+                                            (4096, 128, 2, 80, 3.0), (300, 4, 4, 0, 0.0),
+                                            (777, 32, 3, 50, 2.0), (1, 8, 2, 0, 0.0),
+                                            (513, 64, 1, 1, 0.0)])
+def test_permute_stage_bit_exact(T, N, k, cap, skew):
+    rng = np.random.default_rng(T + N)
+    p = np.exp(skew * rng.normal(size=N)); p /= p.sum()
+    idx = np.stack([rng.choice(N, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    d = 64
+    x = torch.randn((T, d), device="cuda").to(torch.bfloat16)
+    w = torch.rand((T, k), device="cuda")
+    out = B.moe_permute(torch.from_numpy(idx).cuda(), N, x=x, topk_w=w, capacity=cap)
+    torch.cuda.synchronize()
+    g = oracle.group(idx, N, cap)
+    A = g["offsets"][-1]
+    np.testing.assert_array_equal(out["counts"].cpu().numpy(), g["counts"])
+    np.testing.assert_array_equal(out["offsets"].cpu().numpy(), g["offsets"])
+    np.testing.assert_array_equal(out["inv_pos"].cpu().numpy(), g["inv_pos"])
+    np.testing.assert_array_equal(out["perm_token"][:A].cpu().numpy(), g["perm_token"])
+    assert int(out["dropped"].item()) == g["dropped"]
+    pt = torch.from_numpy(g["perm_token"].astype(np.int64)).cuda()
+    assert torch.equal(out["x_perm"][:A], x[pt])
+    slots = torch.from_numpy(g["perm_slot"].astype(np.int64)).cuda()
+    assert torch.equal(out["row_scale"][:A], w[pt, slots])
+
+
+def test_permute_all_tokens_one_expert_and_empty_experts():
+    T, N, k = 1000, 16, 1
+    idx = np.full((T, k), 5, dtype=np.int32)
+    out = B.moe_permute(torch.from_numpy(idx).cuda(), N, capacity=0)
+    torch.cuda.synchronize()
+    off = out["offsets"].cpu().numpy()
+    assert off.tolist() == [0] * 6 + [T] * 11
+    assert out["perm_token"][:T].cpu().tolist() == list(range(T))
+
+
+def test_permute_bad_expert_id_sets_status():
+    idx = torch.tensor([[0, 1], [9, 2], [-3, 0]], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = B.moe_permute(idx, 4, capacity=0, device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & B.MOE_DEV_BAD_EXPERT_ID
+    g = oracle.group(idx.cpu().numpy(), 4, 0)
+    np.testing.assert_array_equal(out["inv_pos"].cpu().numpy(), g["inv_pos"])
+    assert int(out["dropped"].item()) == 2
+
+
+def test_permute_repeat_bit_identical():
+    rng = np.random.default_rng(5)
+    idx = torch.from_numpy(np.stack([rng.choice(256, 8, replace=False) for _ in range(3000)])
+                           .astype(np.int32)).cuda()
+    a = B.moe_permute(idx, 256, capacity=0)
+    b = B.moe_permute(idx, 256, capacity=0)
+    torch.cuda.synchronize()
+    for key in ("counts", "offsets", "inv_pos", "perm_token"):
+        assert torch.equal(a[key], b[key])
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixtral_small", "deepseek_small", "f32_wide"])
+def test_expert_ffn_stage(name):
+    """y_perm rows = row_scale * SwiGLU_e(x_perm) against the oracle's expert rows."""
+    cfg = REDUCED[name]
+    inp = make_inputs(cfg, device=_cuda())
+    idx, w = B.moe_router_topk(inp.x, inp.W_g, cfg.k, bias=inp.bias)
+    perm = B.moe_permute(idx, cfg.N, x=inp.x, topk_w=w, capacity=0)
+    y_perm = B.moe_expert_ffn(perm["x_perm"], perm["offsets"], inp.W_gate, inp.W_up, inp.W_down,
+                              row_scale=perm["row_scale"])
+    torch.cuda.synchronize()
+    off = perm["offsets"].cpu().numpy()
+    xp = perm["x_perm"].cpu()
+    rs = perm["row_scale"].cpu().double().numpy()
+    ref = np.zeros((off[-1], cfg.d))
+    for e in range(cfg.N):
+        if off[e + 1] > off[e]:
+            ref[off[e]:off[e + 1]] = oracle.expert_rows(inp.W_gate[e].cpu(), inp.W_up[e].cpu(),
+                                                        inp.W_down[e].cpu(), xp[off[e]:off[e + 1]])
+    ref *= rs[:off[-1], None]
+    parity.assert_y_close(y_perm[:off[-1]].float().cpu().numpy(), ref, cfg.dtype)
+
+
+def test_combine_stage():
+    T, k, d = 333, 3, 128
+    A = T * k
+    y_perm = torch.randn((A, d), device="cuda").to(torch.bfloat16)
+    inv = torch.randperm(A, device="cuda").int().view(T, k)
+    inv[::7, 1] = -1
+    shared = torch.randn((T, d), device="cuda").to(torch.bfloat16)
+    y = B.moe_combine(y_perm, inv, shared_y=shared)
+    torch.cuda.synchronize()
+    ones = np.ones((T, k))
+    invn = inv.cpu().numpy()
+    o = y_perm.double().cpu().numpy()[np.maximum(invn, 0)]
+    ref = oracle.combine_rows(invn, ones, o, shared.double().cpu().numpy())
+    np.testing.assert_allclose(y.cpu().double().numpy(), ref, rtol=1e-6, atol=1e-5)
+
+
+def test_forward_repeat_bit_identical():
+    inp = make_inputs(REDUCED["deepseek_small"], device=_cuda())
+    y1, o1 = parity.run_forward(inp)
+    y2, o2 = parity.run_forward(inp)
+    assert torch.equal(y1, y2)
+    for key in ("topk_idx", "topk_w", "counts", "offsets", "inv_pos"):
+        assert torch.equal(o1[key], o2[key])
+
+
+def test_host_io_variant_matches_device_call():
+    cfg = REDUCED["capacity_small"]
+    inp = make_inputs(cfg, device=_cuda())
+    y_dev, _ = parity.run_forward(inp, logits=False)
+    layer = B.MoELayer(inp.W_g, inp.W_gate, inp.W_up, inp.W_down, cfg.k, bias=inp.bias,
+                       capacity_factor=cfg.cf)
+    x_stage = torch.empty_like(inp.x)
+    y_stage = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device="cuda")
+    o = layer.outputs_for(cfg.T, inp.x.device)
+    a = layer.args(x_stage, y_stage, o)
+    x_host = inp.x.cpu().pin_memory()
+    y_host = torch.empty((cfg.T, cfg.d), dtype=torch.float32).pin_memory()
+    B.moe_forward_host_io(a, x_host, y_host, layer.workspace(a, inp.x.device))
+    torch.cuda.synchronize()
+    assert torch.equal(y_host, y_dev.cpu())
