@@ -166,6 +166,9 @@ moe_status_t launch_expert_ffn(const void *x_perm, const int32_t *offsets, const
                                void *y_perm, int32_t *device_status, void *workspace,
                                cudaStream_t stream) {
   void *h = workspace;
+  if (dtype == MOE_BF16)
+    return launch_ffn_tc(x_perm, offsets, row_scale, A_max, d, f, N, W_gate, W_up, W_down, h,
+                         y_perm, device_status, stream);
   return launch_ffn_simt(x_perm, offsets, row_scale, A_max, d, f, N, dtype, W_gate, W_up,
                          W_down, h, y_perm, device_status, stream);
 }

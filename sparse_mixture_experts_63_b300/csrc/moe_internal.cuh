@@ -99,6 +99,12 @@ moe_status_t launch_ffn_simt(const void *x_perm, const int32_t *offsets,
                              const void *W_down, void *h, void *y_perm,
                              int32_t *device_status, cudaStream_t stream);
 
+// bf16 tcgen05 grouped SwiGLU FFN (the bf16 layer's path).
+moe_status_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, const float *row_scale,
+                           int A_max, int d, int f, int N, const void *W_gate, const void *W_up,
+                           const void *W_down, void *h, void *y_perm, int32_t *device_status,
+                           cudaStream_t stream);
+
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 }  // namespace moe

@@ -34,6 +34,8 @@ REDUCED = {
                                      fs=64, seed=72),
     "ragged_257": MoEConfig("ragged_257", T=257, d=136, f=200, N=8, k=2, seed=73),
     "k_equals_n": MoEConfig("k_equals_n", T=64, d=64, f=64, N=4, k=4, seed=74),
+    "many_rows": MoEConfig("many_rows", T=2048, d=256, f=320, N=4, k=2, bias_std=1.0, seed=75),
+    "odd_dims": MoEConfig("odd_dims", T=173, d=200, f=136, N=6, k=2, fs=72, seed=76),
 }
 
 
@@ -165,7 +167,8 @@ def test_permute_repeat_bit_identical():
         assert torch.equal(a[key], b[key])
 
 
-@pytest.mark.parametrize("name", ["tiny", "mixtral_small", "deepseek_small", "f32_wide"])
+@pytest.mark.parametrize("name", ["tiny", "mixtral_small", "deepseek_small", "f32_wide",
+                                  "many_rows", "odd_dims", "ragged_257"])
 def test_expert_ffn_stage(name):
     """y_perm rows = row_scale * SwiGLU_e(x_perm) against the oracle's expert rows."""
     cfg = REDUCED[name]
