@@ -52,6 +52,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override T (smaller cases for profiling captures)")
+    ap.add_argument("--forward-only", action="store_true",
+                    help="time moe_forward only (no stage, end-to-end or CPU legs)")
     return ap.parse_args()
 
 
@@ -235,6 +239,8 @@ def cpu_baseline(cfg, dev_inp, seconds):
 # ------------------------------------------------------------ our arm -------
 def run_ours(args, ws, rank, local):
     cfg = CONFIGS[args.config]
+    if args.tokens:
+        cfg = cfg.scaled(T=args.tokens)
     dev = torch.device("cuda", local)
     inp = make_inputs(cfg, device=dev)
     # each rank gets its own batch of the same layer
@@ -277,6 +283,14 @@ def run_ours(args, ws, rank, local):
         return sum(s.elapsed_time(e) for s, e in evs) / args.steps, launches
 
     ms, launches = timed_loop()
+    if args.forward_only:
+        clocks = sampler.stop()
+        ms_max = reduce_max(ms, ws)
+        if rank == 0:
+            return {"config": cfg_desc(cfg), "ms_per_step": round(ms_max, 4),
+                    "value": round(ws * cfg.T / (ms_max / 1e3), 1), "unit": "tokens/s",
+                    "gpu_launches": int(launches), "clocks": clocks, "forward_only": True}
+        return None
 
     # per-stage times through the stage entry points (same inputs, same stream)
     k, N = cfg.k, cfg.N

@@ -99,6 +99,11 @@ moe_status_t launch_ffn_simt(const void *x_perm, const int32_t *offsets,
                              const void *W_down, void *h, void *y_perm,
                              int32_t *device_status, cudaStream_t stream);
 
+// bf16 tcgen05 router (returns MOE_ERR_UNSUPPORTED when N does not suit it).
+moe_status_t launch_router_tc(const void *x, const void *W_g, const float *bias, int T, int d,
+                              int N, int k, float *logits, int32_t *topk_idx, float *topk_w,
+                              int32_t *device_status, cudaStream_t stream);
+
 // bf16 tcgen05 grouped SwiGLU FFN (the bf16 layer's path).
 moe_status_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, const float *row_scale,
                            int A_max, int d, int f, int N, const void *W_gate, const void *W_up,

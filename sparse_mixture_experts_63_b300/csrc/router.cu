@@ -289,6 +289,12 @@ moe_status_t launch_router_topk(const void *x, const void *W_g, const float *bia
                                 moe_dtype_t dtype, int T, int d, int N, int k, float *logits,
                                 int32_t *topk_idx, float *topk_w, int32_t *device_status,
                                 cudaStream_t stream) {
+  if (dtype == MOE_BF16) {
+    // Tensor cores when the expert count suits them (N % 8 == 0, N <= 256).
+    moe_status_t s = launch_router_tc(x, W_g, bias, T, d, N, k, logits, topk_idx, topk_w,
+                                      device_status, stream);
+    if (s != MOE_ERR_UNSUPPORTED) return s;
+  }
   if (dtype == MOE_BF16)
     return launch_typed<__nv_bfloat16>(x, W_g, bias, T, d, N, k, logits, topk_idx, topk_w,
                                        device_status, stream);
