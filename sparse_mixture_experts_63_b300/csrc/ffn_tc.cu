@@ -7,21 +7,27 @@
 // runs once per batch -- here one persistent launch covers every expert).
 // SwiGLU reading: h = SiLU(x W_gate) * (x W_up), y_perm = row_scale * (h W_down).
 //
-// Formulation ("swap AB"): the weights are the 128-row M operand and the
-// expert's tokens the N operand, so a tile's N is that expert's row count
-// rounded up to 16 (no padding of small experts to 128 rows):
+// Formulation ("swap AB"): the weights are the M operand and the expert's
+// tokens the N operand, so a tile's N is that expert's row count rounded up
+// to 32 (no padding of small experts to 128 rows).  Two CTAs of a cluster
+// share one MMA (tcgen05 cta_group::2, M = 256): CTA r holds 128 weight rows
+// and half of the token rows, and gets its 128 rows of D in its own tensor
+// memory.  Per CTA:
 //   GEMM1  D[128 x n] = [W_gate[:, f0:f0+64] | W_up[:, f0:f0+64]]^T x x_perm^T
-//          lanes 0-63 hold gate, lanes 64-127 up for the same 64 hidden units;
-//          the epilogue writes h = SiLU(gate) * up (bf16) for those tokens.
-//   GEMM2  D[128 x n] = W_down[:, m0:m0+128]^T x h^T
+//          lanes 0-63 hold gate, lanes 64-127 up for the same 64 hidden units
+//          (f0 = 128 * pair + 64 * r); the epilogue writes h = SiLU(gate) * up.
+//   GEMM2  D[128 x n] = W_down[:, m0:m0+128]^T x h^T   (m0 = 256 * pair + 128 * r)
 //          the epilogue writes y_perm = row_scale * D (bf16).
 // A (weights) is read MN-major straight from W[N, K, M] by 3-D TMA boxes of
 // 64(M) x 64(K) with 128-byte swizzle; B (token rows, K contiguous) is read
-// K-major by 2-D boxes of 64(K) x {32,64,128,256}(rows).
+// K-major by 2-D boxes of 64(K) x {32,64,128}(rows), half a tile per CTA.
+// Sharing the token tile halves each CTA's bytes per MMA cycle, so six 32 KB
+// stages cover the ~2 us load latency that four 48 KB stages of a one-CTA
+// tile could not (the tensor pipe sat ~30% idle waiting for data).
 //
-// CTA = 6 warps, persistent (one CTA per SM):
-//   warp 0      TMA producer (one lane)
-//   warp 1      tensor-memory allocator + MMA issuer (one lane)
+// CTA = 6 warps, persistent (one CTA pair per two SMs):
+//   warp 0      TMA producer (both CTAs; completions land on the even CTA's barriers)
+//   warp 1      tensor-memory allocator; MMA issuer in the even CTA
 //   warps 2..5  epilogue (tcgen05.ld of their 32 lanes, math, coalesced stores)
 // Pipelines: kStages shared-memory stages (full/empty mbarriers) and two
 // 256-column TMEM accumulators (acc_full/acc_empty), so the epilogue of one
@@ -36,15 +42,15 @@
 namespace moe {
 namespace {
 
-constexpr int kBM = 128;          // MMA M (weight rows per tile)
+constexpr int kBM = 128;          // weight rows per CTA (MMA M = 256 per pair)
 constexpr int kBK = 64;           // K per pipeline stage (128 B of bf16)
 constexpr int kMaxBN = 256;       // MMA N limit (tokens per tile)
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kAChunkBytes = 64 * kBK * 2;               // 8 KB: 64 M x 64 K
 constexpr int kABytes = 2 * kAChunkBytes;                // 16 KB
-constexpr int kBBytesMax = kMaxBN * kBK * 2;             // 32 KB
-constexpr int kStageBytes = kABytes + kBBytesMax;        // 48 KB
-constexpr int kNumBoxes = 4;                             // B box heights 32/64/128/256
+constexpr int kBBytesMax = (kMaxBN / 2) * kBK * 2;       // 16 KB: half a token tile
+constexpr int kStageBytes = kABytes + kBBytesMax;        // 32 KB
+constexpr int kNumBoxes = 3;                             // B box heights 32/64/128
 constexpr int kEpiThreads = 128;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr uint32_t kTmemCols = 512;                      // 2 x 256-column accumulators
@@ -76,7 +82,7 @@ struct TcParams {
   int N;                   // experts
   int K;                   // reduction length (d or f)
   int M;                   // weight columns (f for GEMM1, d for GEMM2)
-  int slabs;               // tiles along M per expert
+  int pairs;               // tiles along M per expert (256 weight rows each)
   int gemm1;               // 1: gate/up + SwiGLU, 0: down + row scale
   __nv_bfloat16 *out;      // h [*, f] or y_perm [*, d]
   int out_ld;              // = M
@@ -85,18 +91,20 @@ struct TcParams {
 };
 
 struct TileInfo {
-  int e, slab, row0, rows;  // rows of this tile: [row0, row0 + rows) of the permuted rows
+  int e, pair, row0, rows;  // rows of this tile: [row0, row0 + rows) of the permuted rows
 };
 
 // Token tiles of an expert with n rows: ceil(n/256) tiles of equal width
-// (rounded up to 16).
+// (rounded up to 32).
 __device__ __forceinline__ int token_tiles(int n) { return (n + kMaxBN - 1) / kMaxBN; }
 __device__ __forceinline__ int tile_width(int n, int jt) {
   int w = (n + jt - 1) / jt;
-  return (w + 15) & ~15;
+  return (w + 31) & ~31;
 }
+// MMA N of a tile: its rows rounded up to 32, at least 64.
+__device__ __forceinline__ int mma_n(int rows) { return max(64, (rows + 31) & ~31); }
 
-// prefix[e] = first global tile of expert e (slab-major inside an expert).
+// prefix[e] = first global tile of expert e (pair-major inside an expert).
 __device__ void build_tile_prefix(const TcParams &p, int *prefix) {
   // one warp scans the experts 32 at a time
   if (threadIdx.x < 32) {
@@ -106,7 +114,7 @@ __device__ void build_tile_prefix(const TcParams &p, int *prefix) {
       int e = e0 + lane;
       int n = 0;
       if (e < p.N) n = p.offsets[e + 1] - p.offsets[e];
-      int cnt = n > 0 ? token_tiles(n) * p.slabs : 0;
+      int cnt = n > 0 ? token_tiles(n) * p.pairs : 0;
       int incl = cnt;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -132,19 +140,21 @@ __device__ __forceinline__ TileInfo decode_tile(const TcParams &p, const int *pr
   const int n = p.offsets[e + 1] - base;
   const int jt = token_tiles(n);
   const int local = t - prefix[e];
-  const int slab = local / jt;
+  const int pair = local / jt;
   const int j = local % jt;
   const int w = tile_width(n, jt);
   TileInfo ti;
   ti.e = e;
-  ti.slab = slab;
+  ti.pair = pair;
   ti.row0 = base + j * w;
   ti.rows = min(w, n - j * w);
   return ti;
 }
 
-__device__ __forceinline__ int box_index(int rows) {
-  return rows <= 32 ? 0 : rows <= 64 ? 1 : rows <= 128 ? 2 : 3;
+// B box per CTA for a tile of MMA width n: n/2 rows -> 32, 64 or 128.
+__device__ __forceinline__ int box_index(int n_mma) {
+  const int half = n_mma / 2;
+  return half <= 32 ? 0 : half <= 64 ? 1 : 2;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -152,21 +162,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmA1,
                     const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1,
-                    const __grid_constant__ CUtensorMap tmB2,
-                    const __grid_constant__ CUtensorMap tmB3, const TcParams p) {
+                    const __grid_constant__ CUtensorMap tmB2, const TcParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Smem::bars);
-  uint64_t *full = bars;                   // [kStages]
+  uint64_t *full = bars;                   // [kStages]   (used in the even CTA)
   uint64_t *empty = bars + kStages;        // [kStages]
   uint64_t *acc_full = bars + 2 * kStages; // [2]
-  uint64_t *acc_empty = acc_full + 2;      // [2]
+  uint64_t *acc_empty = acc_full + 2;      // [2]         (used in the even CTA)
   uint64_t *drain = acc_empty + 2;         // [1]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::tmem_slot);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Smem::abort_flag);
   int *prefix = reinterpret_cast<int *>(smem + Smem::tile_prefix);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = tc::cluster_ctarank();   // 0: even CTA (issues the MMAs)
+  const int cid = (int)tc::cluster_id_x();
+  const int ncl = (int)tc::nclusters_x();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -175,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&acc_full[b], 1);
-      tc::mbar_init(&acc_empty[b], kEpiThreads / 32);
+      tc::mbar_init(&acc_empty[b], 2 * kEpiThreads / 32);
     }
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -188,15 +200,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tma_prefetch_desc(&tmB0);
     tc::tma_prefetch_desc(&tmB1);
     tc::tma_prefetch_desc(&tmB2);
-    tc::tma_prefetch_desc(&tmB3);
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, kTmemCols);
-    tc::tmem_relinquish();
+    tc::tmem_alloc_pair(tmem_slot, kTmemCols);
+    tc::tmem_relinquish_pair();
   }
   build_tile_prefix(p, prefix);
   tc::tc_fence_before();
   __syncthreads();
+  tc::cluster_sync();   // the peer's barriers are initialised before any remote use
   tc::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = prefix[p.N];
@@ -204,88 +216,111 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
+    // Lane 0 runs a tight loop (stage/phase counters, no divisions); the copies
+    // complete on the even CTA's full barrier.
     if (lane == 0) {
       const uint64_t pol_w = tc::policy_evict_first();  // weights: streamed
-      const uint64_t pol_x = tc::policy_evict_last();   // token rows: reused across slabs
-      const CUtensorMap *tmB[kNumBoxes] = {&tmB0, &tmB1, &tmB2, &tmB3};
-      uint32_t it = 0;
+      const uint64_t pol_x = tc::policy_evict_last();   // token rows: reused across pairs
+      unsigned char *stage0 = smem + Smem::stages;
+      // the even CTA's full barriers, in cluster address space (contiguous, 8 B apart)
+      const uint32_t full_leader0 = tc::mapa_shared(&full[0], 0);
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      for (int t = cid; t < total_tiles && ok; t += ncl) {
         const TileInfo ti = decode_tile(p, prefix, t);
-        const int bi = box_index(ti.rows);
-        const uint32_t bbytes = (uint32_t)(32 << bi) * kBK * 2;
-        const int m0 = ti.slab * (p.gemm1 ? 64 : kBM);
+        const int n_mma = mma_n(ti.rows);
+        const int bi = box_index(n_mma);
+        const CUtensorMap *tmB = bi == 0 ? &tmB0 : bi == 1 ? &tmB1 : &tmB2;
+        const uint32_t tx = 2u * (kABytes + (uint32_t)(32 << bi) * kBK * 2);
+        const int m0 = p.gemm1 ? ti.pair * 128 + rank * 64 : ti.pair * 256 + rank * kBM;
         const int m1 = p.gemm1 ? m0 : m0 + 64;
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1;
-          if (!tc::mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, kTimeoutNs)) { ok = false; break; }
-          unsigned char *st = smem + Smem::stages + s * kStageBytes;
-          tc::mbar_arrive_expect_tx(&full[s], kABytes + bbytes);
-          tc::tma_load_3d(st, &tmA0, &full[s], m0, kb * kBK, ti.e, pol_w);
-          tc::tma_load_3d(st + kAChunkBytes, &tmA1, &full[s], m1, kb * kBK, ti.e, pol_w);
-          tc::tma_load_2d(st + kABytes, tmB[bi], &full[s], kb * kBK, ti.row0, pol_x);
+        const int brow = ti.row0 + (int)rank * (n_mma / 2);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!tc::mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, kTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          unsigned char *st = stage0 + s * kStageBytes;
+          if (rank == 0) tc::mbar_arrive_expect_tx(&full[s], tx);
+          const uint32_t fb = full_leader0 + 8u * s;
+          tc::tma_load_3d_pair(st, &tmA0, fb, m0, kb * kBK, ti.e, pol_w);
+          tc::tma_load_3d_pair(st + kAChunkBytes, &tmA1, fb, m1, kb * kBK, ti.e, pol_w);
+          tc::tma_load_2d_pair(st + kABytes, tmB, fb, kb * kBK, brow, pol_x);
+          ++issued;
+          if (++s == kStages) { s = 0; ph ^= 1; }
         }
       }
-      if (!ok) {
-        // Drain: wait (bounded) for every stage still being filled.
-        for (uint32_t q = (it >= kStages ? it - kStages : 0); q < it; ++q) {
+      if (!ok && rank == 0) {
+        // Drain: wait (bounded) for every stage still being filled (both CTAs'
+        // bytes complete on these barriers).
+        const uint32_t first = issued >= kStages ? issued - kStages : 0;
+        for (uint32_t q = first; q < issued; ++q) {
           volatile int dummy = 0;
           tc::mbar_wait_bounded(&full[q % kStages], (q / kStages) & 1, &dummy, kTimeoutNs / 4);
         }
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
-      uint32_t it = 0, tcount = 0;
+    // Even CTA only.  Lane 0 runs a tight loop: the gap between the last MMA of
+    // one stage and the first of the next must stay shorter than the work the
+    // tensor pipe still has queued, or it idles.
+    if (rank == 0 && lane == 0) {
+      const uint32_t stage0 = tc::smem_u32(smem + Smem::stages);
+      // descriptors of stage 0; stage s adds (s * kStageBytes) >> 4 to the start field
+      const uint64_t a_desc0 = tc::sdesc_sw128(stage0, kAChunkBytes, 1024);   // MN-major A
+      const uint64_t b_desc0 = tc::sdesc_sw128(stage0 + kABytes, 16, 1024);   // K-major B
+      int s = 0;
+      uint32_t ph = 0, tcount = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++tcount) {
+      for (int t = cid; t < total_tiles && ok; t += ncl, ++tcount) {
         const TileInfo ti = decode_tile(p, prefix, t);
-        const int n_mma = max(16, (ti.rows + 15) & ~15);
-        const uint32_t idesc = tc::idesc_bf16(kBM, n_mma, /*a_mn=*/1, /*b_mn=*/0);
+        const uint32_t idesc = tc::idesc_bf16(2 * kBM, mma_n(ti.rows), /*a_mn=*/1, /*b_mn=*/0);
         const int buf = tcount & 1;
         const uint32_t d_tmem = tmem_base + buf * 256;
         if (!tc::mbar_wait_bounded(&acc_empty[buf], ((tcount >> 1) & 1) ^ 1, abort_flag,
                                    kTimeoutNs)) { ok = false; break; }
         tc::tc_fence_after();
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
-          const int s = it % kStages;
-          if (!tc::mbar_wait_bounded(&full[s], (it / kStages) & 1, abort_flag, kTimeoutNs)) {
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!tc::mbar_wait_bounded(&full[s], ph, abort_flag, kTimeoutNs)) {
             ok = false;
             break;
           }
           tc::tc_fence_after();
-          const uint32_t a_addr = tc::smem_u32(smem + Smem::stages + s * kStageBytes);
-          const uint32_t b_addr = a_addr + kABytes;
-#pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            // A MN-major: 16 k-rows = two 1024-B atoms further; chunks 8 KB apart.
-            const uint64_t ad = tc::sdesc_sw128(a_addr + k * 2048, kAChunkBytes, 1024);
-            // B K-major: 16 k = 32 B further inside the 128-B swizzled row.
-            const uint64_t bd = tc::sdesc_sw128(b_addr + k * 32, 16, 1024);
-            tc::mma_f16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-          }
-          tc::mma_commit(&empty[s]);  // frees the stage once these MMAs finish
+          const uint64_t off = (uint64_t)((s * kStageBytes) >> 4);
+          const uint64_t ad = a_desc0 + off, bd = b_desc0 + off;
+          // A MN-major: 16 k-rows = two 1024-B atoms further (+128 in 16-B units);
+          // B K-major: 16 k = 32 B further inside the 128-B swizzled row (+2).
+          tc::mma_f16_pair(d_tmem, ad, bd, idesc, kb > 0 ? 1u : 0u);
+          tc::mma_f16_pair(d_tmem, ad + 128, bd + 2, idesc, 1u);
+          tc::mma_f16_pair(d_tmem, ad + 256, bd + 4, idesc, 1u);
+          tc::mma_f16_pair(d_tmem, ad + 384, bd + 6, idesc, 1u);
+          tc::mma_commit_pair(&empty[s], 0x3);  // frees the stage in both CTAs
+          if (++s == kStages) { s = 0; ph ^= 1; }
         }
         if (!ok) break;
-        tc::mma_commit(&acc_full[buf]);
+        tc::mma_commit_pair(&acc_full[buf], 0x3);
       }
-      // Drain: make sure no MMA is still writing tensor memory.
-      tc::mma_commit(drain);
+      // Drain: make sure no MMA is still reading shared or writing tensor memory.
+      tc::mma_commit_pair(drain, 0x1);
       volatile int dummy = 0;
       tc::mbar_wait_bounded(drain, 0, &dummy, kTimeoutNs);
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue --
-    const int ew = warp - 2;                 // 0..3
     const int lane_grp = warp % 4;           // TMEM lanes 32*lane_grp .. +31
     const int etid = threadIdx.x - 64;       // 0..127
     volatile int *epi_ok = reinterpret_cast<volatile int *>(smem + Smem::epi_ok);
     float *ubuf = reinterpret_cast<float *>(smem + Smem::u);
     __nv_bfloat16 *obuf = reinterpret_cast<__nv_bfloat16 *>(smem + Smem::out);
+    const uint32_t acc_empty_leader[2] = {tc::mapa_shared(&acc_empty[0], 0),
+                                          tc::mapa_shared(&acc_empty[1], 0)};
     uint32_t tcount = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++tcount) {
+    for (int t = cid; t < total_tiles; t += ncl, ++tcount) {
       const TileInfo ti = decode_tile(p, prefix, t);
       const int buf = tcount & 1;
       // One thread waits (bounded) and the outcome is shared, so the four
@@ -325,8 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::named_bar(1, kEpiThreads);
           // copy out: ncols token rows x 64 hidden units (128 B) each
-          const int m0 = ti.slab * 64;
-          const int vec_valid = min(8, (p.M - m0) / 8);
+          const int m0 = ti.pair * 128 + rank * 64;
+          const int vec_valid = max(0, min(8, (p.M - m0) / 8));
           for (int q = etid; q < ncols * 8; q += kEpiThreads) {
             const int c = q / 8, v = q % 8;
             if (v < vec_valid) {
@@ -343,12 +378,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int dr = lane_grp * 32 + lane;             // output column within the slab
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const float s = __shfl_sync(0xffffffffu, sc, c);
-            obuf[c * 128 + dr] = __float2bfloat16_rn(__uint_as_float(r[c]) * s);
+            const float sv = __shfl_sync(0xffffffffu, sc, c);
+            obuf[c * 128 + dr] = __float2bfloat16_rn(__uint_as_float(r[c]) * sv);
           }
           tc::named_bar(1, kEpiThreads);
-          const int m0 = ti.slab * kBM;
-          const int vec_valid = min(16, (p.M - m0) / 8);
+          const int m0 = ti.pair * 256 + rank * kBM;
+          const int vec_valid = max(0, min(16, (p.M - m0) / 8));
           for (int q = etid; q < ncols * 16; q += kEpiThreads) {
             const int c = q / 16, v = q % 16;
             if (v < vec_valid) {
@@ -361,16 +396,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc::tc_fence_before();
-      if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
-      (void)ew;
+      if (lane == 0) tc::mbar_arrive_cluster(acc_empty_leader[buf]);
     }
   }
 
   __syncthreads();
+  tc::cluster_sync();   // no CTA leaves while its pair may still touch its memory
   if (*abort_flag && threadIdx.x == 0) report(p.status, MOE_DEV_TIMEOUT);
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem_base, kTmemCols);
+    tc::tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -417,13 +452,30 @@ bool make_rows_map(CUtensorMap *m, const void *X, int rows, int K, int box_rows)
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int num_sms() {
+// Co-resident CTA pairs on this device (one pair per two SMs at most).
+int max_pairs() {
   static int n = 0;
   if (!n) {
-    int dev = 0;
+    int dev = 0, sms = 148;
     cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (sms / 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int c = 0;
+    if (cudaOccupancyMaxActiveClusters(&c, grouped_gemm_tc, &cfg) != cudaSuccess || c <= 0) {
+      cudaGetLastError();
+      c = sms / 2;
+    }
+    n = c < sms / 2 ? c : sms / 2;
   }
   return n;
 }
@@ -434,10 +486,23 @@ moe_status_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUt
   if (!attr_set) {
     MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc,
+                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 0));
     attr_set = true;
   }
-  grouped_gemm_tc<<<num_sms(), kThreads, kSmemBytes, stream>>>(a0, a1, b[0], b[1], b[2], b[3],
-                                                               p);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * max_pairs());
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, grouped_gemm_tc, a0, a1, b[0], b[1], b[2], p));
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
@@ -469,11 +534,11 @@ moe_status_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, const flo
     set_error("tensor map encoding failed (alignment or size)");
     return MOE_ERR_INVALID_ARG;
   }
-  TcParams p1{offsets, N, d, f, (f + 63) / 64, 1, static_cast<__nv_bfloat16 *>(h), f, nullptr,
+  TcParams p1{offsets, N, d, f, (f + 127) / 128, 1, static_cast<__nv_bfloat16 *>(h), f, nullptr,
               device_status};
   moe_status_t s = launch_gemm(wg, wu, bx, p1, stream);
   if (s != MOE_OK) return s;
-  TcParams p2{offsets, N, f, d, (d + kBM - 1) / kBM, 0, static_cast<__nv_bfloat16 *>(y_perm), d,
+  TcParams p2{offsets, N, f, d, (d + 255) / 256, 0, static_cast<__nv_bfloat16 *>(y_perm), d,
               row_scale, device_status};
   return launch_gemm(wd, wd, bh, p2, stream);
 }

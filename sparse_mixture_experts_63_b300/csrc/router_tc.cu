@@ -107,37 +107,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kblocks = (p.d + kBK - 1) / kBK;
 
   if (warp == 0) {
+    // ---- TMA producer: lane 0 runs a tight loop (stage/phase counters)
     if (lane == 0) {
       const uint64_t pol_x = tc::policy_evict_last();   // re-read by every pass
       const uint64_t pol_w = tc::policy_evict_last();
       const uint32_t bytes = kXBytes + kWChunk;
-      uint32_t it = 0;
+      int s = 0;
+      uint32_t ph = 0, issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         for (int ps = 0; ps < p.passes && ok; ++ps) {
-          for (int kb = 0; kb < kblocks; ++kb, ++it) {
-            const int s = it % kStages;
-            if (!tc::mbar_wait_bounded(&empty[s], ((it / kStages) & 1) ^ 1, abort_flag,
-                                       kTimeoutNs)) { ok = false; break; }
+          for (int kb = 0; kb < kblocks; ++kb) {
+            if (!tc::mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, kTimeoutNs)) {
+              ok = false;
+              break;
+            }
             unsigned char *st = smem + s * kStageBytes;
             tc::mbar_arrive_expect_tx(&full[s], bytes);
             tc::tma_load_2d(st, &tmX, &full[s], kb * kBK, t * kBM, pol_x);
             tc::tma_load_2d(st + kXBytes, &tmW, &full[s], ps * p.ng, kb * kBK, pol_w);
+            ++issued;
+            if (++s == kStages) { s = 0; ph ^= 1; }
           }
         }
       }
       if (!ok) {
-        for (uint32_t q = (it >= kStages ? it - kStages : 0); q < it; ++q) {
+        const uint32_t first = issued >= kStages ? issued - kStages : 0;
+        for (uint32_t q = first; q < issued; ++q) {
           volatile int dummy = 0;
           tc::mbar_wait_bounded(&full[q % kStages], (q / kStages) & 1, &dummy, kTimeoutNs / 4);
         }
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
+    // ---- MMA issuer: lane 0 runs a tight loop.  K block kb accumulates into
+    // partial `part`, which advances every ceil-spaced boundary bound[part].
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_bf16(kBM, p.ng, /*a_mn=*/0, /*b_mn=*/1);
       const int parts = kblocks < kParts ? kblocks : kParts;
-      uint32_t it = 0, round = 0;
+      const uint32_t stage0 = tc::smem_u32(smem);
+      const uint64_t a_desc0 = tc::sdesc_sw128(stage0, 16, 1024);              // x, K-major
+      const uint64_t b_desc0 = tc::sdesc_sw128(stage0 + kXBytes, kWChunk, 1024); // W, MN-major
+      int s = 0;
+      uint32_t ph = 0, round = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         for (int ps = 0; ps < p.passes; ++ps, ++round) {
@@ -146,25 +159,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc::tc_fence_after();
-          for (int kb = 0; kb < kblocks; ++kb, ++it) {
-            const int s = it % kStages;
-            if (!tc::mbar_wait_bounded(&full[s], (it / kStages) & 1, abort_flag, kTimeoutNs)) {
+          int part = 0;
+          int next_bound = (kblocks + parts - 1) / parts;   // first kb of partial 1
+          for (int kb = 0; kb < kblocks; ++kb) {
+            if (!tc::mbar_wait_bounded(&full[s], ph, abort_flag, kTimeoutNs)) {
               ok = false;
               break;
             }
             tc::tc_fence_after();
-            const int part = kb * parts / kblocks;
-            const bool first = (kb == 0) || ((kb - 1) * parts / kblocks != part);
-            const uint32_t d_tmem = tmem_base + part * kGroup;
-            const uint32_t x_addr = tc::smem_u32(smem + s * kStageBytes);
-            const uint32_t w_addr = x_addr + kXBytes;
-#pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
-              const uint64_t ad = tc::sdesc_sw128(x_addr + k * 32, 16, 1024);        // K-major
-              const uint64_t bd = tc::sdesc_sw128(w_addr + k * 2048, kWChunk, 1024);  // MN-major
-              tc::mma_f16(d_tmem, ad, bd, idesc, (!first || k > 0) ? 1u : 0u);
+            bool first = (kb == 0);
+            if (kb == next_bound) {
+              ++part;
+              next_bound = ((part + 1) * kblocks + parts - 1) / parts;
+              first = true;
             }
+            const uint32_t d_tmem = tmem_base + part * kGroup;
+            const uint64_t off = (uint64_t)((s * kStageBytes) >> 4);
+            const uint64_t ad = a_desc0 + off, bd = b_desc0 + off;
+            // x K-major: +32 B per 16 k (+2); W MN-major: +2048 B per 16 k (+128)
+            tc::mma_f16(d_tmem, ad, bd, idesc, first ? 0u : 1u);
+            tc::mma_f16(d_tmem, ad + 2, bd + 128, idesc, 1u);
+            tc::mma_f16(d_tmem, ad + 4, bd + 256, idesc, 1u);
+            tc::mma_f16(d_tmem, ad + 6, bd + 384, idesc, 1u);
             tc::mma_commit(&empty[s]);
+            if (++s == kStages) { s = 0; ph ^= 1; }
           }
           if (!ok) break;
           tc::mma_commit(&acc_full[0]);
@@ -174,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       volatile int dummy = 0;
       tc::mbar_wait_bounded(&drain, 0, &dummy, kTimeoutNs);
     }
+    __syncwarp();
   } else {
     // epilogue: thread = token row (TMEM lane)
     const int lane_grp = warp % 4;
