@@ -88,6 +88,7 @@ struct TcParams {
   int out_ld;              // = M
   const float *row_scale;  // GEMM2 only (nullable)
   int32_t *status;
+  int group;               // token tiles per raster group (see decode_tile)
 };
 
 struct TileInfo {
@@ -128,6 +129,11 @@ __device__ void build_tile_prefix(const TcParams &p, int *prefix) {
   }
 }
 
+// Tile order inside an expert: token tiles in groups of p.group; for each
+// group, every weight pair; inside that, the group's token tiles.  Tiles that
+// run at the same time then share both operands through L2 (a group's token
+// rows are sized on the host to stay resident), instead of every weight pair
+// re-streaming all of a large expert's token rows.
 __device__ __forceinline__ TileInfo decode_tile(const TcParams &p, const int *prefix, int t) {
   // binary search: last e with prefix[e] <= t (experts with no tiles share prefixes)
   int lo = 0, hi = p.N - 1;
@@ -140,8 +146,20 @@ __device__ __forceinline__ TileInfo decode_tile(const TcParams &p, const int *pr
   const int n = p.offsets[e + 1] - base;
   const int jt = token_tiles(n);
   const int local = t - prefix[e];
-  const int pair = local / jt;
-  const int j = local % jt;
+  const int full_groups = jt / p.group;
+  const int per_group = p.group * p.pairs;
+  int g, gsize, idx;
+  if (local < full_groups * per_group) {
+    g = local / per_group;
+    gsize = p.group;
+    idx = local - g * per_group;
+  } else {
+    g = full_groups;
+    gsize = jt - full_groups * p.group;
+    idx = local - full_groups * per_group;
+  }
+  const int pair = idx / gsize;
+  const int j = g * p.group + idx % gsize;
   const int w = tile_width(n, jt);
   TileInfo ti;
   ti.e = e;
@@ -219,8 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Lane 0 runs a tight loop (stage/phase counters, no divisions); the copies
     // complete on the even CTA's full barrier.
     if (lane == 0) {
-      const uint64_t pol_w = tc::policy_evict_first();  // weights: streamed
-      const uint64_t pol_x = tc::policy_evict_last();   // token rows: reused across pairs
+      const uint64_t pol_w = tc::policy_evict_normal();  // weights: shared by a group's tiles
+      const uint64_t pol_x = tc::policy_evict_last();    // token rows: reused across pairs
       unsigned char *stage0 = smem + Smem::stages;
       // the even CTA's full barriers, in cluster address space (contiguous, 8 B apart)
       const uint32_t full_leader0 = tc::mapa_shared(&full[0], 0);
@@ -452,6 +470,14 @@ bool make_rows_map(CUtensorMap *m, const void *X, int rows, int K, int box_rows)
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Token tiles per raster group: a group's token rows (256 rows x K bf16 per
+// tile) stay within ~32 MB, a quarter of the 126 MB L2.
+int raster_group(int K) {
+  const long tile_bytes = 256L * K * 2;
+  long g = (32L << 20) / tile_bytes;
+  return (int)(g < 1 ? 1 : g > 64 ? 64 : g);
+}
+
 // Co-resident CTA pairs on this device (one pair per two SMs at most).
 int max_pairs() {
   static int n = 0;
@@ -535,11 +561,11 @@ moe_status_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, const flo
     return MOE_ERR_INVALID_ARG;
   }
   TcParams p1{offsets, N, d, f, (f + 127) / 128, 1, static_cast<__nv_bfloat16 *>(h), f, nullptr,
-              device_status};
+              device_status, raster_group(d)};
   moe_status_t s = launch_gemm(wg, wu, bx, p1, stream);
   if (s != MOE_OK) return s;
   TcParams p2{offsets, N, f, d, (d + 255) / 256, 0, static_cast<__nv_bfloat16 *>(y_perm), d,
-              row_scale, device_status};
+              row_scale, device_status, raster_group(f)};
   return launch_gemm(wd, wd, bh, p2, stream);
 }
 
