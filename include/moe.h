@@ -125,6 +125,28 @@ moe_status_t moe_permute(const int32_t *topk_idx, const float *topk_w,
                          int32_t *device_status, void *workspace,
                          size_t workspace_bytes, void *stream);
 
+/* moe_permute without a workspace argument, for callers that cannot allocate
+ * device memory where they dispatch tokens (e.g. an operator inside a host
+ * framework that receives only its input and output buffers and may not
+ * allocate while the model runs).  It has no counterpart in the source pages:
+ * it is an interface convenience of this library.  Same arguments, outputs
+ * and errors as moe_permute; the scratch comes from a fixed array inside the
+ * library (256 KB, held on every GPU that loads it until the process exits):
+ *   - requires ceil(T/256) * N <= 65536, else MOE_ERR_UNSUPPORTED with a
+ *     message (e.g. T <= 65536 tokens for N = 256 experts);
+ *   - allocates nothing; the first call on each device looks up the array's
+ *     device address (with that device current), so make that first call
+ *     before any stream capture;
+ *   - every call shares the one array: calls that overlap on the GPU race;
+ *     order them on one stream.  Nothing in it needs clearing between calls. */
+moe_status_t moe_permute_noalloc(const int32_t *topk_idx, const float *topk_w,
+                                 const void *x, moe_dtype_t dtype, int T, int d,
+                                 int N, int k, int capacity, int32_t *counts,
+                                 int32_t *offsets, int32_t *perm_token,
+                                 float *row_scale, int32_t *inv_pos,
+                                 void *x_perm, int32_t *dropped,
+                                 int32_t *device_status, void *stream);
+
 /* ---------------------------------------------------------------------------
  * Step 5: grouped expert FFN (SwiGLU) over permuted rows.
  *   x_perm [A_max,d] (dtype): rows of expert e are offsets[e]..offsets[e+1]-1.

@@ -23,6 +23,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTS = ("moe_status_string", "moe_last_error", "moe_version", "moe_launch_counter",
            "moe_capacity",
            "moe_router_topk", "moe_permute_workspace_size", "moe_permute",
+           "moe_permute_noalloc",
            "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
            "moe_forward_workspace_size", "moe_forward", "moe_forward_host_io")
 
@@ -73,6 +74,8 @@ def lib():
         L.moe_permute_workspace_size.restype = sz
         L.moe_permute.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp,
                                   vp, vp, vp, sz, vp]
+        L.moe_permute_noalloc.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp,
+                                          vp, vp, vp, vp]
         L.moe_expert_ffn_workspace_size.argtypes = [ci, ci, ci, ci, ci]
         L.moe_expert_ffn_workspace_size.restype = sz
         L.moe_expert_ffn.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp,
@@ -82,7 +85,8 @@ def lib():
         L.moe_forward_workspace_size.restype = sz
         L.moe_forward.argtypes = [ctypes.POINTER(moe_forward_args), vp, sz, vp]
         L.moe_forward_host_io.argtypes = [ctypes.POINTER(moe_forward_args), vp, vp, vp, sz, vp]
-        for n in ("moe_router_topk", "moe_permute", "moe_expert_ffn", "moe_combine",
+        for n in ("moe_router_topk", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn",
+                  "moe_combine",
                   "moe_forward", "moe_forward_host_io"):
             getattr(L, n).restype = ci
         _lib = L
@@ -170,6 +174,32 @@ def moe_permute(topk_idx, N, x=None, topk_w=None, capacity=0, gather=True,
         int(capacity), _p(out["counts"]), _p(out["offsets"]), _p(out["perm_token"]),
         _p(out["row_scale"]), _p(out["inv_pos"]), _p(out["x_perm"]), _p(out["dropped"]),
         _p(device_status), _p(ws), ws_bytes, _stream(stream)))
+    return out
+
+
+def moe_permute_noalloc(topk_idx, N, x=None, topk_w=None, capacity=0, gather=True,
+                        device_status=None, stream=None, A_max=None):
+    """moe_permute without a workspace: the library's fixed scratch is used
+    instead (see include/moe.h for its size limit and sharing rules)."""
+    _cuda(topk_idx, x, topk_w)
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    d = x.shape[1] if x is not None else 0
+    A = T * k if A_max is None else A_max
+    out = dict(counts=torch.empty(N, dtype=torch.int32, device=dev),
+               offsets=torch.empty(N + 1, dtype=torch.int32, device=dev),
+               perm_token=torch.empty(max(T * k, 1), dtype=torch.int32, device=dev),
+               row_scale=(torch.empty(max(T * k, 1), dtype=torch.float32, device=dev)
+                          if topk_w is not None else None),
+               inv_pos=torch.empty((T, k), dtype=torch.int32, device=dev),
+               x_perm=(torch.empty((max(A, 1), d), dtype=x.dtype, device=dev)
+                       if (gather and x is not None) else None),
+               dropped=torch.zeros(1, dtype=torch.int32, device=dev))
+    _check("moe_permute_noalloc", lib().moe_permute_noalloc(
+        _p(topk_idx), _p(topk_w), _p(x), _dt(x) if x is not None else MOE_BF16, T, d, N, k,
+        int(capacity), _p(out["counts"]), _p(out["offsets"]), _p(out["perm_token"]),
+        _p(out["row_scale"]), _p(out["inv_pos"]), _p(out["x_perm"]), _p(out["dropped"]),
+        _p(device_status), _stream(stream)))
     return out
 
 
