@@ -54,6 +54,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override T (smaller cases for profiling captures)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override N (smaller profiling cases with the same per-expert shape)")
+    ap.add_argument("--ffn-dim", type=int, default=0,
+                    help="override f (e.g. tiny experts to profile the router alone)")
     ap.add_argument("--forward-only", action="store_true",
                     help="time moe_forward only (no stage, end-to-end or CPU legs)")
     return ap.parse_args()
@@ -215,17 +219,26 @@ def prefetch(inp, S, fetch):
         fetch(e)
 
 
+def calibrate_sample(inp, fetch, T, seconds, cap):
+    """Token count whose oracle pass takes about `seconds` (grown geometrically
+    from a tiny sample, since fixed costs dominate the smallest ones)."""
+    S = min(T, 2 if inp["cfg"].d * inp["cfg"].f > 1 << 24 else 16)
+    while True:
+        prefetch(inp, S, fetch)
+        t = time.perf_counter()
+        oracle_sample(inp, S, fetch)
+        dt = time.perf_counter() - t
+        if dt >= seconds / 4 or S >= cap:
+            return int(min(cap, max(1, S * seconds / max(dt, 1e-4))))
+        S = min(cap, S * 4)
+
+
 def cpu_baseline(cfg, dev_inp, seconds):
     """Times the oracle on the host cores on a bounded token sample; returns dict."""
     import oracle
     S_cap = min(cfg.T, 4096)
     inp, fetch, _ = host_layer(cfg, dev_inp, S_cap)
-    S0 = min(cfg.T, 2 if cfg.d * cfg.f > 1 << 24 else 16)
-    prefetch(inp, S0, fetch)
-    t = time.perf_counter()
-    oracle_sample(inp, S0, fetch)
-    dt0 = max(time.perf_counter() - t, 1e-4)
-    S = int(min(S_cap, max(S0, S0 * seconds / dt0)))
+    S = calibrate_sample(inp, fetch, cfg.T, seconds, S_cap)
     prefetch(inp, S, fetch)
     t = time.perf_counter()
     oracle_sample(inp, S, fetch)
@@ -241,6 +254,10 @@ def run_ours(args, ws, rank, local):
     cfg = CONFIGS[args.config]
     if args.tokens:
         cfg = cfg.scaled(T=args.tokens)
+    if args.experts:
+        cfg = cfg.scaled(N=args.experts)
+    if args.ffn_dim:
+        cfg = cfg.scaled(f=args.ffn_dim, fs=args.ffn_dim if cfg.fs else 0)
     dev = torch.device("cuda", local)
     inp = make_inputs(cfg, device=dev)
     # each rank gets its own batch of the same layer
@@ -431,12 +448,7 @@ def run_reference(args, ws, rank):
     dinp = make_inputs(cfg, device=dev)
     per_step = max(0.5, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
     inp, fetch, _ = host_layer(cfg, dinp, min(cfg.T, 4096))
-    S0 = min(cfg.T, 2 if cfg.d * cfg.f > 1 << 24 else 16)
-    prefetch(inp, S0, fetch)
-    t = time.perf_counter()
-    oracle_sample(inp, S0, fetch)
-    dt0 = max(time.perf_counter() - t, 1e-4)
-    S = int(min(cfg.T, 4096, max(1, S0 * per_step / dt0)))
+    S = calibrate_sample(inp, fetch, cfg.T, per_step, min(cfg.T, 4096))
     prefetch(inp, S, fetch)
     for _ in range(args.warmup):
         oracle_sample(inp, S, fetch)
