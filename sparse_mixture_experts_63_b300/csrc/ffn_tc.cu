@@ -29,7 +29,7 @@
 //   warp 0      TMA producer (both CTAs; completions land on the even CTA's barriers)
 //   warp 1      tensor-memory allocator; MMA issuer in the even CTA
 //   warps 2..5  epilogue (tcgen05.ld of their 32 lanes, math, coalesced stores)
-// Pipelines: kStages shared-memory stages (full/empty mbarriers) and two
+// Pipelines: 6-9 shared-memory stages (full/empty mbarriers) and two
 // 256-column TMEM accumulators (acc_full/acc_empty), so the epilogue of one
 // tile overlaps the MMAs of the next.  Every wait is bounded (2 s): on timeout
 // the CTA sets MOE_DEV_TIMEOUT, drains what it issued and exits cleanly.
@@ -45,11 +45,15 @@ namespace {
 constexpr int kBM = 128;          // weight rows per CTA (MMA M = 256 per pair)
 constexpr int kBK = 64;           // K per pipeline stage (128 B of bf16)
 constexpr int kMaxBN = 256;       // MMA N limit (tokens per tile)
-constexpr int kStages = 6;
+constexpr int kMaxStages = 10;
 constexpr int kAChunkBytes = 64 * kBK * 2;               // 8 KB: 64 M x 64 K
 constexpr int kABytes = 2 * kAChunkBytes;                // 16 KB
-constexpr int kBBytesMax = (kMaxBN / 2) * kBK * 2;       // 16 KB: half a token tile
-constexpr int kStageBytes = kABytes + kBBytesMax;        // 32 KB
+constexpr int kStageRegion = 192 * 1024;                 // shared memory for all stages
+// A stage holds 16 KB of weights and half a token tile (width/2 rows x 128 B):
+// tile width 256 -> 32 KB stages x 6; 128 -> 24 KB x 8; 64 -> 20 KB x 9.  The
+// host picks the width per layer from its expected largest expert, so narrow
+// layers (decode, capacity-limited) get more stages and more weight bytes in
+// flight.
 constexpr int kNumBoxes = 3;                             // B box heights 32/64/128
 constexpr int kEpiThreads = 128;
 constexpr int kThreads = 64 + kEpiThreads;
@@ -65,10 +69,10 @@ constexpr int kOutBytes = 32 * 256;                      // 32 token rows x up t
 struct Smem {
   // offsets inside the 1024-aligned dynamic smem block
   static constexpr int stages = 0;
-  static constexpr int u = kStages * kStageBytes;
+  static constexpr int u = kStageRegion;
   static constexpr int out = u + kUBytes;
   static constexpr int bars = out + kOutBytes;                    // 8-byte aligned
-  static constexpr int nbars = 2 * kStages + 4 + 1;
+  static constexpr int nbars = 2 * kMaxStages + 4 + 1;
   static constexpr int tmem_slot = bars + nbars * 8;
   static constexpr int abort_flag = tmem_slot + 4;
   static constexpr int epi_ok = abort_flag + 4;
@@ -89,15 +93,18 @@ struct TcParams {
   const float *row_scale;  // GEMM2 only (nullable)
   int32_t *status;
   int group;               // token tiles per raster group (see decode_tile)
+  int max_bn;              // token tile width cap: 64, 128 or 256
+  int stages;              // pipeline stages (kStageRegion / stage_bytes)
+  int stage_bytes;         // kABytes + max_bn/2 rows x 128 B
 };
 
 struct TileInfo {
   int e, pair, row0, rows;  // rows of this tile: [row0, row0 + rows) of the permuted rows
 };
 
-// Token tiles of an expert with n rows: ceil(n/256) tiles of equal width
+// Token tiles of an expert with n rows: ceil(n/max_bn) tiles of equal width
 // (rounded up to 32).
-__device__ __forceinline__ int token_tiles(int n) { return (n + kMaxBN - 1) / kMaxBN; }
+__device__ __forceinline__ int token_tiles(int n, int max_bn) { return (n + max_bn - 1) / max_bn; }
 __device__ __forceinline__ int tile_width(int n, int jt) {
   int w = (n + jt - 1) / jt;
   return (w + 31) & ~31;
@@ -115,7 +122,7 @@ __device__ void build_tile_prefix(const TcParams &p, int *prefix) {
       int e = e0 + lane;
       int n = 0;
       if (e < p.N) n = p.offsets[e + 1] - p.offsets[e];
-      int cnt = n > 0 ? token_tiles(n) * p.pairs : 0;
+      int cnt = n > 0 ? token_tiles(n, p.max_bn) * p.pairs : 0;
       int incl = cnt;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -144,7 +151,7 @@ __device__ __forceinline__ TileInfo decode_tile(const TcParams &p, const int *pr
   const int e = lo;
   const int base = p.offsets[e];
   const int n = p.offsets[e + 1] - base;
-  const int jt = token_tiles(n);
+  const int jt = token_tiles(n, p.max_bn);
   const int local = t - prefix[e];
   const int full_groups = jt / p.group;
   const int per_group = p.group * p.pairs;
@@ -185,9 +192,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Smem::bars);
-  uint64_t *full = bars;                   // [kStages]   (used in the even CTA)
-  uint64_t *empty = bars + kStages;        // [kStages]
-  uint64_t *acc_full = bars + 2 * kStages; // [2]
+  uint64_t *full = bars;                   // [kMaxStages] (used in the even CTA)
+  uint64_t *empty = bars + kMaxStages;     // [kMaxStages]
+  uint64_t *acc_full = bars + 2 * kMaxStages; // [2]
   uint64_t *acc_empty = acc_full + 2;      // [2]         (used in the even CTA)
   uint64_t *drain = acc_empty + 2;         // [1]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::tmem_slot);
@@ -199,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ncl = (int)tc::nclusters_x();
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kMaxStages; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
@@ -260,23 +267,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          unsigned char *st = stage0 + s * kStageBytes;
+          unsigned char *st = stage0 + s * p.stage_bytes;
           if (rank == 0) tc::mbar_arrive_expect_tx(&full[s], tx);
           const uint32_t fb = full_leader0 + 8u * s;
           tc::tma_load_3d_pair(st, &tmA0, fb, m0, kb * kBK, ti.e, pol_w);
           tc::tma_load_3d_pair(st + kAChunkBytes, &tmA1, fb, m1, kb * kBK, ti.e, pol_w);
           tc::tma_load_2d_pair(st + kABytes, tmB, fb, kb * kBK, brow, pol_x);
           ++issued;
-          if (++s == kStages) { s = 0; ph ^= 1; }
+          if (++s == p.stages) { s = 0; ph ^= 1; }
         }
       }
       if (!ok && rank == 0) {
         // Drain: wait (bounded) for every stage still being filled (both CTAs'
         // bytes complete on these barriers).
-        const uint32_t first = issued >= kStages ? issued - kStages : 0;
+        const uint32_t ns = (uint32_t)p.stages;
+        const uint32_t first = issued >= ns ? issued - ns : 0;
         for (uint32_t q = first; q < issued; ++q) {
           volatile int dummy = 0;
-          tc::mbar_wait_bounded(&full[q % kStages], (q / kStages) & 1, &dummy, kTimeoutNs / 4);
+          tc::mbar_wait_bounded(&full[q % ns], (q / ns) & 1, &dummy, kTimeoutNs / 4);
         }
       }
     }
@@ -288,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tensor pipe still has queued, or it idles.
     if (rank == 0 && lane == 0) {
       const uint32_t stage0 = tc::smem_u32(smem + Smem::stages);
-      // descriptors of stage 0; stage s adds (s * kStageBytes) >> 4 to the start field
+      // descriptors of stage 0; stage s adds (s * stage_bytes) >> 4 to the start field
       const uint64_t a_desc0 = tc::sdesc_sw128(stage0, kAChunkBytes, 1024);   // MN-major A
       const uint64_t b_desc0 = tc::sdesc_sw128(stage0 + kABytes, 16, 1024);   // K-major B
       int s = 0;
@@ -308,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc::tc_fence_after();
-          const uint64_t off = (uint64_t)((s * kStageBytes) >> 4);
+          const uint64_t off = (uint64_t)((s * p.stage_bytes) >> 4);
           const uint64_t ad = a_desc0 + off, bd = b_desc0 + off;
           // A MN-major: 16 k-rows = two 1024-B atoms further (+128 in 16-B units);
           // B K-major: 16 k = 32 B further inside the 128-B swizzled row (+2).
@@ -317,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_f16_pair(d_tmem, ad + 256, bd + 4, idesc, 1u);
           tc::mma_f16_pair(d_tmem, ad + 384, bd + 6, idesc, 1u);
           tc::mma_commit_pair(&empty[s], 0x3);  // frees the stage in both CTAs
-          if (++s == kStages) { s = 0; ph ^= 1; }
+          if (++s == p.stages) { s = 0; ph ^= 1; }
         }
         if (!ok) break;
         tc::mma_commit_pair(&acc_full[buf], 0x3);
@@ -537,9 +545,9 @@ moe_status_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUt
 
 // x_perm [A_max, d] -> h [A_max, f] -> y_perm [A_max, d], bf16, per expert.
 moe_status_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, const float *row_scale,
-                           int A_max, int d, int f, int N, const void *W_gate, const void *W_up,
-                           const void *W_down, void *h, void *y_perm, int32_t *device_status,
-                           cudaStream_t stream) {
+                           int A_max, int d, int f, int N, int capacity, const void *W_gate,
+                           const void *W_up, const void *W_down, void *h, void *y_perm,
+                           int32_t *device_status, cudaStream_t stream) {
   if (A_max == 0) return MOE_OK;
   if (!encode_fn()) {
     set_error("cuTensorMapEncodeTiled unavailable from the driver");
@@ -560,12 +568,22 @@ moe_status_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, const flo
     set_error("tensor map encoding failed (alignment or size)");
     return MOE_ERR_INVALID_ARG;
   }
+  // Token tile width cap: the expected largest expert (1.25x the average rows,
+  // or the capacity when that is smaller) rounded up to 64/128/256.  Narrow
+  // layers then fit more, smaller stages.
+  const long avg_rows = ((long)A_max + N - 1) / N;
+  long exp_rows = avg_rows + avg_rows / 4;
+  if (capacity > 0 && capacity < exp_rows) exp_rows = capacity;
+  const int max_bn = exp_rows > 128 ? 256 : exp_rows > 64 ? 128 : 64;
+  const int stage_bytes = kABytes + (max_bn / 2) * kBK * 2;
+  int stages = kStageRegion / stage_bytes;
+  if (stages > kMaxStages) stages = kMaxStages;
   TcParams p1{offsets, N, d, f, (f + 127) / 128, 1, static_cast<__nv_bfloat16 *>(h), f, nullptr,
-              device_status, raster_group(d)};
+              device_status, raster_group(d), max_bn, stages, stage_bytes};
   moe_status_t s = launch_gemm(wg, wu, bx, p1, stream);
   if (s != MOE_OK) return s;
   TcParams p2{offsets, N, f, d, (d + 255) / 256, 0, static_cast<__nv_bfloat16 *>(y_perm), d,
-              row_scale, device_status, raster_group(f)};
+              row_scale, device_status, raster_group(f), max_bn, stages, stage_bytes};
   return launch_gemm(wd, wd, bh, p2, stream);
 }
 

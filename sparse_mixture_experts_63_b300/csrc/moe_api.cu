@@ -161,14 +161,14 @@ size_t ffn_workspace_bytes(int A_max, int d, int f, int N, moe_dtype_t dtype) {
 }
 
 moe_status_t launch_expert_ffn(const void *x_perm, const int32_t *offsets, const float *row_scale,
-                               int A_max, int d, int f, int N, moe_dtype_t dtype,
+                               int A_max, int d, int f, int N, int capacity, moe_dtype_t dtype,
                                const void *W_gate, const void *W_up, const void *W_down,
                                void *y_perm, int32_t *device_status, void *workspace,
                                cudaStream_t stream) {
   void *h = workspace;
   if (dtype == MOE_BF16)
-    return launch_ffn_tc(x_perm, offsets, row_scale, A_max, d, f, N, W_gate, W_up, W_down, h,
-                         y_perm, device_status, stream);
+    return launch_ffn_tc(x_perm, offsets, row_scale, A_max, d, f, N, capacity, W_gate, W_up,
+                         W_down, h, y_perm, device_status, stream);
   return launch_ffn_simt(x_perm, offsets, row_scale, A_max, d, f, N, dtype, W_gate, W_up,
                          W_down, h, y_perm, device_status, stream);
 }
@@ -269,7 +269,7 @@ moe_status_t moe_expert_ffn(const void *x_perm, const int32_t *offsets, const fl
     return MOE_ERR_WORKSPACE;
   }
   if ((s = check_device()) != MOE_OK) return s;
-  return launch_expert_ffn(x_perm, offsets, row_scale, A_max, d, f, N, dtype, W_gate, W_up,
+  return launch_expert_ffn(x_perm, offsets, row_scale, A_max, d, f, N, 0, dtype, W_gate, W_up,
                            W_down, y_perm, device_status, workspace,
                            static_cast<cudaStream_t>(stream));
 }
@@ -342,14 +342,14 @@ moe_status_t moe_forward(const moe_forward_args *a, void *workspace, size_t work
                      L.counts, L.offsets, L.perm_token, L.row_scale, L.inv_pos, L.x_perm,
                      L.dropped, a->device_status, L.perm_ws, stream);
   if (s != MOE_OK) return s;
-  s = launch_expert_ffn(L.x_perm, L.offsets, L.row_scale, A_max, a->d, a->f, a->N, a->dtype,
-                        a->W_gate, a->W_up, a->W_down, L.y_perm, a->device_status, L.ffn_ws,
-                        stream);
+  s = launch_expert_ffn(L.x_perm, L.offsets, L.row_scale, A_max, a->d, a->f, a->N, cap,
+                        a->dtype, a->W_gate, a->W_up, a->W_down, L.y_perm, a->device_status,
+                        L.ffn_ws, stream);
   if (s != MOE_OK) return s;
   if (a->fs > 0) {
     set_shared_offsets<<<1, 1, 0, stream>>>(L.sh_offsets, a->T);
     MOE_LAUNCH_CHECK();
-    s = launch_expert_ffn(a->x, L.sh_offsets, nullptr, a->T, a->d, a->fs, 1, a->dtype,
+    s = launch_expert_ffn(a->x, L.sh_offsets, nullptr, a->T, a->d, a->fs, 1, 0, a->dtype,
                           a->Ws_gate, a->Ws_up, a->Ws_down, L.ys, a->device_status,
                           L.sh_ffn_ws, stream);
     if (s != MOE_OK) return s;

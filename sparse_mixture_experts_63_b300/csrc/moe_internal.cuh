@@ -81,11 +81,13 @@ moe_status_t launch_permute(const int32_t *topk_idx, const float *topk_w, const 
                             cudaStream_t stream);
 
 size_t ffn_workspace_bytes(int A_max, int d, int f, int N, moe_dtype_t dtype);
+// capacity: rows per expert the dispatch kept at most (0 = unknown/none); a
+// tiling hint only.
 moe_status_t launch_expert_ffn(const void *x_perm, const int32_t *offsets,
                                const float *row_scale, int A_max, int d, int f, int N,
-                               moe_dtype_t dtype, const void *W_gate, const void *W_up,
-                               const void *W_down, void *y_perm, int32_t *device_status,
-                               void *workspace, cudaStream_t stream);
+                               int capacity, moe_dtype_t dtype, const void *W_gate,
+                               const void *W_up, const void *W_down, void *y_perm,
+                               int32_t *device_status, void *workspace, cudaStream_t stream);
 
 moe_status_t launch_combine(const void *y_perm, moe_dtype_t y_perm_dtype,
                             const int32_t *inv_pos, int T, int k, int d,
@@ -106,9 +108,9 @@ moe_status_t launch_router_tc(const void *x, const void *W_g, const float *bias,
 
 // bf16 tcgen05 grouped SwiGLU FFN (the bf16 layer's path).
 moe_status_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, const float *row_scale,
-                           int A_max, int d, int f, int N, const void *W_gate, const void *W_up,
-                           const void *W_down, void *h, void *y_perm, int32_t *device_status,
-                           cudaStream_t stream);
+                           int A_max, int d, int f, int N, int capacity, const void *W_gate,
+                           const void *W_up, const void *W_down, void *h, void *y_perm,
+                           int32_t *device_status, cudaStream_t stream);
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
