@@ -7,22 +7,25 @@
 // vs 总参数与专家路由", section 深入原理 (a linear layer gives N gate logits;
 // top-k softmax gives the weights).
 //
-// Layout: tokens are the MMA M operand (128 rows of x, K-major) and the
-// experts the N operand (W_g [d, N] read MN-major, N padded to a multiple of
-// 16, at most 256), so TMEM lane t holds token t's whole logit row and each
-// epilogue thread ranks its own token with a register top-k list -- no
-// logits round trip through memory and no cross-thread merge.
-// Ranking: logit descending, equal logits -> lower expert id, NaN lowest.
+// Layout: tokens are the MMA M operand (128 rows of x, K-major) and experts
+// the N operand (W_g [d, N] read MN-major), so TMEM lane t holds token t's
+// logits and each epilogue thread ranks its own token with a register top-k
+// list.  Ranking: logit descending, equal logits -> lower expert id, NaN lowest.
+//
+// Work split: one 128-token tile per cluster, one group of at most 64 experts
+// per CTA of the cluster (N = 256 -> 4 CTAs, 128 -> 2, <= 64 -> 1).  Each CTA
+// ranks its group; the cluster's first CTA merges the groups' candidate lists
+// through distributed shared memory (the comparator is a total order, so the
+// merge gives exactly the global top-k), applies the softmax and writes.
 //
 // Precision: the tensor core's fp32 accumulator loses about half an ulp per
 // accumulation step in one direction, so a long K (d = 4096..7168) alone
-// would put the gate weights ~2e-5 off.  K is therefore split over kParts
-// partial accumulators (contiguous K ranges), summed in fp32 in a fixed order
-// by the epilogue: 8x fewer steps per accumulator.  TMEM holds kParts x 64
-// columns, so experts are processed in passes of up to 64 (x re-read from L2).
+// would put the gate weights ~2e-5 off.  K is split over kParts partial
+// accumulators (contiguous K ranges), summed in fp32 in a fixed order by the
+// epilogue: 8x fewer steps per accumulator (TMEM: kParts x 64 columns).
 //
-// CTA = 6 warps (TMA producer, MMA issuer, 4 epilogue warps), persistent over
-// 128-token tiles, 4-stage mbarrier pipeline.
+// CTA = 6 warps: TMA producer, MMA issuer, 4 epilogue warps; 6-stage mbarrier
+// pipeline; every wait bounded (2 s) with a clean drain on timeout.
 #include <cuda.h>
 #include <math.h>
 
@@ -35,7 +38,7 @@ namespace {
 constexpr int kBM = 128;                      // tokens per tile
 constexpr int kBK = 64;
 constexpr int kStages = 6;
-constexpr int kMaxNE = 256;                   // experts (MMA N) limit
+constexpr int kMaxNE = 256;                   // experts limit
 constexpr int kXBytes = kBM * kBK * 2;        // 16 KB
 constexpr int kWChunk = 64 * kBK * 2;         // 8 KB: 64 experts x 64 k
 constexpr int kStageBytes = kXBytes + kWChunk;      // 24 KB
@@ -43,12 +46,14 @@ constexpr int kThreads = 192;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kMaxK = 32;
 constexpr int kParts = 8;                     // partial accumulators over K
-constexpr int kGroup = 64;                    // experts per pass (TMEM: kParts * 64 = 512)
+constexpr int kGroup = 64;                    // experts per CTA (TMEM: kParts * 64 = 512)
+constexpr int kCandOffset = kStages * kStageBytes;          // candidate lists after the stages
+constexpr int kCandBytes = 2 * kMaxK * kBM * 4;             // values + ids
 
 struct RParams {
   int T, d, N, k;
-  int ng;                    // experts per pass (multiple of 16, <= 64)
-  int passes;                // ceil(N / ng)
+  int ng;                    // experts per CTA (multiple of 16, <= 64)
+  int group_ctas;            // CTAs per cluster = ceil(N / ng)
   const float *bias;
   float *logits;             // nullable
   int32_t *topk_idx;
@@ -63,6 +68,37 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
   return ia < ib;
 }
 
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Inserts (v, e) into the sorted list of the best k; a candidate that ranks
+// below all of them moves nothing.
+template <int KMAX>
+__device__ __forceinline__ void insert_sorted(float (&bv)[KMAX], int (&bi)[KMAX], int k, float v,
+                                              int e) {
+  float cv = v;
+  int ci = e;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    if (j < k && ranks_before(cv, ci, bv[j], bi[j])) {
+      const float tv = bv[j];
+      const int ti = bi[j];
+      bv[j] = cv;
+      bi[j] = ci;
+      cv = tv;
+      ci = ti;
+    }
+  }
+}
+
 template <int KMAX>
 __global__ void __launch_bounds__(kThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX,
@@ -70,22 +106,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2], drain;
+  __shared__ uint64_t full[kStages], empty[kStages], acc_full, drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag_s, epi_ok_s;
   volatile int *abort_flag = &abort_flag_s;
   volatile int *epi_ok = &epi_ok_s;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int rank = p.group_ctas > 1 ? (int)tc::cluster_ctarank() : 0;
+  const int tile = p.group_ctas > 1 ? (int)tc::cluster_id_x() : (int)blockIdx.x;
+  const int e0 = rank * p.ng;                           // this CTA's expert group
+  const int ncol = min(p.ng, p.N - e0);
+  float *cand_v = reinterpret_cast<float *>(smem + kCandOffset);        // [KMAX][128]
+  int *cand_i = reinterpret_cast<int *>(smem + kCandOffset + KMAX * kBM * 4);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      tc::mbar_init(&acc_full[b], 1);
-      tc::mbar_init(&acc_empty[b], 4);
-    }
+    tc::mbar_init(&acc_full, 1);
     tc::mbar_init(&drain, 1);
     abort_flag_s = 0;
     tc::fence_barrier_init();
@@ -103,33 +142,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem_base = tmem_slot;
-  const int tiles = (p.T + kBM - 1) / kBM;
   const int kblocks = (p.d + kBK - 1) / kBK;
+  const int parts = kblocks < kParts ? kblocks : kParts;
+  float bv[KMAX];
+  int bi[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) { bv[j] = -INFINITY; bi[j] = INT_MAX; }
+  bool nan_seen = false;
+  bool have_list = false;
 
   if (warp == 0) {
     // ---- TMA producer: lane 0 runs a tight loop (stage/phase counters)
     if (lane == 0) {
-      const uint64_t pol_x = tc::policy_evict_last();   // re-read by every pass
+      const uint64_t pol_x = tc::policy_evict_normal();
       const uint64_t pol_w = tc::policy_evict_last();
-      const uint32_t bytes = kXBytes + kWChunk;
       int s = 0;
       uint32_t ph = 0, issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        for (int ps = 0; ps < p.passes && ok; ++ps) {
-          for (int kb = 0; kb < kblocks; ++kb) {
-            if (!tc::mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, kTimeoutNs)) {
-              ok = false;
-              break;
-            }
-            unsigned char *st = smem + s * kStageBytes;
-            tc::mbar_arrive_expect_tx(&full[s], bytes);
-            tc::tma_load_2d(st, &tmX, &full[s], kb * kBK, t * kBM, pol_x);
-            tc::tma_load_2d(st + kXBytes, &tmW, &full[s], ps * p.ng, kb * kBK, pol_w);
-            ++issued;
-            if (++s == kStages) { s = 0; ph ^= 1; }
-          }
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!tc::mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, kTimeoutNs)) {
+          ok = false;
+          break;
         }
+        unsigned char *st = smem + s * kStageBytes;
+        tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
+        tc::tma_load_2d(st, &tmX, &full[s], kb * kBK, tile * kBM, pol_x);
+        tc::tma_load_2d(st + kXBytes, &tmW, &full[s], e0, kb * kBK, pol_w);
+        ++issued;
+        if (++s == kStages) { s = 0; ph ^= 1; }
       }
       if (!ok) {
         const uint32_t first = issued >= kStages ? issued - kStages : 0;
@@ -142,133 +182,88 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---- MMA issuer: lane 0 runs a tight loop.  K block kb accumulates into
-    // partial `part`, which advances every ceil-spaced boundary bound[part].
+    // partial `part`, which advances at the ceil-spaced boundaries.
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_bf16(kBM, p.ng, /*a_mn=*/0, /*b_mn=*/1);
-      const int parts = kblocks < kParts ? kblocks : kParts;
       const uint32_t stage0 = tc::smem_u32(smem);
-      const uint64_t a_desc0 = tc::sdesc_sw128(stage0, 16, 1024);              // x, K-major
+      const uint64_t a_desc0 = tc::sdesc_sw128(stage0, 16, 1024);               // x, K-major
       const uint64_t b_desc0 = tc::sdesc_sw128(stage0 + kXBytes, kWChunk, 1024); // W, MN-major
       int s = 0;
-      uint32_t ph = 0, round = 0;
+      uint32_t ph = 0;
+      int part = 0;
+      int next_bound = (kblocks + parts - 1) / parts;   // first kb of partial 1
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        for (int ps = 0; ps < p.passes; ++ps, ++round) {
-          if (!tc::mbar_wait_bounded(&acc_empty[0], (round & 1) ^ 1, abort_flag, kTimeoutNs)) {
-            ok = false;
-            break;
-          }
-          tc::tc_fence_after();
-          int part = 0;
-          int next_bound = (kblocks + parts - 1) / parts;   // first kb of partial 1
-          for (int kb = 0; kb < kblocks; ++kb) {
-            if (!tc::mbar_wait_bounded(&full[s], ph, abort_flag, kTimeoutNs)) {
-              ok = false;
-              break;
-            }
-            tc::tc_fence_after();
-            bool first = (kb == 0);
-            if (kb == next_bound) {
-              ++part;
-              next_bound = ((part + 1) * kblocks + parts - 1) / parts;
-              first = true;
-            }
-            const uint32_t d_tmem = tmem_base + part * kGroup;
-            const uint64_t off = (uint64_t)((s * kStageBytes) >> 4);
-            const uint64_t ad = a_desc0 + off, bd = b_desc0 + off;
-            // x K-major: +32 B per 16 k (+2); W MN-major: +2048 B per 16 k (+128)
-            tc::mma_f16(d_tmem, ad, bd, idesc, first ? 0u : 1u);
-            tc::mma_f16(d_tmem, ad + 2, bd + 128, idesc, 1u);
-            tc::mma_f16(d_tmem, ad + 4, bd + 256, idesc, 1u);
-            tc::mma_f16(d_tmem, ad + 6, bd + 384, idesc, 1u);
-            tc::mma_commit(&empty[s]);
-            if (++s == kStages) { s = 0; ph ^= 1; }
-          }
-          if (!ok) break;
-          tc::mma_commit(&acc_full[0]);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!tc::mbar_wait_bounded(&full[s], ph, abort_flag, kTimeoutNs)) {
+          ok = false;
+          break;
         }
+        tc::tc_fence_after();
+        bool first = (kb == 0);
+        if (kb == next_bound) {
+          ++part;
+          next_bound = ((part + 1) * kblocks + parts - 1) / parts;
+          first = true;
+        }
+        const uint32_t d_tmem = tmem_base + part * kGroup;
+        const uint64_t off = (uint64_t)((s * kStageBytes) >> 4);
+        const uint64_t ad = a_desc0 + off, bd = b_desc0 + off;
+        // x K-major: +32 B per 16 k (+2); W MN-major: +2048 B per 16 k (+128)
+        tc::mma_f16(d_tmem, ad, bd, idesc, first ? 0u : 1u);
+        tc::mma_f16(d_tmem, ad + 2, bd + 128, idesc, 1u);
+        tc::mma_f16(d_tmem, ad + 4, bd + 256, idesc, 1u);
+        tc::mma_f16(d_tmem, ad + 6, bd + 384, idesc, 1u);
+        tc::mma_commit(&empty[s]);
+        if (++s == kStages) { s = 0; ph ^= 1; }
       }
+      if (ok) tc::mma_commit(&acc_full);
       tc::mma_commit(&drain);
       volatile int dummy = 0;
       tc::mbar_wait_bounded(&drain, 0, &dummy, kTimeoutNs);
     }
     __syncwarp();
   } else {
-    // epilogue: thread = token row (TMEM lane)
+    // ---- epilogue: thread = token row (TMEM lane)
     const int lane_grp = warp % 4;
     const int etid = threadIdx.x - 64;
-    const int row_in_tile = lane_grp * 32 + lane;
-    bool nan_seen = false;
-    const int parts = kblocks < kParts ? kblocks : kParts;
-    uint32_t round = 0;
-    bool go = true;
-    for (int t = blockIdx.x; t < tiles && go; t += gridDim.x) {
-      const int tok = t * kBM + row_in_tile;
-      float bv[KMAX];
-      int bi[KMAX];
+    const int row = lane_grp * 32 + lane;
+    const int tok = tile * kBM + row;
+    if (etid == 0)
+      *epi_ok = tc::mbar_wait_bounded(&acc_full, 0, abort_flag, kTimeoutNs) ? 1 : 0;
+    tc::named_bar(1, 128);
+    const bool go = *epi_ok != 0;
+    if (go) {
+      tc::tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(lane_grp * 32) << 16);
+      for (int c0 = 0; c0 < ncol; c0 += 32) {
+        float v32[32];
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j) { bv[j] = -INFINITY; bi[j] = INT_MAX; }
-      for (int ps = 0; ps < p.passes; ++ps, ++round) {
-        if (etid == 0)
-          *epi_ok = tc::mbar_wait_bounded(&acc_full[0], round & 1, abort_flag, kTimeoutNs) ? 1
-                                                                                           : 0;
-        tc::named_bar(1, 128);
-        go = *epi_ok != 0;
-        tc::named_bar(1, 128);
-        if (!go) break;
-        tc::tc_fence_after();
-        const uint32_t taddr = tmem_base + ((uint32_t)(lane_grp * 32) << 16);
-        const int e0 = ps * p.ng;
-        const int ncol = min(p.ng, p.N - e0);
-        for (int c0 = 0; c0 < ncol; c0 += 32) {
-          float v32[32];
+        for (int c = 0; c < 32; ++c) v32[c] = 0.f;
+        for (int q = 0; q < parts; ++q) {
+          uint32_t r[32];
+          tc::tmem_ld_32x32b_x32(taddr + q * kGroup + c0, r);
+          tc::tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) v32[c] = 0.f;
-          for (int q = 0; q < parts; ++q) {
-            uint32_t r[32];
-            tc::tmem_ld_32x32b_x32(taddr + q * kGroup + c0, r);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) v32[c] += __uint_as_float(r[c]);
-          }
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            if (c0 + c >= ncol) break;
-            const int e = e0 + c0 + c;
-            float v = v32[c];
-            if (p.bias) v += __ldg(p.bias + e);
-            nan_seen |= isnan(v);
-            if (p.logits && tok < p.T) p.logits[(size_t)tok * p.N + e] = v;
-            // insert (v, e) into the sorted list of the best k (a candidate
-            // that ranks below all of them moves nothing)
-            float cv = v;
-            int ci = e;
-#pragma unroll
-            for (int j = 0; j < KMAX; ++j) {
-              if (j < p.k && ranks_before(cv, ci, bv[j], bi[j])) {
-                const float tv = bv[j];
-                const int ti = bi[j];
-                bv[j] = cv;
-                bi[j] = ci;
-                cv = tv;
-                ci = ti;
-              }
-            }
-          }
+          for (int c = 0; c < 32; ++c) v32[c] += __uint_as_float(r[c]);
         }
-        tc::tc_fence_before();
-        if (lane == 0) tc::mbar_arrive(&acc_empty[0]);
-      }
-      if (go && tok < p.T) {
-        float s = 0.f;
 #pragma unroll
-        for (int j = 0; j < KMAX; ++j)
-          if (j < p.k) s += expf(bv[j] - bv[0]);
+        for (int c = 0; c < 32; ++c) {
+          if (c0 + c >= ncol) break;
+          const int e = e0 + c0 + c;
+          float v = v32[c];
+          if (p.bias) v += __ldg(p.bias + e);
+          nan_seen |= isnan(v);
+          if (p.logits && tok < p.T) p.logits[(size_t)tok * p.N + e] = v;
+          insert_sorted<KMAX>(bv, bi, p.k, v, e);
+        }
+      }
+      have_list = true;
+      if (p.group_ctas > 1) {
 #pragma unroll
         for (int j = 0; j < KMAX; ++j)
           if (j < p.k) {
-            p.topk_idx[(size_t)tok * p.k + j] = bi[j];
-            p.topk_w[(size_t)tok * p.k + j] = expf(bv[j] - bv[0]) / s;
+            cand_v[j * kBM + row] = bv[j];
+            cand_i[j * kBM + row] = bi[j];
           }
       }
     }
@@ -276,6 +271,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
+  if (p.group_ctas > 1) tc::cluster_sync();   // every group's list is in place
+  if (warp >= 2 && rank == 0 && have_list) {
+    const int row = (warp % 4) * 32 + lane;
+    const int tok = tile * kBM + row;
+    for (int q = 1; q < p.group_ctas; ++q) {
+      const uint32_t rv = tc::mapa_shared(cand_v, (uint32_t)q);
+      const uint32_t ri = tc::mapa_shared(cand_i, (uint32_t)q);
+      for (int j = 0; j < p.k; ++j) {
+        const float v = ld_cluster_f32(rv + (uint32_t)((j * kBM + row) * 4));
+        const int e = ld_cluster_s32(ri + (uint32_t)((j * kBM + row) * 4));
+        insert_sorted<KMAX>(bv, bi, p.k, v, e);
+      }
+    }
+    if (tok < p.T) {
+      float s = 0.f;
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (j < p.k) s += expf(bv[j] - bv[0]);
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (j < p.k) {
+          p.topk_idx[(size_t)tok * p.k + j] = bi[j];
+          p.topk_w[(size_t)tok * p.k + j] = expf(bv[j] - bv[0]) / s;
+        }
+    }
+  }
+  if (p.group_ctas > 1) tc::cluster_sync();   // peers keep their lists until read
   if (*abort_flag && threadIdx.x == 0) report(p.status, MOE_DEV_TIMEOUT);
   if (warp == 1) {
     tc::tc_fence_after();
@@ -313,6 +335,33 @@ bool encode2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, 
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int KMAX>
+moe_status_t launch_k(const CUtensorMap &tx, const CUtensorMap &tw, const RParams &p, int tiles,
+                      cudaStream_t stream) {
+  constexpr int smem = kStages * kStageBytes + kCandBytes + 1024;
+  static bool attr = false;
+  if (!attr) {
+    MOE_CUDA_TRY(cudaFuncSetAttribute(router_tc_kernel<KMAX>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    attr = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = p.group_ctas;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(tiles * p.group_ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attrs;
+  cfg.numAttrs = p.group_ctas > 1 ? 1 : 0;
+  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, router_tc_kernel<KMAX>, tx, tw, p));
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
 }  // namespace
 
 // Returns MOE_ERR_UNSUPPORTED when the shape does not suit the tensor-core
@@ -326,40 +375,12 @@ moe_status_t launch_router_tc(const void *x, const void *W_g, const float *bias,
   if (!encode2d(&tx, x, d, T, kBK, kBM) || !encode2d(&tw, W_g, N, d, 64, kBK))
     return MOE_ERR_UNSUPPORTED;
   const int ng = N < kGroup ? ((N + 15) & ~15) : kGroup;
-  RParams p{T, d, N, k, ng, (N + ng - 1) / ng, bias, logits, topk_idx, topk_w, device_status};
-  const int smem = kStages * kStageBytes + 1024;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int groups = (N + ng - 1) / ng;
+  RParams p{T, d, N, k, ng, groups, bias, logits, topk_idx, topk_w, device_status};
   const int tiles = (T + kBM - 1) / kBM;
-  const int grid = tiles < sms ? tiles : sms;
-  if (k <= 2) {
-    static bool attr2 = false;
-    if (!attr2) {
-      MOE_CUDA_TRY(cudaFuncSetAttribute(router_tc_kernel<2>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-      attr2 = true;
-    }
-    router_tc_kernel<2><<<grid, kThreads, smem, stream>>>(tx, tw, p);
-  } else if (k <= 8) {
-    static bool attr8 = false;
-    if (!attr8) {
-      MOE_CUDA_TRY(cudaFuncSetAttribute(router_tc_kernel<8>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-      attr8 = true;
-    }
-    router_tc_kernel<8><<<grid, kThreads, smem, stream>>>(tx, tw, p);
-  } else {
-    static bool attr32 = false;
-    if (!attr32) {
-      MOE_CUDA_TRY(cudaFuncSetAttribute(router_tc_kernel<32>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-      attr32 = true;
-    }
-    router_tc_kernel<32><<<grid, kThreads, smem, stream>>>(tx, tw, p);
-  }
-  MOE_LAUNCH_CHECK();
-  return MOE_OK;
+  if (k <= 2) return launch_k<2>(tx, tw, p, tiles, stream);
+  if (k <= 8) return launch_k<8>(tx, tw, p, tiles, stream);
+  return launch_k<32>(tx, tw, p, tiles, stream);
 }
 
 }  // namespace moe
