@@ -9,7 +9,7 @@
 //
 // Formulation ("swap AB"): the weights are the M operand and the expert's
 // tokens the N operand, so a tile's N is that expert's row count rounded up
-// to 32 (no padding of small experts to 128 rows).  Two CTAs of a cluster
+// to 16 (no padding of small experts to 128 rows).  Two CTAs of a cluster
 // share one MMA (tcgen05 cta_group::2, M = 256): CTA r holds 128 weight rows
 // and half of the token rows, and gets its 128 rows of D in its own tensor
 // memory.  Per CTA:
@@ -20,19 +20,20 @@
 //          the epilogue writes y_perm = row_scale * D (bf16).
 // A (weights) is read MN-major straight from W[N, K, M] by 3-D TMA boxes of
 // 64(M) x 64(K) with 128-byte swizzle; B (token rows, K contiguous) is read
-// K-major by 2-D boxes of 64(K) x {32,64,128}(rows), half a tile per CTA.
-// Sharing the token tile halves each CTA's bytes per MMA cycle, so six 32 KB
-// stages cover the ~2 us load latency that four 48 KB stages of a one-CTA
+// K-major by 2-D boxes of 64(K) x {32,64,80,128}(rows), half a sub-tile per CTA.
+// Sharing the token tile halves each CTA's bytes per MMA cycle, so 5-9 stages
+// of 20-36 KB cover the ~2 us load latency that four 48 KB stages of a one-CTA
 // tile could not (the tensor pipe sat ~30% idle waiting for data).
 //
 // CTA = 6 warps, persistent (one CTA pair per two SMs):
 //   warp 0      TMA producer (both CTAs; completions land on the even CTA's barriers)
 //   warp 1      tensor-memory allocator; MMA issuer in the even CTA
 //   warps 2..5  epilogue (tcgen05.ld of their 32 lanes, math, coalesced stores)
-// Pipelines: 6-9 shared-memory stages (full/empty mbarriers) and two
-// 256-column TMEM accumulators (acc_full/acc_empty), so the epilogue of one
-// tile overlaps the MMAs of the next.  Every wait is bounded (2 s): on timeout
-// the CTA sets MOE_DEV_TIMEOUT, drains what it issued and exits cleanly.
+// Pipelines: shared-memory stages (full/empty mbarriers) and a ring of 2 or 3
+// accumulator slots in tensor memory (acc_full/acc_empty), so the epilogue of
+// one (sub-)tile overlaps the MMAs of the next.  Every wait is bounded (2 s):
+// on timeout the CTA sets MOE_DEV_TIMEOUT, drains what it issued and exits
+// cleanly.
 #include <cuda.h>
 #include <math.h>
 
@@ -44,35 +45,45 @@ namespace {
 
 constexpr int kBM = 128;          // weight rows per CTA (MMA M = 256 per pair)
 constexpr int kBK = 64;           // K per pipeline stage (128 B of bf16)
-constexpr int kMaxBN = 256;       // MMA N limit (tokens per tile)
 constexpr int kMaxStages = 10;
 constexpr int kAChunkBytes = 64 * kBK * 2;               // 8 KB: 64 M x 64 K
 constexpr int kABytes = 2 * kAChunkBytes;                // 16 KB
 constexpr int kStageRegion = 192 * 1024;                 // shared memory for all stages
-// A stage holds 16 KB of weights and half a token tile (width/2 rows x 128 B):
-// tile width 256 -> 32 KB stages x 6; 128 -> 24 KB x 8; 64 -> 20 KB x 9.  The
-// host picks the width per layer from its expected largest expert, so narrow
-// layers (decode, capacity-limited) get more stages and more weight bytes in
-// flight.
-constexpr int kNumBoxes = 3;                             // B box heights 32/64/128
+// Token tiling.  A tile is one expert's weight pair times up to tile_cap of its
+// token rows.  Normal layers: tile_cap 64/128/256, one MMA per K-step and two
+// 256-column accumulator slots in tensor memory.  Wide layers (experts of
+// ~160-320 rows, where cutting an expert into two tiles would stream its
+// weights through the SMs twice): tile_cap 320, split into two balanced token
+// sub-tiles of <= 160 rows that share every weight stage, and three 160-column
+// slots, so one sub-tile's epilogue still overlaps the next tile's MMAs.
+// A stage holds 16 KB of weights and the tile's token rows (half per CTA):
+// tile_cap 256 -> 32 KB stages x 6; 128 -> 24 KB x 8; 64 -> 20 KB x 9;
+// wide -> 16 KB + 2 x 80 rows = 36 KB x 5.
+constexpr int kWideSub = 160;                            // sub-tile cap (wide layers)
+constexpr int kWideTile = 2 * kWideSub;
+constexpr int kSubBytes = (kWideSub / 2) * kBK * 2;      // 10 KB: 80 rows per CTA
+constexpr int kNumBoxes = 4;                             // B box heights 32/64/80/128
+constexpr int kMaxSlots = 3;
 constexpr int kEpiThreads = 128;
 constexpr int kThreads = 64 + kEpiThreads;
-constexpr uint32_t kTmemCols = 512;                      // 2 x 256-column accumulators
+constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kMaxExperts = 1024;
 
 // Epilogue staging (per 32-column chunk)
-constexpr int kUPitch = 33;                              // floats per row of the up buffer
-constexpr int kUBytes = 64 * kUPitch * 4;                // 8448
-constexpr int kOutBytes = 32 * 256;                      // 32 token rows x up to 128 bf16
+constexpr int kXPitch = 17;                              // floats per row of a swap buffer
+constexpr int kXHalf = 64 * kXPitch;                     // floats per swap buffer
+constexpr int kXBytes = 2 * kXHalf * 4;                  // 8704: gate->up and up->gate
+constexpr int kOutHalf = 32 * 128;                       // bf16 per output buffer (8 KB)
+constexpr int kOutBytes = 2 * kOutHalf * 2;              // two output buffers
 
 struct Smem {
   // offsets inside the 1024-aligned dynamic smem block
   static constexpr int stages = 0;
-  static constexpr int u = kStageRegion;
-  static constexpr int out = u + kUBytes;
+  static constexpr int x = kStageRegion;
+  static constexpr int out = x + kXBytes;
   static constexpr int bars = out + kOutBytes;                    // 8-byte aligned
-  static constexpr int nbars = 2 * kMaxStages + 4 + 1;
+  static constexpr int nbars = 2 * kMaxStages + 2 * kMaxSlots + 1;
   static constexpr int tmem_slot = bars + nbars * 8;
   static constexpr int abort_flag = tmem_slot + 4;
   static constexpr int epi_ok = abort_flag + 4;
@@ -80,6 +91,7 @@ struct Smem {
   static constexpr int total = tile_prefix + (kMaxExperts + 1) * 4;
 };
 constexpr int kSmemBytes = Smem::total + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 struct TcParams {
   const int32_t *offsets;  // [N+1]
@@ -93,24 +105,29 @@ struct TcParams {
   const float *row_scale;  // GEMM2 only (nullable)
   int32_t *status;
   int group;               // token tiles per raster group (see decode_tile)
-  int max_bn;              // token tile width cap: 64, 128 or 256
+  int tile_cap;            // token rows per tile: 64, 128, 256, or 320 (wide)
+  int wide;                // 1: tiles over 160 rows run as two sub-tiles
+  int slot_cols;           // accumulator slot width in tensor-memory columns (256 or 160)
+  int nslots;              // accumulator slots (2 or 3)
   int stages;              // pipeline stages (kStageRegion / stage_bytes)
-  int stage_bytes;         // kABytes + max_bn/2 rows x 128 B
+  int stage_bytes;         // kABytes + token rows of a stage (both sub-tiles)
 };
 
+// Token sub-tiles of a tile: rows [row0, row0 + rows0) and, for a wide tile
+// over 160 rows, [row0 + rows0, row0 + rows0 + rows1).
 struct TileInfo {
-  int e, pair, row0, rows;  // rows of this tile: [row0, row0 + rows) of the permuted rows
+  int e, pair, row0, rows0, rows1;
 };
 
-// Token tiles of an expert with n rows: ceil(n/max_bn) tiles of equal width
+// Token tiles of an expert with n rows: ceil(n/tile_cap) tiles of equal width
 // (rounded up to 32).
-__device__ __forceinline__ int token_tiles(int n, int max_bn) { return (n + max_bn - 1) / max_bn; }
+__device__ __forceinline__ int token_tiles(int n, int cap) { return (n + cap - 1) / cap; }
 __device__ __forceinline__ int tile_width(int n, int jt) {
   int w = (n + jt - 1) / jt;
   return (w + 31) & ~31;
 }
-// MMA N of a tile: its rows rounded up to 32, at least 64.
-__device__ __forceinline__ int mma_n(int rows) { return max(64, (rows + 31) & ~31); }
+// MMA N of a sub-tile: its rows rounded up to 16, at least 64.
+__device__ __forceinline__ int mma_n(int rows) { return max(64, (rows + 15) & ~15); }
 
 // prefix[e] = first global tile of expert e (pair-major inside an expert).
 __device__ void build_tile_prefix(const TcParams &p, int *prefix) {
@@ -122,7 +139,7 @@ __device__ void build_tile_prefix(const TcParams &p, int *prefix) {
       int e = e0 + lane;
       int n = 0;
       if (e < p.N) n = p.offsets[e + 1] - p.offsets[e];
-      int cnt = n > 0 ? token_tiles(n, p.max_bn) * p.pairs : 0;
+      int cnt = n > 0 ? token_tiles(n, p.tile_cap) * p.pairs : 0;
       int incl = cnt;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -151,7 +168,7 @@ __device__ __forceinline__ TileInfo decode_tile(const TcParams &p, const int *pr
   const int e = lo;
   const int base = p.offsets[e];
   const int n = p.offsets[e + 1] - base;
-  const int jt = token_tiles(n, p.max_bn);
+  const int jt = token_tiles(n, p.tile_cap);
   const int local = t - prefix[e];
   const int full_groups = jt / p.group;
   const int per_group = p.group * p.pairs;
@@ -168,18 +185,28 @@ __device__ __forceinline__ TileInfo decode_tile(const TcParams &p, const int *pr
   const int pair = idx / gsize;
   const int j = g * p.group + idx % gsize;
   const int w = tile_width(n, jt);
+  const int rows = min(w, n - j * w);
   TileInfo ti;
   ti.e = e;
   ti.pair = pair;
   ti.row0 = base + j * w;
-  ti.rows = min(w, n - j * w);
+  if (p.wide && rows > kWideSub) {
+    ti.rows0 = ((rows + 1) / 2 + 15) & ~15;   // 96..160
+    ti.rows1 = rows - ti.rows0;                // 65..160
+  } else {
+    ti.rows0 = rows;
+    ti.rows1 = 0;
+  }
   return ti;
 }
 
-// B box per CTA for a tile of MMA width n: n/2 rows -> 32, 64 or 128.
+// B box per CTA for a sub-tile of MMA width n: n/2 rows -> 32, 64, 80 or 128.
 __device__ __forceinline__ int box_index(int n_mma) {
   const int half = n_mma / 2;
-  return half <= 32 ? 0 : half <= 64 ? 1 : 2;
+  return half <= 32 ? 0 : half <= 64 ? 1 : half <= 80 ? 2 : 3;
+}
+__device__ __forceinline__ uint32_t box_bytes(int bi) {
+  return (uint32_t)(bi == 0 ? 32 : bi == 1 ? 64 : bi == 2 ? 80 : 128) * kBK * 2;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -187,16 +214,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmA1,
                     const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1,
-                    const __grid_constant__ CUtensorMap tmB2, const TcParams p) {
+                    const __grid_constant__ CUtensorMap tmB2,
+                    const __grid_constant__ CUtensorMap tmB3, const TcParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Smem::bars);
-  uint64_t *full = bars;                   // [kMaxStages] (used in the even CTA)
-  uint64_t *empty = bars + kMaxStages;     // [kMaxStages]
-  uint64_t *acc_full = bars + 2 * kMaxStages; // [2]
-  uint64_t *acc_empty = acc_full + 2;      // [2]         (used in the even CTA)
-  uint64_t *drain = acc_empty + 2;         // [1]
+  uint64_t *full = bars;                        // [kMaxStages] (used in the even CTA)
+  uint64_t *empty = bars + kMaxStages;          // [kMaxStages]
+  uint64_t *acc_full = bars + 2 * kMaxStages;   // [kMaxSlots]
+  uint64_t *acc_empty = acc_full + kMaxSlots;   // [kMaxSlots]  (used in the even CTA)
+  uint64_t *drain = acc_empty + kMaxSlots;      // [1]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::tmem_slot);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Smem::abort_flag);
   int *prefix = reinterpret_cast<int *>(smem + Smem::tile_prefix);
@@ -210,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kMaxSlots; ++b) {
       tc::mbar_init(&acc_full[b], 1);
       tc::mbar_init(&acc_empty[b], 2 * kEpiThreads / 32);
     }
@@ -225,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tma_prefetch_desc(&tmB0);
     tc::tma_prefetch_desc(&tmB1);
     tc::tma_prefetch_desc(&tmB2);
+    tc::tma_prefetch_desc(&tmB3);
   }
   if (warp == 1) {
     tc::tmem_alloc_pair(tmem_slot, kTmemCols);
@@ -255,13 +284,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = cid; t < total_tiles && ok; t += ncl) {
         const TileInfo ti = decode_tile(p, prefix, t);
-        const int n_mma = mma_n(ti.rows);
-        const int bi = box_index(n_mma);
-        const CUtensorMap *tmB = bi == 0 ? &tmB0 : bi == 1 ? &tmB1 : &tmB2;
-        const uint32_t tx = 2u * (kABytes + (uint32_t)(32 << bi) * kBK * 2);
+        const int n0 = mma_n(ti.rows0);
+        const int bi0 = box_index(n0);
+        const CUtensorMap *tb0 = bi0 == 0 ? &tmB0 : bi0 == 1 ? &tmB1 : bi0 == 2 ? &tmB2 : &tmB3;
+        const int n1 = ti.rows1 > 0 ? mma_n(ti.rows1) : 0;
+        const int bi1 = box_index(n1);
+        const CUtensorMap *tb1 = bi1 == 0 ? &tmB0 : bi1 == 1 ? &tmB1 : bi1 == 2 ? &tmB2 : &tmB3;
+        uint32_t tx = kABytes + box_bytes(bi0);
+        if (n1) tx += box_bytes(bi1);
+        tx *= 2u;   // both CTAs' bytes complete on the even CTA's barrier
         const int m0 = p.gemm1 ? ti.pair * 128 + rank * 64 : ti.pair * 256 + rank * kBM;
         const int m1 = p.gemm1 ? m0 : m0 + 64;
-        const int brow = ti.row0 + (int)rank * (n_mma / 2);
+        const int brow0 = ti.row0 + (int)rank * (n0 / 2);
+        const int brow1 = ti.row0 + ti.rows0 + (int)rank * (n1 / 2);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!tc::mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, kTimeoutNs)) {
             ok = false;
@@ -272,7 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = full_leader0 + 8u * s;
           tc::tma_load_3d_pair(st, &tmA0, fb, m0, kb * kBK, ti.e, pol_w);
           tc::tma_load_3d_pair(st + kAChunkBytes, &tmA1, fb, m1, kb * kBK, ti.e, pol_w);
-          tc::tma_load_2d_pair(st + kABytes, tmB, fb, kb * kBK, brow, pol_x);
+          tc::tma_load_2d_pair(st + kABytes, tb0, fb, kb * kBK, brow0, pol_x);
+          if (n1) tc::tma_load_2d_pair(st + kABytes + kSubBytes, tb1, fb, kb * kBK, brow1, pol_x);
           ++issued;
           if (++s == p.stages) { s = 0; ph ^= 1; }
         }
@@ -300,15 +336,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t a_desc0 = tc::sdesc_sw128(stage0, kAChunkBytes, 1024);   // MN-major A
       const uint64_t b_desc0 = tc::sdesc_sw128(stage0 + kABytes, 16, 1024);   // K-major B
       int s = 0;
-      uint32_t ph = 0, tcount = 0;
+      uint32_t ph = 0;
+      int sl = 0;          // accumulator slot of the next sub-tile (ring of p.nslots)
+      uint32_t sph = 0;    // parity of the slot ring's current round
       bool ok = true;
-      for (int t = cid; t < total_tiles && ok; t += ncl, ++tcount) {
+      for (int t = cid; t < total_tiles && ok; t += ncl) {
         const TileInfo ti = decode_tile(p, prefix, t);
-        const uint32_t idesc = tc::idesc_bf16(2 * kBM, mma_n(ti.rows), /*a_mn=*/1, /*b_mn=*/0);
-        const int buf = tcount & 1;
-        const uint32_t d_tmem = tmem_base + buf * 256;
-        if (!tc::mbar_wait_bounded(&acc_empty[buf], ((tcount >> 1) & 1) ^ 1, abort_flag,
-                                   kTimeoutNs)) { ok = false; break; }
+        const bool two = ti.rows1 > 0;
+        const uint32_t idesc0 = tc::idesc_bf16(2 * kBM, mma_n(ti.rows0), /*a_mn=*/1, /*b_mn=*/0);
+        const uint32_t idesc1 = two ? tc::idesc_bf16(2 * kBM, mma_n(ti.rows1), 1, 0) : 0u;
+        const int sl0 = sl;
+        const uint32_t sph0 = sph;
+        if (++sl == p.nslots) { sl = 0; sph ^= 1; }
+        int sl1 = sl0;
+        uint32_t sph1 = sph0;
+        if (two) {
+          sl1 = sl;
+          sph1 = sph;
+          if (++sl == p.nslots) { sl = 0; sph ^= 1; }
+        }
+        const uint32_t d0 = tmem_base + (uint32_t)(sl0 * p.slot_cols);
+        const uint32_t d1 = tmem_base + (uint32_t)(sl1 * p.slot_cols);
+        if (!tc::mbar_wait_bounded(&acc_empty[sl0], sph0 ^ 1, abort_flag, kTimeoutNs)) {
+          ok = false;
+          break;
+        }
+        if (two && !tc::mbar_wait_bounded(&acc_empty[sl1], sph1 ^ 1, abort_flag, kTimeoutNs)) {
+          ok = false;
+          break;
+        }
         tc::tc_fence_after();
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!tc::mbar_wait_bounded(&full[s], ph, abort_flag, kTimeoutNs)) {
@@ -320,15 +376,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t ad = a_desc0 + off, bd = b_desc0 + off;
           // A MN-major: 16 k-rows = two 1024-B atoms further (+128 in 16-B units);
           // B K-major: 16 k = 32 B further inside the 128-B swizzled row (+2).
-          tc::mma_f16_pair(d_tmem, ad, bd, idesc, kb > 0 ? 1u : 0u);
-          tc::mma_f16_pair(d_tmem, ad + 128, bd + 2, idesc, 1u);
-          tc::mma_f16_pair(d_tmem, ad + 256, bd + 4, idesc, 1u);
-          tc::mma_f16_pair(d_tmem, ad + 384, bd + 6, idesc, 1u);
+          tc::mma_f16_pair(d0, ad, bd, idesc0, kb > 0 ? 1u : 0u);
+          tc::mma_f16_pair(d0, ad + 128, bd + 2, idesc0, 1u);
+          tc::mma_f16_pair(d0, ad + 256, bd + 4, idesc0, 1u);
+          tc::mma_f16_pair(d0, ad + 384, bd + 6, idesc0, 1u);
+          if (two) {
+            const uint64_t bd1 = bd + (kSubBytes >> 4);   // second sub-tile's token rows
+            tc::mma_f16_pair(d1, ad, bd1, idesc1, kb > 0 ? 1u : 0u);
+            tc::mma_f16_pair(d1, ad + 128, bd1 + 2, idesc1, 1u);
+            tc::mma_f16_pair(d1, ad + 256, bd1 + 4, idesc1, 1u);
+            tc::mma_f16_pair(d1, ad + 384, bd1 + 6, idesc1, 1u);
+          }
           tc::mma_commit_pair(&empty[s], 0x3);  // frees the stage in both CTAs
           if (++s == p.stages) { s = 0; ph ^= 1; }
         }
         if (!ok) break;
-        tc::mma_commit_pair(&acc_full[buf], 0x3);
+        tc::mma_commit_pair(&acc_full[sl0], 0x3);
+        if (two) tc::mma_commit_pair(&acc_full[sl1], 0x3);
       }
       // Drain: make sure no MMA is still reading shared or writing tensor memory.
       tc::mma_commit_pair(drain, 0x1);
@@ -341,88 +405,105 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane_grp = warp % 4;           // TMEM lanes 32*lane_grp .. +31
     const int etid = threadIdx.x - 64;       // 0..127
     volatile int *epi_ok = reinterpret_cast<volatile int *>(smem + Smem::epi_ok);
-    float *ubuf = reinterpret_cast<float *>(smem + Smem::u);
+    float *xbuf = reinterpret_cast<float *>(smem + Smem::x);
     __nv_bfloat16 *obuf = reinterpret_cast<__nv_bfloat16 *>(smem + Smem::out);
-    const uint32_t acc_empty_leader[2] = {tc::mapa_shared(&acc_empty[0], 0),
-                                          tc::mapa_shared(&acc_empty[1], 0)};
-    uint32_t tcount = 0;
-    for (int t = cid; t < total_tiles; t += ncl, ++tcount) {
+    int sl = 0;
+    uint32_t sph = 0;
+    uint32_t obi = 0;     // output buffer parity (GEMM2 alternates two buffers)
+    bool go_on = true;
+    for (int t = cid; t < total_tiles && go_on; t += ncl) {
       const TileInfo ti = decode_tile(p, prefix, t);
-      const int buf = tcount & 1;
-      // One thread waits (bounded) and the outcome is shared, so the four
-      // epilogue warps always leave the loop together.
-      if (etid == 0)
-        *epi_ok = tc::mbar_wait_bounded(&acc_full[buf], (tcount >> 1) & 1, abort_flag,
-                                        kTimeoutNs) ? 1 : 0;
-      tc::named_bar(1, kEpiThreads);
-      const int go = *epi_ok;
-      tc::named_bar(1, kEpiThreads);
-      if (!go) break;
-      tc::tc_fence_after();
-      const uint32_t t_base = tmem_base + ((uint32_t)(lane_grp * 32) << 16) + buf * 256;
-      const int nchunks = (ti.rows + 31) / 32;
-      for (int cc = 0; cc < nchunks; ++cc) {
-        uint32_t r[32];
-        tc::tmem_ld_32x32b_x32(t_base + cc * 32, r);
-        tc::tmem_ld_wait();
-        const int ncols = min(32, ti.rows - cc * 32);
-        if (p.gemm1) {
-          // lanes 64..127 (up) hand their values to lanes 0..63 (gate)
-          if (lane_grp >= 2) {
-            float *urow = ubuf + ((lane_grp - 2) * 32 + lane) * kUPitch;
+      const int nsub = ti.rows1 > 0 ? 2 : 1;
+      for (int sub = 0; sub < nsub; ++sub) {
+        const int slot = sl;
+        const uint32_t par = sph;
+        if (++sl == p.nslots) { sl = 0; sph ^= 1; }
+        const int srow0 = ti.row0 + (sub ? ti.rows0 : 0);   // first permuted row of the sub-tile
+        const int srows = sub ? ti.rows1 : ti.rows0;
+        // One thread waits (bounded) and the outcome is shared, so the four
+        // epilogue warps always leave the loop together.
+        if (etid == 0)
+          *epi_ok = tc::mbar_wait_bounded(&acc_full[slot], par, abort_flag, kTimeoutNs) ? 1 : 0;
+        tc::named_bar(1, kEpiThreads);
+        const int go = *epi_ok;
+        tc::named_bar(1, kEpiThreads);
+        if (!go) {
+          go_on = false;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t t_base = tmem_base + ((uint32_t)(lane_grp * 32) << 16) +
+                                (uint32_t)(slot * p.slot_cols);
+        const int nchunks = (srows + 31) / 32;
+        for (int cc = 0; cc < nchunks; ++cc) {
+          uint32_t r[32];
+          tc::tmem_ld_32x32b_x32(t_base + cc * 32, r);
+          tc::tmem_ld_wait();
+          const int ncols = min(32, srows - cc * 32);
+          if (p.gemm1) {
+            // Gate lanes (lane_grp 0,1) and up lanes (2,3) of the same hidden
+            // unit hand each other half of the 32 token columns, so all four
+            // warps compute SiLU(gate) * up for 16 columns.
+            const bool gate_side = lane_grp < 2;
+            const int hr = (lane_grp & 1) * 32 + lane;     // hidden unit within the slab
+            float *mine = xbuf + (gate_side ? kXHalf : 0) + hr * kXPitch;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) urow[c] = __uint_as_float(r[c]);
-          }
-          tc::named_bar(1, kEpiThreads);
-          if (lane_grp < 2) {
-            const int hr = lane_grp * 32 + lane;          // hidden unit within the slab
-            const float *urow = ubuf + hr * kUPitch;
+            for (int c = 0; c < 16; ++c)
+              mine[c] = gate_side ? __uint_as_float(r[16 + c]) : __uint_as_float(r[c]);
+            tc::named_bar(1, kEpiThreads);
+            const float *other = xbuf + (gate_side ? 0 : kXHalf) + hr * kXPitch;
+            __nv_bfloat16 *ob = obuf + (gate_side ? 0 : 16 * 64);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const float o = other[c];
+              const float g = gate_side ? __uint_as_float(r[c]) : o;
+              const float u = gate_side ? o : __uint_as_float(r[16 + c]);
+              const float h = __fdividef(g, 1.f + __expf(-g)) * u;
+              ob[c * 64 + hr] = __float2bfloat16_rn(h);
+            }
+            tc::named_bar(1, kEpiThreads);
+            // copy out: ncols token rows x 64 hidden units (128 B) each.  The
+            // next chunk writes obuf only after its exchange barrier, which
+            // every thread reaches after finishing this copy.
+            const int m0 = ti.pair * 128 + rank * 64;
+            const int vec_valid = max(0, min(8, (p.M - m0) / 8));
+            for (int q = etid; q < ncols * 8; q += kEpiThreads) {
+              const int c = q / 8, v = q % 8;
+              if (v < vec_valid) {
+                const uint4 val = *reinterpret_cast<const uint4 *>(obuf + c * 64 + v * 8);
+                *reinterpret_cast<uint4 *>(p.out + (size_t)(srow0 + cc * 32 + c) * p.out_ld +
+                                           m0 + v * 8) = val;
+              }
+            }
+          } else {
+            // scale each token column by its gate weight; two output buffers
+            // alternate, so a chunk's writes never meet the previous chunk's copy
+            __nv_bfloat16 *ob = obuf + (obi & 1) * kOutHalf;
+            ++obi;
+            float scl = 1.f;
+            if (p.row_scale && lane < ncols) scl = p.row_scale[srow0 + cc * 32 + lane];
+            const int dr = lane_grp * 32 + lane;             // output column within the slab
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-              const float g = __uint_as_float(r[c]);
-              const float h = g / (1.f + __expf(-g)) * urow[c];
-              obuf[c * 64 + hr] = __float2bfloat16_rn(h);
+              const float sv = __shfl_sync(0xffffffffu, scl, c);
+              ob[c * 128 + dr] = __float2bfloat16_rn(__uint_as_float(r[c]) * sv);
+            }
+            tc::named_bar(1, kEpiThreads);
+            const int m0 = ti.pair * 256 + rank * kBM;
+            const int vec_valid = max(0, min(16, (p.M - m0) / 8));
+            for (int q = etid; q < ncols * 16; q += kEpiThreads) {
+              const int c = q / 16, v = q % 16;
+              if (v < vec_valid) {
+                const uint4 val = *reinterpret_cast<const uint4 *>(ob + c * 128 + v * 8);
+                *reinterpret_cast<uint4 *>(p.out + (size_t)(srow0 + cc * 32 + c) * p.out_ld +
+                                           m0 + v * 8) = val;
+              }
             }
           }
-          tc::named_bar(1, kEpiThreads);
-          // copy out: ncols token rows x 64 hidden units (128 B) each
-          const int m0 = ti.pair * 128 + rank * 64;
-          const int vec_valid = max(0, min(8, (p.M - m0) / 8));
-          for (int q = etid; q < ncols * 8; q += kEpiThreads) {
-            const int c = q / 8, v = q % 8;
-            if (v < vec_valid) {
-              const uint4 val = *reinterpret_cast<const uint4 *>(obuf + c * 64 + v * 8);
-              *reinterpret_cast<uint4 *>(p.out + (size_t)(ti.row0 + cc * 32 + c) * p.out_ld +
-                                         m0 + v * 8) = val;
-            }
-          }
-          tc::named_bar(1, kEpiThreads);
-        } else {
-          // scale each token column by its gate weight
-          float sc = 1.f;
-          if (p.row_scale && lane < ncols) sc = p.row_scale[ti.row0 + cc * 32 + lane];
-          const int dr = lane_grp * 32 + lane;             // output column within the slab
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float sv = __shfl_sync(0xffffffffu, sc, c);
-            obuf[c * 128 + dr] = __float2bfloat16_rn(__uint_as_float(r[c]) * sv);
-          }
-          tc::named_bar(1, kEpiThreads);
-          const int m0 = ti.pair * 256 + rank * kBM;
-          const int vec_valid = max(0, min(16, (p.M - m0) / 8));
-          for (int q = etid; q < ncols * 16; q += kEpiThreads) {
-            const int c = q / 16, v = q % 16;
-            if (v < vec_valid) {
-              const uint4 val = *reinterpret_cast<const uint4 *>(obuf + c * 128 + v * 8);
-              *reinterpret_cast<uint4 *>(p.out + (size_t)(ti.row0 + cc * 32 + c) * p.out_ld +
-                                         m0 + v * 8) = val;
-            }
-          }
-          tc::named_bar(1, kEpiThreads);
         }
+        tc::tc_fence_before();
+        if (lane == 0) tc::mbar_arrive_cluster(tc::mapa_shared(&acc_empty[slot], 0));
       }
-      tc::tc_fence_before();
-      if (lane == 0) tc::mbar_arrive_cluster(acc_empty_leader[buf]);
     }
   }
 
@@ -536,7 +617,7 @@ moe_status_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUt
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, grouped_gemm_tc, a0, a1, b[0], b[1], b[2], p));
+  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, grouped_gemm_tc, a0, a1, b[0], b[1], b[2], b[3], p));
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
@@ -560,30 +641,38 @@ moe_status_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, const flo
   CUtensorMap wg, wu, wd, bx[kNumBoxes], bh[kNumBoxes];
   bool ok = make_weight_map(&wg, W_gate, N, d, f) && make_weight_map(&wu, W_up, N, d, f) &&
             make_weight_map(&wd, W_down, N, f, d);
+  const int box_rows[kNumBoxes] = {32, 64, 80, 128};
   for (int i = 0; i < kNumBoxes; ++i) {
-    ok = ok && make_rows_map(&bx[i], x_perm, A_max, d, 32 << i) &&
-         make_rows_map(&bh[i], h, A_max, f, 32 << i);
+    ok = ok && make_rows_map(&bx[i], x_perm, A_max, d, box_rows[i]) &&
+         make_rows_map(&bh[i], h, A_max, f, box_rows[i]);
   }
   if (!ok) {
     set_error("tensor map encoding failed (alignment or size)");
     return MOE_ERR_INVALID_ARG;
   }
-  // Token tile width cap: the expected largest expert (1.25x the average rows,
-  // or the capacity when that is smaller) rounded up to 64/128/256.  Narrow
-  // layers then fit more, smaller stages.
+  // Token tile width: the expected largest expert (1.25x the average rows, or
+  // the capacity when that is smaller) rounded up to 64/128/256, so narrow
+  // layers fit more, smaller stages.  Layers whose experts run ~160-320 rows
+  // (most experts just over or under 256) take wide tiles instead, which keep
+  // such an expert in one tile.
   const long avg_rows = ((long)A_max + N - 1) / N;
   long exp_rows = avg_rows + avg_rows / 4;
   if (capacity > 0 && capacity < exp_rows) exp_rows = capacity;
-  const int max_bn = exp_rows > 128 ? 256 : exp_rows > 64 ? 128 : 64;
-  const int stage_bytes = kABytes + (max_bn / 2) * kBK * 2;
+  const int wide = (exp_rows > 256 && avg_rows <= 320) ? 1 : 0;
+  const int tile_cap = wide ? kWideTile : exp_rows > 128 ? 256 : exp_rows > 64 ? 128 : 64;
+  const int stage_bytes = wide ? kABytes + 2 * kSubBytes : kABytes + (tile_cap / 2) * kBK * 2;
+  const int slot_cols = wide ? kWideSub : 256;
+  const int nslots = wide ? 3 : 2;
   int stages = kStageRegion / stage_bytes;
   if (stages > kMaxStages) stages = kMaxStages;
   TcParams p1{offsets, N, d, f, (f + 127) / 128, 1, static_cast<__nv_bfloat16 *>(h), f, nullptr,
-              device_status, raster_group(d), max_bn, stages, stage_bytes};
+              device_status, raster_group(d), tile_cap, wide, slot_cols, nslots, stages,
+              stage_bytes};
   moe_status_t s = launch_gemm(wg, wu, bx, p1, stream);
   if (s != MOE_OK) return s;
   TcParams p2{offsets, N, f, d, (d + 255) / 256, 0, static_cast<__nv_bfloat16 *>(y_perm), d,
-              row_scale, device_status, raster_group(f), max_bn, stages, stage_bytes};
+              row_scale, device_status, raster_group(f), tile_cap, wide, slot_cols, nslots,
+              stages, stage_bytes};
   return launch_gemm(wd, wd, bh, p2, stream);
 }
 

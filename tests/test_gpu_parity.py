@@ -36,6 +36,9 @@ REDUCED = {
     "k_equals_n": MoEConfig("k_equals_n", T=64, d=64, f=64, N=4, k=4, seed=74),
     "many_rows": MoEConfig("many_rows", T=2048, d=256, f=320, N=4, k=2, bias_std=1.0, seed=75),
     "odd_dims": MoEConfig("odd_dims", T=173, d=200, f=136, N=6, k=2, fs=72, seed=76),
+    # ~300 rows per expert: tiles of one 256-row and one <=64-row token sub-tile
+    "wide_tiles": MoEConfig("wide_tiles", T=1200, d=256, f=192, N=8, k=2, bias_std=0.4,
+                            seed=77),
 }
 
 
@@ -168,7 +171,7 @@ def test_permute_repeat_bit_identical():
 
 
 @pytest.mark.parametrize("name", ["tiny", "mixtral_small", "deepseek_small", "f32_wide",
-                                  "many_rows", "odd_dims", "ragged_257"])
+                                  "many_rows", "odd_dims", "ragged_257", "wide_tiles"])
 def test_expert_ffn_stage(name):
     """y_perm rows = row_scale * SwiGLU_e(x_perm) against the oracle's expert rows."""
     cfg = REDUCED[name]
@@ -188,6 +191,35 @@ def test_expert_ffn_stage(name):
                                                         inp.W_down[e].cpu(), xp[off[e]:off[e + 1]])
     ref *= rs[:off[-1], None]
     parity.assert_y_close(y_perm[:off[-1]].float().cpu().numpy(), ref, cfg.dtype)
+
+
+@pytest.mark.parametrize("counts", [
+    # ~340 rows per expert: 256-row tiles; experts split into 2-4 tiles
+    [0, 1, 256, 257, 288, 320, 321, 600, 641, 100, 0, 960],
+    # ~280 rows per expert: wide tiles (two balanced sub-tiles above 160 rows)
+    [0, 1, 160, 161, 255, 256, 257, 288, 320, 321, 600, 641, 100, 0, 960, 200],
+])
+def test_expert_ffn_crafted_counts(counts):
+    """Expert sizes on every tiling edge of the grouped GEMMs: empty, one row,
+    one sub-tile, two sub-tiles, and experts split into two or three tiles."""
+    N, d, f = len(counts), 256, 192
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    A = int(off[-1])
+    g = torch.Generator().manual_seed(78)
+    xp = (torch.randn((A, d), generator=g) * 0.5).to(torch.bfloat16)
+    Wg = (torch.randn((N, d, f), generator=g) * d ** -0.5).to(torch.bfloat16)
+    Wu = (torch.randn((N, d, f), generator=g) * d ** -0.5).to(torch.bfloat16)
+    Wd = (torch.randn((N, f, d), generator=g) * f ** -0.5).to(torch.bfloat16)
+    rs = torch.rand((A,), generator=g) + 0.5
+    y = B.moe_expert_ffn(xp.cuda(), torch.from_numpy(off).cuda(), Wg.cuda(), Wu.cuda(),
+                         Wd.cuda(), row_scale=rs.cuda())
+    torch.cuda.synchronize()
+    ref = np.zeros((A, d))
+    for e in range(N):
+        if counts[e]:
+            ref[off[e]:off[e + 1]] = oracle.expert_rows(Wg[e], Wu[e], Wd[e], xp[off[e]:off[e + 1]])
+    ref *= rs.double().numpy()[:, None]
+    parity.assert_y_close(y[:A].float().cpu().numpy(), ref, "bf16")
 
 
 def test_combine_stage():
