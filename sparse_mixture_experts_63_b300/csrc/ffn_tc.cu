@@ -29,9 +29,9 @@
 //   warp 0      TMA producer (both CTAs; completions land on the even CTA's barriers)
 //   warp 1      tensor-memory allocator; MMA issuer in the even CTA
 //   warps 2..5  epilogue (tcgen05.ld of their 32 lanes, math, coalesced stores)
-// Pipelines: shared-memory stages (full/empty mbarriers) and a ring of 2 or 3
-// accumulator slots in tensor memory (acc_full/acc_empty), so the epilogue of
-// one (sub-)tile overlaps the MMAs of the next.  Every wait is bounded (2 s):
+// Pipelines: shared-memory stages (full/empty mbarriers) and a ring of 32-column
+// accumulator chunks in tensor memory (acc_full per sub-tile, col_free per
+// chunk), so the epilogue of one (sub-)tile overlaps the MMAs of the next.  Every wait is bounded (2 s):
 // on timeout the CTA sets MOE_DEV_TIMEOUT, drains what it issued and exits
 // cleanly.
 #include <cuda.h>
@@ -50,20 +50,25 @@ constexpr int kAChunkBytes = 64 * kBK * 2;               // 8 KB: 64 M x 64 K
 constexpr int kABytes = 2 * kAChunkBytes;                // 16 KB
 constexpr int kStageRegion = 192 * 1024;                 // shared memory for all stages
 // Token tiling.  A tile is one expert's weight pair times up to tile_cap of its
-// token rows.  Normal layers: tile_cap 64/128/256, one MMA per K-step and two
-// 256-column accumulator slots in tensor memory.  Wide layers (experts of
-// ~160-320 rows, where cutting an expert into two tiles would stream its
-// weights through the SMs twice): tile_cap 320, split into two balanced token
-// sub-tiles of <= 160 rows that share every weight stage, and three 160-column
-// slots, so one sub-tile's epilogue still overlaps the next tile's MMAs.
+// token rows: tile_cap 64/128/256, one MMA (N <= 256) per 16 K.  Wide layers
+// (experts of ~250-320 rows, where cutting an expert into two tiles would
+// stream its weights through the SMs twice) take tile_cap 320: a tile over 256
+// rows runs as two balanced token sub-tiles of <= 160 rows that share every
+// weight stage (two MMAs per 16 K).
 // A stage holds 16 KB of weights and the tile's token rows (half per CTA):
 // tile_cap 256 -> 32 KB stages x 6; 128 -> 24 KB x 8; 64 -> 20 KB x 9;
 // wide -> 16 KB + 2 x 80 rows = 36 KB x 5.
-constexpr int kWideSub = 160;                            // sub-tile cap (wide layers)
+// Accumulators: tensor memory is a ring of 16 chunks of 32 columns; each
+// sub-tile takes ceil(N/32) consecutive chunks (wrapping to chunk 0 when the
+// rest of the ring is too short), and the epilogue hands every chunk back as
+// soon as it has loaded it, so the next sub-tile's MMAs start while the
+// epilogue still works on the previous one.
+constexpr int kWideSub = 160;                            // sub-tile cap in a split wide tile
 constexpr int kWideTile = 2 * kWideSub;
 constexpr int kSubBytes = (kWideSub / 2) * kBK * 2;      // 10 KB: 80 rows per CTA
 constexpr int kNumBoxes = 4;                             // B box heights 32/64/80/128
-constexpr int kMaxSlots = 3;
+constexpr int kChunks = 16;                              // 32-column chunks of tensor memory
+constexpr int kAccRing = 16;                             // acc_full barriers (sub-tile ring)
 constexpr int kEpiThreads = 128;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr uint32_t kTmemCols = 512;
@@ -83,7 +88,7 @@ struct Smem {
   static constexpr int x = kStageRegion;
   static constexpr int out = x + kXBytes;
   static constexpr int bars = out + kOutBytes;                    // 8-byte aligned
-  static constexpr int nbars = 2 * kMaxStages + 2 * kMaxSlots + 1;
+  static constexpr int nbars = 2 * kMaxStages + kAccRing + kChunks + 1;
   static constexpr int tmem_slot = bars + nbars * 8;
   static constexpr int abort_flag = tmem_slot + 4;
   static constexpr int epi_ok = abort_flag + 4;
@@ -106,15 +111,13 @@ struct TcParams {
   int32_t *status;
   int group;               // token tiles per raster group (see decode_tile)
   int tile_cap;            // token rows per tile: 64, 128, 256, or 320 (wide)
-  int wide;                // 1: tiles over 160 rows run as two sub-tiles
-  int slot_cols;           // accumulator slot width in tensor-memory columns (256 or 160)
-  int nslots;              // accumulator slots (2 or 3)
+  int wide;                // 1: tiles over 256 rows run as two sub-tiles
   int stages;              // pipeline stages (kStageRegion / stage_bytes)
   int stage_bytes;         // kABytes + token rows of a stage (both sub-tiles)
 };
 
 // Token sub-tiles of a tile: rows [row0, row0 + rows0) and, for a wide tile
-// over 160 rows, [row0 + rows0, row0 + rows0 + rows1).
+// over 256 rows, [row0 + rows0, row0 + rows0 + rows1).
 struct TileInfo {
   int e, pair, row0, rows0, rows1;
 };
@@ -190,9 +193,9 @@ __device__ __forceinline__ TileInfo decode_tile(const TcParams &p, const int *pr
   ti.e = e;
   ti.pair = pair;
   ti.row0 = base + j * w;
-  if (p.wide && rows > kWideSub) {
-    ti.rows0 = ((rows + 1) / 2 + 15) & ~15;   // 96..160
-    ti.rows1 = rows - ti.rows0;                // 65..160
+  if (p.wide && rows > 256) {
+    ti.rows0 = ((rows + 1) / 2 + 15) & ~15;   // 144..160
+    ti.rows1 = rows - ti.rows0;                // 113..160
   } else {
     ti.rows0 = rows;
     ti.rows1 = 0;
@@ -209,6 +212,16 @@ __device__ __forceinline__ uint32_t box_bytes(int bi) {
   return (uint32_t)(bi == 0 ? 32 : bi == 1 ? 64 : bi == 2 ? 80 : 128) * kBK * 2;
 }
 
+// Tensor-memory chunks of a sub-tile of MMA width n, taken from the ring at
+// *pos (wrapping to 0 when fewer than needed remain before the end).
+__device__ __forceinline__ int ring_take(int &pos, int n_mma) {
+  const int nch = (n_mma + 31) / 32;
+  if (pos + nch > kChunks) pos = 0;
+  const int c0 = pos;
+  pos += nch;
+  return c0;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
@@ -222,9 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Smem::bars);
   uint64_t *full = bars;                        // [kMaxStages] (used in the even CTA)
   uint64_t *empty = bars + kMaxStages;          // [kMaxStages]
-  uint64_t *acc_full = bars + 2 * kMaxStages;   // [kMaxSlots]
-  uint64_t *acc_empty = acc_full + kMaxSlots;   // [kMaxSlots]  (used in the even CTA)
-  uint64_t *drain = acc_empty + kMaxSlots;      // [1]
+  uint64_t *acc_full = bars + 2 * kMaxStages;   // [kAccRing] sub-tile accumulated
+  uint64_t *col_free = acc_full + kAccRing;     // [kChunks]  chunk loaded by the epilogue
+                                                //            (used in the even CTA)
+  uint64_t *drain = col_free + kChunks;         // [1]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::tmem_slot);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Smem::abort_flag);
   int *prefix = reinterpret_cast<int *>(smem + Smem::tile_prefix);
@@ -238,10 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < kMaxSlots; ++b) {
-      tc::mbar_init(&acc_full[b], 1);
-      tc::mbar_init(&acc_empty[b], 2 * kEpiThreads / 32);
-    }
+    for (int b = 0; b < kAccRing; ++b) tc::mbar_init(&acc_full[b], 1);
+    for (int c = 0; c < kChunks; ++c) tc::mbar_init(&col_free[c], 2 * kEpiThreads / 32);
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
@@ -337,34 +349,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t b_desc0 = tc::sdesc_sw128(stage0 + kABytes, 16, 1024);   // K-major B
       int s = 0;
       uint32_t ph = 0;
-      int sl = 0;          // accumulator slot of the next sub-tile (ring of p.nslots)
-      uint32_t sph = 0;    // parity of the slot ring's current round
+      int pos = 0;              // tensor-memory ring position (chunks)
+      uint32_t cuse = 0;        // bit c: parity of chunk c's uses so far
+      uint32_t k = 0;           // token sub-tiles so far
       bool ok = true;
       for (int t = cid; t < total_tiles && ok; t += ncl) {
         const TileInfo ti = decode_tile(p, prefix, t);
         const bool two = ti.rows1 > 0;
-        const uint32_t idesc0 = tc::idesc_bf16(2 * kBM, mma_n(ti.rows0), /*a_mn=*/1, /*b_mn=*/0);
-        const uint32_t idesc1 = two ? tc::idesc_bf16(2 * kBM, mma_n(ti.rows1), 1, 0) : 0u;
-        const int sl0 = sl;
-        const uint32_t sph0 = sph;
-        if (++sl == p.nslots) { sl = 0; sph ^= 1; }
-        int sl1 = sl0;
-        uint32_t sph1 = sph0;
+        const int n0 = mma_n(ti.rows0), n1 = two ? mma_n(ti.rows1) : 0;
+        const uint32_t idesc0 = tc::idesc_bf16(2 * kBM, n0, /*a_mn=*/1, /*b_mn=*/0);
+        const uint32_t idesc1 = two ? tc::idesc_bf16(2 * kBM, n1, 1, 0) : 0u;
+        const int c0 = ring_take(pos, n0);
+        const int c1 = two ? ring_take(pos, n1) : c0;
+        // every chunk of the sub-tiles must have been loaded by the epilogue
+        // since its previous use
+        const int e0 = c0 + (n0 + 31) / 32;
+        for (int c = c0; c < e0 && ok; ++c) {
+          ok = tc::mbar_wait_bounded(&col_free[c], ((cuse >> c) & 1) ^ 1, abort_flag, kTimeoutNs);
+          cuse ^= 1u << c;
+        }
         if (two) {
-          sl1 = sl;
-          sph1 = sph;
-          if (++sl == p.nslots) { sl = 0; sph ^= 1; }
+          const int e1 = c1 + (n1 + 31) / 32;
+          for (int c = c1; c < e1 && ok; ++c) {
+            ok = tc::mbar_wait_bounded(&col_free[c], ((cuse >> c) & 1) ^ 1, abort_flag,
+                                       kTimeoutNs);
+            cuse ^= 1u << c;
+          }
         }
-        const uint32_t d0 = tmem_base + (uint32_t)(sl0 * p.slot_cols);
-        const uint32_t d1 = tmem_base + (uint32_t)(sl1 * p.slot_cols);
-        if (!tc::mbar_wait_bounded(&acc_empty[sl0], sph0 ^ 1, abort_flag, kTimeoutNs)) {
-          ok = false;
-          break;
-        }
-        if (two && !tc::mbar_wait_bounded(&acc_empty[sl1], sph1 ^ 1, abort_flag, kTimeoutNs)) {
-          ok = false;
-          break;
-        }
+        if (!ok) break;
+        const uint32_t d0 = tmem_base + (uint32_t)(c0 * 32);
+        const uint32_t d1 = tmem_base + (uint32_t)(c1 * 32);
         tc::tc_fence_after();
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!tc::mbar_wait_bounded(&full[s], ph, abort_flag, kTimeoutNs)) {
@@ -391,8 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++s == p.stages) { s = 0; ph ^= 1; }
         }
         if (!ok) break;
-        tc::mma_commit_pair(&acc_full[sl0], 0x3);
-        if (two) tc::mma_commit_pair(&acc_full[sl1], 0x3);
+        tc::mma_commit_pair(&acc_full[k % kAccRing], 0x3);
+        if (two) tc::mma_commit_pair(&acc_full[(k + 1) % kAccRing], 0x3);
+        k += two ? 2 : 1;
       }
       // Drain: make sure no MMA is still reading shared or writing tensor memory.
       tc::mma_commit_pair(drain, 0x1);
@@ -407,23 +422,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *epi_ok = reinterpret_cast<volatile int *>(smem + Smem::epi_ok);
     float *xbuf = reinterpret_cast<float *>(smem + Smem::x);
     __nv_bfloat16 *obuf = reinterpret_cast<__nv_bfloat16 *>(smem + Smem::out);
-    int sl = 0;
-    uint32_t sph = 0;
+    int pos = 0;          // tensor-memory ring position, as in the MMA issuer
+    uint32_t k = 0;       // token sub-tiles so far
     uint32_t obi = 0;     // output buffer parity (GEMM2 alternates two buffers)
     bool go_on = true;
     for (int t = cid; t < total_tiles && go_on; t += ncl) {
       const TileInfo ti = decode_tile(p, prefix, t);
       const int nsub = ti.rows1 > 0 ? 2 : 1;
       for (int sub = 0; sub < nsub; ++sub) {
-        const int slot = sl;
-        const uint32_t par = sph;
-        if (++sl == p.nslots) { sl = 0; sph ^= 1; }
         const int srow0 = ti.row0 + (sub ? ti.rows0 : 0);   // first permuted row of the sub-tile
         const int srows = sub ? ti.rows1 : ti.rows0;
+        const int n_mma = mma_n(srows);
+        const int c0 = ring_take(pos, n_mma);
+        const int nalloc = (n_mma + 31) / 32;
+        const uint32_t par = (k / kAccRing) & 1;
+        uint64_t *accb = &acc_full[k % kAccRing];
+        ++k;
         // One thread waits (bounded) and the outcome is shared, so the four
         // epilogue warps always leave the loop together.
         if (etid == 0)
-          *epi_ok = tc::mbar_wait_bounded(&acc_full[slot], par, abort_flag, kTimeoutNs) ? 1 : 0;
+          *epi_ok = tc::mbar_wait_bounded(accb, par, abort_flag, kTimeoutNs) ? 1 : 0;
         tc::named_bar(1, kEpiThreads);
         const int go = *epi_ok;
         tc::named_bar(1, kEpiThreads);
@@ -433,12 +451,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::tc_fence_after();
         const uint32_t t_base = tmem_base + ((uint32_t)(lane_grp * 32) << 16) +
-                                (uint32_t)(slot * p.slot_cols);
+                                (uint32_t)(c0 * 32);
         const int nchunks = (srows + 31) / 32;
+        // chunks the MMA wrote but that hold no rows (N rounded up) go back at once
+        for (int cc = nchunks; cc < nalloc; ++cc) {
+          tc::tc_fence_before();
+          if (lane == 0) tc::mbar_arrive_cluster_relaxed(tc::mapa_shared(&col_free[c0 + cc], 0));
+        }
         for (int cc = 0; cc < nchunks; ++cc) {
           uint32_t r[32];
           tc::tmem_ld_32x32b_x32(t_base + cc * 32, r);
           tc::tmem_ld_wait();
+          // the chunk is in registers: hand it back to the MMA issuer (relaxed:
+          // the loads have completed; nothing else needs ordering)
+          tc::tc_fence_before();
+          if (lane == 0) tc::mbar_arrive_cluster_relaxed(tc::mapa_shared(&col_free[c0 + cc], 0));
           const int ncols = min(32, srows - cc * 32);
           if (p.gemm1) {
             // Gate lanes (lane_grp 0,1) and up lanes (2,3) of the same hidden
@@ -501,8 +528,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        tc::tc_fence_before();
-        if (lane == 0) tc::mbar_arrive_cluster(tc::mapa_shared(&acc_empty[slot], 0));
       }
     }
   }
@@ -652,27 +677,23 @@ moe_status_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, const flo
   }
   // Token tile width: the expected largest expert (1.25x the average rows, or
   // the capacity when that is smaller) rounded up to 64/128/256, so narrow
-  // layers fit more, smaller stages.  Layers whose experts run ~160-320 rows
-  // (most experts just over or under 256) take wide tiles instead, which keep
-  // such an expert in one tile.
+  // layers fit more, smaller stages.  Layers whose experts run ~250-320 rows
+  // (many experts just over 256) take wide tiles instead, which keep such an
+  // expert in one tile.
   const long avg_rows = ((long)A_max + N - 1) / N;
   long exp_rows = avg_rows + avg_rows / 4;
   if (capacity > 0 && capacity < exp_rows) exp_rows = capacity;
   const int wide = (exp_rows > 256 && avg_rows <= 320) ? 1 : 0;
   const int tile_cap = wide ? kWideTile : exp_rows > 128 ? 256 : exp_rows > 64 ? 128 : 64;
   const int stage_bytes = wide ? kABytes + 2 * kSubBytes : kABytes + (tile_cap / 2) * kBK * 2;
-  const int slot_cols = wide ? kWideSub : 256;
-  const int nslots = wide ? 3 : 2;
   int stages = kStageRegion / stage_bytes;
   if (stages > kMaxStages) stages = kMaxStages;
   TcParams p1{offsets, N, d, f, (f + 127) / 128, 1, static_cast<__nv_bfloat16 *>(h), f, nullptr,
-              device_status, raster_group(d), tile_cap, wide, slot_cols, nslots, stages,
-              stage_bytes};
+              device_status, raster_group(d), tile_cap, wide, stages, stage_bytes};
   moe_status_t s = launch_gemm(wg, wu, bx, p1, stream);
   if (s != MOE_OK) return s;
   TcParams p2{offsets, N, f, d, (d + 255) / 256, 0, static_cast<__nv_bfloat16 *>(y_perm), d,
-              row_scale, device_status, raster_group(f), tile_cap, wide, slot_cols, nslots,
-              stages, stage_bytes};
+              row_scale, device_status, raster_group(f), tile_cap, wide, stages, stage_bytes};
   return launch_gemm(wd, wd, bh, p2, stream);
 }
 

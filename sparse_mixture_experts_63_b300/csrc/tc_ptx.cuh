@@ -219,6 +219,13 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
+// Relaxed form: orders nothing but the arrival itself (no wait for this
+// thread's earlier global stores).  For hand-backs of resources whose use
+// has already completed, e.g. tensor memory after tcgen05.wait::ld.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
 // TMA 2-D/3-D load into this CTA's shared memory, completing on an mbarrier
 // that may live in the peer CTA of the pair (cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m,
