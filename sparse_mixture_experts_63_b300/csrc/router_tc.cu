@@ -12,8 +12,9 @@
 // logits and each epilogue thread ranks its own token with a register top-k
 // list.  Ranking: logit descending, equal logits -> lower expert id, NaN lowest.
 //
-// Work split: one 128-token tile per cluster, one group of at most 64 experts
-// per CTA of the cluster (N = 256 -> 4 CTAs, 128 -> 2, <= 64 -> 1).  Each CTA
+// Work split: one 128-token tile per cluster, one group of at most 128 experts
+// per CTA of the cluster (N = 256 -> 2 CTAs, <= 128 -> 1), so T = 8192 tokens
+// and 256 experts run as 128 CTAs, one wave on 148 SMs.  Each CTA
 // ranks its group; the cluster's first CTA merges the groups' candidate lists
 // through distributed shared memory (the comparator is a total order, so the
 // merge gives exactly the global top-k), applies the softmax and writes.
@@ -22,10 +23,10 @@
 // accumulation step in one direction, so a long K (d = 4096..7168) alone
 // would put the gate weights ~2e-5 off.  K is split over kParts partial
 // accumulators (contiguous K ranges), summed in fp32 in a fixed order by the
-// epilogue: 8x fewer steps per accumulator (TMEM: kParts x 64 columns).
+// epilogue: 4x fewer steps per accumulator (TMEM: kParts x 128 columns).
 //
-// CTA = 6 warps: TMA producer, MMA issuer, 4 epilogue warps; 6-stage mbarrier
-// pipeline; every wait bounded (2 s) with a clean drain on timeout.
+// CTA = 6 warps: TMA producer, MMA issuer, 4 epilogue warps; 6-8 stage
+// mbarrier pipeline; every wait bounded (2 s) with a clean drain on timeout.
 #include <cuda.h>
 #include <math.h>
 
@@ -37,23 +38,25 @@ namespace {
 
 constexpr int kBM = 128;                      // tokens per tile
 constexpr int kBK = 64;
-constexpr int kStages = 6;
+constexpr int kMaxStages = 8;
 constexpr int kMaxNE = 256;                   // experts limit
 constexpr int kXBytes = kBM * kBK * 2;        // 16 KB
 constexpr int kWChunk = 64 * kBK * 2;         // 8 KB: 64 experts x 64 k
-constexpr int kStageBytes = kXBytes + kWChunk;      // 24 KB
+constexpr int kStageRegion = 192 * 1024;      // 6 x 32 KB (128 experts) or 8 x 24 KB (<= 64)
 constexpr int kThreads = 192;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kMaxK = 32;
-constexpr int kParts = 8;                     // partial accumulators over K
-constexpr int kGroup = 64;                    // experts per CTA (TMEM: kParts * 64 = 512)
-constexpr int kCandOffset = kStages * kStageBytes;          // candidate lists after the stages
-constexpr int kCandBytes = 2 * kMaxK * kBM * 4;             // values + ids
+constexpr int kParts = 4;                     // partial accumulators over K
+constexpr int kGroup = 128;                   // experts per CTA (TMEM: kParts * 128 = 512)
+constexpr int kCandOffset = kStageRegion;     // candidate lists after the stages
 
 struct RParams {
   int T, d, N, k;
-  int ng;                    // experts per CTA (multiple of 16, <= 64)
+  int ng;                    // experts per CTA (multiple of 16, <= 128)
   int group_ctas;            // CTAs per cluster = ceil(N / ng)
+  int wchunks;               // 64-expert W boxes per stage = ceil(ng / 64)
+  int stages;                // pipeline stages
+  int stage_bytes;           // kXBytes + wchunks * kWChunk
   const float *bias;
   float *logits;             // nullable
   int32_t *topk_idx;
@@ -80,23 +83,30 @@ __device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
 }
 
 // Inserts (v, e) into the sorted list of the best k; a candidate that ranks
-// below all of them moves nothing.
+// below all of them moves nothing.  Branch-free: every slot compares against
+// the candidate at once (the list is sorted, so the slots it beats are a
+// suffix), then each slot of that suffix takes the candidate or its
+// predecessor -- no chain of dependent compare-and-swaps.
 template <int KMAX>
 __device__ __forceinline__ void insert_sorted(float (&bv)[KMAX], int (&bi)[KMAX], int k, float v,
                                               int e) {
-  float cv = v;
-  int ci = e;
+  const float kv = rank_key(v);
+  bool gt[KMAX];
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) {
-    if (j < k && ranks_before(cv, ci, bv[j], bi[j])) {
-      const float tv = bv[j];
-      const int ti = bi[j];
-      bv[j] = cv;
-      bi[j] = ci;
-      cv = tv;
-      ci = ti;
-    }
+    const float kj = rank_key(bv[j]);
+    // same order as ranks_before, written without branches
+    gt[j] = (j < k) & ((kv > kj) | ((kv == kj) & (e < bi[j])));
   }
+#pragma unroll
+  for (int j = KMAX - 1; j > 0; --j) {
+    const float nv = gt[j - 1] ? bv[j - 1] : v;
+    const int ni = gt[j - 1] ? bi[j - 1] : e;
+    bv[j] = gt[j] ? nv : bv[j];
+    bi[j] = gt[j] ? ni : bi[j];
+  }
+  bv[0] = gt[0] ? v : bv[0];
+  bi[0] = gt[0] ? e : bi[0];
 }
 
 template <int KMAX>
@@ -106,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full[kStages], empty[kStages], acc_full, drain;
+  __shared__ uint64_t full[kMaxStages], empty[kMaxStages], acc_full, drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag_s, epi_ok_s;
   volatile int *abort_flag = &abort_flag_s;
@@ -120,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int *cand_i = reinterpret_cast<int *>(smem + kCandOffset + KMAX * kBM * 4);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kMaxStages; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
@@ -164,18 +174,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        unsigned char *st = smem + s * kStageBytes;
-        tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
+        unsigned char *st = smem + s * p.stage_bytes;
+        tc::mbar_arrive_expect_tx(&full[s], (uint32_t)p.stage_bytes);
         tc::tma_load_2d(st, &tmX, &full[s], kb * kBK, tile * kBM, pol_x);
         tc::tma_load_2d(st + kXBytes, &tmW, &full[s], e0, kb * kBK, pol_w);
+        if (p.wchunks > 1)
+          tc::tma_load_2d(st + kXBytes + kWChunk, &tmW, &full[s], e0 + 64, kb * kBK, pol_w);
         ++issued;
-        if (++s == kStages) { s = 0; ph ^= 1; }
+        if (++s == p.stages) { s = 0; ph ^= 1; }
       }
       if (!ok) {
-        const uint32_t first = issued >= kStages ? issued - kStages : 0;
+        const uint32_t ns = (uint32_t)p.stages;
+        const uint32_t first = issued >= ns ? issued - ns : 0;
         for (uint32_t q = first; q < issued; ++q) {
           volatile int dummy = 0;
-          tc::mbar_wait_bounded(&full[q % kStages], (q / kStages) & 1, &dummy, kTimeoutNs / 4);
+          tc::mbar_wait_bounded(&full[q % ns], (q / ns) & 1, &dummy, kTimeoutNs / 4);
         }
       }
     }
@@ -206,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           first = true;
         }
         const uint32_t d_tmem = tmem_base + part * kGroup;
-        const uint64_t off = (uint64_t)((s * kStageBytes) >> 4);
+        const uint64_t off = (uint64_t)((s * p.stage_bytes) >> 4);
         const uint64_t ad = a_desc0 + off, bd = b_desc0 + off;
         // x K-major: +32 B per 16 k (+2); W MN-major: +2048 B per 16 k (+128)
         tc::mma_f16(d_tmem, ad, bd, idesc, first ? 0u : 1u);
@@ -214,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mma_f16(d_tmem, ad + 4, bd + 256, idesc, 1u);
         tc::mma_f16(d_tmem, ad + 6, bd + 384, idesc, 1u);
         tc::mma_commit(&empty[s]);
-        if (++s == kStages) { s = 0; ph ^= 1; }
+        if (++s == p.stages) { s = 0; ph ^= 1; }
       }
       if (ok) tc::mma_commit(&acc_full);
       tc::mma_commit(&drain);
@@ -338,7 +351,7 @@ bool encode2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, 
 template <int KMAX>
 moe_status_t launch_k(const CUtensorMap &tx, const CUtensorMap &tw, const RParams &p, int tiles,
                       cudaStream_t stream) {
-  constexpr int smem = kStages * kStageBytes + kCandBytes + 1024;
+  constexpr int smem = kStageRegion + 2 * KMAX * kBM * 4 + 1024;   // stages + candidate lists
   static bool attr = false;
   if (!attr) {
     MOE_CUDA_TRY(cudaFuncSetAttribute(router_tc_kernel<KMAX>,
@@ -376,7 +389,12 @@ moe_status_t launch_router_tc(const void *x, const void *W_g, const float *bias,
     return MOE_ERR_UNSUPPORTED;
   const int ng = N < kGroup ? ((N + 15) & ~15) : kGroup;
   const int groups = (N + ng - 1) / ng;
-  RParams p{T, d, N, k, ng, groups, bias, logits, topk_idx, topk_w, device_status};
+  const int wchunks = (ng + 63) / 64;
+  const int stage_bytes = kXBytes + wchunks * kWChunk;
+  int stages = kStageRegion / stage_bytes;
+  if (stages > kMaxStages) stages = kMaxStages;
+  RParams p{T, d, N, k, ng, groups, wchunks, stages, stage_bytes, bias, logits, topk_idx,
+            topk_w, device_status};
   const int tiles = (T + kBM - 1) / kBM;
   if (k <= 2) return launch_k<2>(tx, tw, p, tiles, stream);
   if (k <= 8) return launch_k<8>(tx, tw, p, tiles, stream);
