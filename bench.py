@@ -421,7 +421,13 @@ def run_ours(args, ws, rank, local):
                      "per_launch_ms": round(ffn_ms, 4),
                      "algorithmic": (f"{ffn_flop:.4g} FLOP" if unit == "TFLOP/s"
                                      else f"{ffn_bytes:.4g} B"),
-                     "peak_source": f"{pk['source']} (burst)"},
+                     "peak_source": f"{pk['source']} (burst)",
+                     # context only: the same kernel against the measured sustained
+                     # (power-capped) cuBLAS rate; the bench runs back to back for
+                     # seconds, so its clocks sit in that regime
+                     **({"peak_sustained": pk["bf16_tflops_sustained"],
+                         "frac_of_sustained": round(achieved / pk["bf16_tflops_sustained"], 4)}
+                        if unit == "TFLOP/s" else {})},
         "stages_ms": {k_: round(v, 4) for k_, v in stage_ms.items()},
         "routing": {"kept_rows": A, "dropped": int(outs["dropped"].item()),
                     "touched_experts": touched, "max_rows_per_expert": int(kept.max().item()),

@@ -76,9 +76,10 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kMaxExperts = 1024;
 
 // Epilogue staging (per 32-column chunk)
-constexpr int kXPitch = 17;                              // floats per row of a swap buffer
+constexpr int kXPitch = 20;                              // floats per row of a swap buffer
+                                                         // (16-B rows, float4 conflict-free)
 constexpr int kXHalf = 64 * kXPitch;                     // floats per swap buffer
-constexpr int kXBytes = 2 * kXHalf * 4;                  // 8704: gate->up and up->gate
+constexpr int kXBytes = 2 * kXHalf * 4;                  // 10 KB: gate->up and up->gate
 constexpr int kOutHalf = 32 * 128;                       // bf16 per output buffer (8 KB)
 constexpr int kOutBytes = 2 * kOutHalf * 2;              // two output buffers
 
@@ -220,6 +221,89 @@ __device__ __forceinline__ int ring_take(int &pos, int n_mma) {
   const int c0 = pos;
   pos += nch;
   return c0;
+}
+
+// Epilogue of one 32-column chunk of accumulators (r: this thread's TMEM
+// lane, 32 token columns): GEMM1 writes h = SiLU(gate) * up, GEMM2 writes
+// y_perm = row_scale * D, both staged through shared memory into coalesced
+// 16-B row stores.  All 128 epilogue threads call it together.
+__device__ __forceinline__ void epilogue_chunk(const TcParams &p, const TileInfo &ti,
+                                               uint32_t rank, int lane_grp, int lane, int etid,
+                                               float *xbuf, __nv_bfloat16 *obuf, uint32_t &obi,
+                                               int srow0, int srows, int cc,
+                                               const uint32_t (&r)[32]) {
+  const int ncols = min(32, srows - cc * 32);
+  if (p.gemm1) {
+    // Gate lanes (lane_grp 0,1) and up lanes (2,3) of the same hidden unit
+    // hand each other half of the 32 token columns, so all four warps compute
+    // SiLU(gate) * up for 16 columns.
+    const bool gate_side = lane_grp < 2;
+    const int hr = (lane_grp & 1) * 32 + lane;     // hidden unit within the slab
+    float4 *mine = reinterpret_cast<float4 *>(xbuf + (gate_side ? kXHalf : 0) + hr * kXPitch);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int c = 4 * q;
+      mine[q] = gate_side ? make_float4(__uint_as_float(r[16 + c]), __uint_as_float(r[17 + c]),
+                                        __uint_as_float(r[18 + c]), __uint_as_float(r[19 + c]))
+                          : make_float4(__uint_as_float(r[c]), __uint_as_float(r[c + 1]),
+                                        __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]));
+    }
+    tc::named_bar(1, kEpiThreads);
+    const float4 *other4 =
+        reinterpret_cast<const float4 *>(xbuf + (gate_side ? 0 : kXHalf) + hr * kXPitch);
+    __nv_bfloat16 *ob = obuf + (gate_side ? 0 : 16 * 64);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 o4 = other4[q];
+      const float o[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = 4 * q + i;
+        const float g = gate_side ? __uint_as_float(r[c]) : o[i];
+        const float u = gate_side ? o[i] : __uint_as_float(r[16 + c]);
+        const float h = __fdividef(g, 1.f + __expf(-g)) * u;
+        ob[c * 64 + hr] = __float2bfloat16_rn(h);
+      }
+    }
+    tc::named_bar(1, kEpiThreads);
+    // copy out: ncols token rows x 64 hidden units (128 B) each.  The next
+    // chunk writes obuf only after its exchange barrier, which every thread
+    // reaches after finishing this copy.
+    const int m0 = ti.pair * 128 + rank * 64;
+    const int vec_valid = max(0, min(8, (p.M - m0) / 8));
+    for (int q = etid; q < ncols * 8; q += kEpiThreads) {
+      const int c = q / 8, v = q % 8;
+      if (v < vec_valid) {
+        const uint4 val = *reinterpret_cast<const uint4 *>(obuf + c * 64 + v * 8);
+        *reinterpret_cast<uint4 *>(p.out + (size_t)(srow0 + cc * 32 + c) * p.out_ld + m0 +
+                                   v * 8) = val;
+      }
+    }
+  } else {
+    // scale each token column by its gate weight; two output buffers
+    // alternate, so a chunk's writes never meet the previous chunk's copy
+    __nv_bfloat16 *ob = obuf + (obi & 1) * kOutHalf;
+    ++obi;
+    float scl = 1.f;
+    if (p.row_scale && lane < ncols) scl = p.row_scale[srow0 + cc * 32 + lane];
+    const int dr = lane_grp * 32 + lane;             // output column within the slab
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const float sv = __shfl_sync(0xffffffffu, scl, c);
+      ob[c * 128 + dr] = __float2bfloat16_rn(__uint_as_float(r[c]) * sv);
+    }
+    tc::named_bar(1, kEpiThreads);
+    const int m0 = ti.pair * 256 + rank * kBM;
+    const int vec_valid = max(0, min(16, (p.M - m0) / 8));
+    for (int q = etid; q < ncols * 16; q += kEpiThreads) {
+      const int c = q / 16, v = q % 16;
+      if (v < vec_valid) {
+        const uint4 val = *reinterpret_cast<const uint4 *>(ob + c * 128 + v * 8);
+        *reinterpret_cast<uint4 *>(p.out + (size_t)(srow0 + cc * 32 + c) * p.out_ld + m0 +
+                                   v * 8) = val;
+      }
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -458,75 +542,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tc_fence_before();
           if (lane == 0) tc::mbar_arrive_cluster_relaxed(tc::mapa_shared(&col_free[c0 + cc], 0));
         }
-        for (int cc = 0; cc < nchunks; ++cc) {
-          uint32_t r[32];
-          tc::tmem_ld_32x32b_x32(t_base + cc * 32, r);
+        // Chunks are loaded two at a time and handed back to the MMA issuer
+        // before any math, so the next sub-tile can take them early.
+        for (int c2 = 0; c2 < nchunks; c2 += 2) {
+          const bool pair = c2 + 1 < nchunks;
+          uint32_t ra[32], rb[32];
+          tc::tmem_ld_32x32b_x32(t_base + c2 * 32, ra);
+          if (pair) tc::tmem_ld_32x32b_x32(t_base + (c2 + 1) * 32, rb);
           tc::tmem_ld_wait();
-          // the chunk is in registers: hand it back to the MMA issuer (relaxed:
-          // the loads have completed; nothing else needs ordering)
+          // the chunks are in registers: hand them back (relaxed: the loads
+          // have completed; nothing else needs ordering)
           tc::tc_fence_before();
-          if (lane == 0) tc::mbar_arrive_cluster_relaxed(tc::mapa_shared(&col_free[c0 + cc], 0));
-          const int ncols = min(32, srows - cc * 32);
-          if (p.gemm1) {
-            // Gate lanes (lane_grp 0,1) and up lanes (2,3) of the same hidden
-            // unit hand each other half of the 32 token columns, so all four
-            // warps compute SiLU(gate) * up for 16 columns.
-            const bool gate_side = lane_grp < 2;
-            const int hr = (lane_grp & 1) * 32 + lane;     // hidden unit within the slab
-            float *mine = xbuf + (gate_side ? kXHalf : 0) + hr * kXPitch;
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-              mine[c] = gate_side ? __uint_as_float(r[16 + c]) : __uint_as_float(r[c]);
-            tc::named_bar(1, kEpiThreads);
-            const float *other = xbuf + (gate_side ? 0 : kXHalf) + hr * kXPitch;
-            __nv_bfloat16 *ob = obuf + (gate_side ? 0 : 16 * 64);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const float o = other[c];
-              const float g = gate_side ? __uint_as_float(r[c]) : o;
-              const float u = gate_side ? o : __uint_as_float(r[16 + c]);
-              const float h = __fdividef(g, 1.f + __expf(-g)) * u;
-              ob[c * 64 + hr] = __float2bfloat16_rn(h);
-            }
-            tc::named_bar(1, kEpiThreads);
-            // copy out: ncols token rows x 64 hidden units (128 B) each.  The
-            // next chunk writes obuf only after its exchange barrier, which
-            // every thread reaches after finishing this copy.
-            const int m0 = ti.pair * 128 + rank * 64;
-            const int vec_valid = max(0, min(8, (p.M - m0) / 8));
-            for (int q = etid; q < ncols * 8; q += kEpiThreads) {
-              const int c = q / 8, v = q % 8;
-              if (v < vec_valid) {
-                const uint4 val = *reinterpret_cast<const uint4 *>(obuf + c * 64 + v * 8);
-                *reinterpret_cast<uint4 *>(p.out + (size_t)(srow0 + cc * 32 + c) * p.out_ld +
-                                           m0 + v * 8) = val;
-              }
-            }
-          } else {
-            // scale each token column by its gate weight; two output buffers
-            // alternate, so a chunk's writes never meet the previous chunk's copy
-            __nv_bfloat16 *ob = obuf + (obi & 1) * kOutHalf;
-            ++obi;
-            float scl = 1.f;
-            if (p.row_scale && lane < ncols) scl = p.row_scale[srow0 + cc * 32 + lane];
-            const int dr = lane_grp * 32 + lane;             // output column within the slab
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const float sv = __shfl_sync(0xffffffffu, scl, c);
-              ob[c * 128 + dr] = __float2bfloat16_rn(__uint_as_float(r[c]) * sv);
-            }
-            tc::named_bar(1, kEpiThreads);
-            const int m0 = ti.pair * 256 + rank * kBM;
-            const int vec_valid = max(0, min(16, (p.M - m0) / 8));
-            for (int q = etid; q < ncols * 16; q += kEpiThreads) {
-              const int c = q / 16, v = q % 16;
-              if (v < vec_valid) {
-                const uint4 val = *reinterpret_cast<const uint4 *>(ob + c * 128 + v * 8);
-                *reinterpret_cast<uint4 *>(p.out + (size_t)(srow0 + cc * 32 + c) * p.out_ld +
-                                           m0 + v * 8) = val;
-              }
-            }
+          if (lane == 0) {
+            tc::mbar_arrive_cluster_relaxed(tc::mapa_shared(&col_free[c0 + c2], 0));
+            if (pair) tc::mbar_arrive_cluster_relaxed(tc::mapa_shared(&col_free[c0 + c2 + 1], 0));
           }
+          epilogue_chunk(p, ti, rank, lane_grp, lane, etid, xbuf, obuf, obi, srow0, srows, c2, ra);
+          if (pair)
+            epilogue_chunk(p, ti, rank, lane_grp, lane, etid, xbuf, obuf, obi, srow0, srows,
+                           c2 + 1, rb);
         }
       }
     }
