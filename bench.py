@@ -342,6 +342,12 @@ def run_ours(args, ws, rank, local):
                                                           y_perm=y_perm, A_max=A_max), reps),
         "combine": time_stage(lambda: B.moe_combine(y_perm, perm["inv_pos"], y=y), reps),
     }
+    if cfg.fs > 0:
+        sh_off = torch.tensor([0, cfg.T], dtype=torch.int32, device=inp.x.device)
+        ys = torch.empty((cfg.T, cfg.d), dtype=inp.x.dtype, device=inp.x.device)
+        stage_ms["shared_ffn"] = time_stage(
+            lambda: B.moe_expert_ffn(inp.x, sh_off, inp.Ws_gate[None], inp.Ws_up[None],
+                                     inp.Ws_down[None], y_perm=ys), reps)
 
     # end to end through the host-buffer entry point (pinned host x in, y out)
     x_host = inp.x.cpu().pin_memory()

@@ -173,23 +173,28 @@ def test_permute_repeat_bit_identical():
 @pytest.mark.parametrize("name", ["tiny", "mixtral_small", "deepseek_small", "f32_wide",
                                   "many_rows", "odd_dims", "ragged_257", "wide_tiles"])
 def test_expert_ffn_stage(name):
-    """y_perm rows = row_scale * SwiGLU_e(x_perm) against the oracle's expert rows."""
+    """y_perm rows = row_scale * SwiGLU_e(x_perm) against the oracle's expert
+    rows; the stage's inputs (x_perm, offsets, row scales) are built on the
+    CPU from the oracle's routing and grouping of the layer's inputs."""
     cfg = REDUCED[name]
     inp = make_inputs(cfg, device=_cuda())
-    idx, w = B.moe_router_topk(inp.x, inp.W_g, cfg.k, bias=inp.bias)
-    perm = B.moe_permute(idx, cfg.N, x=inp.x, topk_w=w, capacity=0)
-    y_perm = B.moe_expert_ffn(perm["x_perm"], perm["offsets"], inp.W_gate, inp.W_up, inp.W_down,
-                              row_scale=perm["row_scale"])
+    x_c = inp.x.cpu()
+    lo = oracle.router_logits(x_c, inp.W_g.cpu(), None if inp.bias is None else inp.bias.cpu())
+    idx_o, w_o = oracle.topk_softmax(lo, cfg.k)
+    g = oracle.group(idx_o, cfg.N, 0)
+    off = g["offsets"]
+    pt = torch.from_numpy(g["perm_token"].astype(np.int64))
+    xp = x_c[pt].contiguous()
+    rs = torch.from_numpy(w_o[g["perm_token"], g["perm_slot"]]).float()
+    y_perm = B.moe_expert_ffn(xp.cuda(), torch.from_numpy(off).cuda(), inp.W_gate, inp.W_up,
+                              inp.W_down, row_scale=rs.cuda())
     torch.cuda.synchronize()
-    off = perm["offsets"].cpu().numpy()
-    xp = perm["x_perm"].cpu()
-    rs = perm["row_scale"].cpu().double().numpy()
     ref = np.zeros((off[-1], cfg.d))
     for e in range(cfg.N):
         if off[e + 1] > off[e]:
             ref[off[e]:off[e + 1]] = oracle.expert_rows(inp.W_gate[e].cpu(), inp.W_up[e].cpu(),
                                                         inp.W_down[e].cpu(), xp[off[e]:off[e + 1]])
-    ref *= rs[:off[-1], None]
+    ref *= rs.double().numpy()[:, None]
     parity.assert_y_close(y_perm[:off[-1]].float().cpu().numpy(), ref, cfg.dtype)
 
 
@@ -236,6 +241,26 @@ def test_combine_stage():
     o = y_perm.double().cpu().numpy()[np.maximum(invn, 0)]
     ref = oracle.combine_rows(invn, ones, o, shared.double().cpu().numpy())
     np.testing.assert_allclose(y.cpu().double().numpy(), ref, rtol=1e-6, atol=1e-5)
+
+
+@pytest.mark.parametrize("y_dtype", [torch.float32, torch.bfloat16])
+def test_forward_equals_stage_calls(y_dtype):
+    """moe_forward equals, bit for bit, its stage entry points run one after
+    another (router, dispatch, routed FFN, shared-expert FFN, combine)."""
+    cfg = REDUCED["deepseek_small"]
+    inp = make_inputs(cfg, device=_cuda())
+    y_forward, outs = parity.run_forward(inp, y_dtype=y_dtype)
+    A_max = cfg.T * cfg.k
+    idx, w = B.moe_router_topk(inp.x, inp.W_g, cfg.k, bias=inp.bias)
+    perm = B.moe_permute(idx, cfg.N, x=inp.x, topk_w=w, capacity=0, A_max=A_max)
+    y_perm = B.moe_expert_ffn(perm["x_perm"], perm["offsets"], inp.W_gate, inp.W_up, inp.W_down,
+                              row_scale=perm["row_scale"], A_max=A_max)
+    sh_off = torch.tensor([0, cfg.T], dtype=torch.int32, device="cuda")
+    ys = B.moe_expert_ffn(inp.x, sh_off, inp.Ws_gate[None], inp.Ws_up[None], inp.Ws_down[None])
+    y_staged = B.moe_combine(y_perm, perm["inv_pos"], shared_y=ys, y_dtype=y_dtype)
+    torch.cuda.synchronize()
+    assert torch.equal(outs["topk_idx"], idx)
+    assert torch.equal(y_forward, y_staged)
 
 
 def test_forward_repeat_bit_identical():
