@@ -40,12 +40,13 @@ def _load(path=None):
                                      i32p, i32p]
         lib.oracle_expert_rows.argtypes = [ci, ci, ci, vp, vp, vp, ci, vp, ci, f64p, ci]
         lib.oracle_combine_rows.argtypes = [ci, ci, ci, i32p, f64p, f64p, f64p, f64p]
+        lib.oracle_routing_stats.argtypes = [ci, ci, f64p, i32p, f64p, i32p, f64p, f64p]
         lib.oracle_moe_forward.argtypes = (
             [ci] * 6 + [vp, vp, f32p, vp, vp, vp, ci, vp, vp, vp, cd, f64p, f64p,
                         i32p, f64p, i32p, i32p, i32p, i32p, ci])
         for name in ("oracle_router_logits", "oracle_topk_softmax", "oracle_capacity",
                      "oracle_group", "oracle_expert_rows", "oracle_combine_rows",
-                     "oracle_moe_forward"):
+                     "oracle_moe_forward", "oracle_routing_stats"):
             getattr(lib, name).restype = ci
         _lib = lib
     return _lib
@@ -271,6 +272,32 @@ def forward_rows(x_rows, topk_idx_rows, topk_w_rows, inv_pos_rows, fetch_expert,
     if shared is not None:
         sh = expert_rows(shared[0], shared[1], shared[2], x_rows, cores)
     return combine_rows(inv, topk_w_rows, out, sh)
+
+
+def routing_stats(counts, logits=None):
+    """Routing diagnostics from per-expert assignment counts [N] and, when
+    given, the router logits [T,N] (fp64).  Returns a dict: freq [N],
+    prob_mean [N] (None without logits), entropy_bits, entropy_max_bits,
+    top3 (ids), top3_share, max_share, freq_cv, balance (NaN without logits)."""
+    lib = _load()
+    c = _i32(counts)
+    N = c.shape[0]
+    lg = None
+    T = 0
+    if logits is not None:
+        lg = np.ascontiguousarray(logits, dtype=np.float64)
+        T = lg.shape[0]
+        assert lg.shape[1] == N
+    stats = np.empty(6, dtype=np.float64)
+    top3 = np.empty(3, dtype=np.int32)
+    freq = np.empty(N, dtype=np.float64)
+    prob = np.empty(N, dtype=np.float64) if lg is not None else None
+    _check(lib.oracle_routing_stats(T, N, _p(lg), c.ctypes.data, stats.ctypes.data,
+                                    top3.ctypes.data, freq.ctypes.data, _p(prob)),
+           "oracle_routing_stats")
+    return dict(freq=freq, prob_mean=prob, entropy_bits=stats[0], entropy_max_bits=stats[1],
+                top3=top3, top3_share=stats[2], max_share=stats[3], freq_cv=stats[4],
+                balance=stats[5])
 
 
 def near_tie_tokens(logits, k, rel=1e-4):

@@ -403,3 +403,80 @@ done:
   free(o); free(sh);
   return rc;
 }
+
+/*
+ * Routing diagnostics (forward only).
+ *
+ * [MoE-Sparse] 4.2 (路由质量诊断): how often each expert is chosen among the
+ * tokens' top-k, the entropy of that frequency distribution in bits (log2 N
+ * when the load is even), the three most chosen experts and their combined
+ * share, the largest single share, and the calibration term's std/mean of the
+ * frequencies.  [MoE-DSV4] (负载均衡损失): N * sum_i f_i * p_i with f_i the
+ * selection frequency and p_i the mean routing probability of expert i.
+ *
+ * Readings: f_i = counts_i / sum(counts), so the f_i sum to 1; the entropy
+ * takes 0 log 0 = 0 (the page's "+1e-8" inside the logarithm is a numerical
+ * guard); std is the population std over the N experts; p_i is the mean over
+ * tokens of the softmax over all N logits (the router's probabilities before
+ * the top-k); the three most chosen go by frequency, equal frequencies ->
+ * lower expert id, -1 past N.  With no assignments every statistic is 0.
+ *
+ * stats[0] entropy (bits)  [1] log2 N  [2] top-3 share  [3] largest share
+ *      [4] std/mean  [5] balance (NaN when logits is NULL)
+ */
+int oracle_routing_stats(int T, int N, const double *logits, const int32_t *counts,
+                         double *stats, int32_t *top3, double *freq, double *prob) {
+  if (T < 0 || N < 1 || !counts || !stats || !top3 || !freq) return 1;
+  double total = 0.0;
+  for (int e = 0; e < N; ++e) total += counts[e];
+  for (int e = 0; e < N; ++e) freq[e] = total > 0 ? counts[e] / total : 0.0;
+  double h = 0.0;
+  for (int e = 0; e < N; ++e)
+    if (freq[e] > 0) h -= freq[e] * log2(freq[e]);
+  stats[0] = h;
+  stats[1] = log2((double)N);
+  double share = 0.0;
+  for (int r = 0; r < 3; ++r) {
+    int best = -1;
+    for (int e = 0; e < N; ++e) {
+      int taken = 0;
+      for (int q = 0; q < r; ++q) taken |= (top3[q] == e);
+      if (taken) continue;
+      if (best < 0 || freq[e] > freq[best]) best = e;
+    }
+    top3[r] = best;
+    if (best >= 0) share += freq[best];
+  }
+  stats[2] = share;
+  stats[3] = top3[0] >= 0 ? freq[top3[0]] : 0.0;
+  double mean = 0.0, var = 0.0;
+  for (int e = 0; e < N; ++e) mean += freq[e];
+  mean /= N;
+  for (int e = 0; e < N; ++e) var += (freq[e] - mean) * (freq[e] - mean);
+  var /= N;
+  stats[4] = mean > 0 ? sqrt(var) / mean : 0.0;
+  if (!logits) {
+    stats[5] = NAN;
+    return 0;
+  }
+  double *p = prob ? prob : (double *)calloc((size_t)N, sizeof(double));
+  if (!p) return 2;
+  for (int e = 0; e < N; ++e) p[e] = 0.0;
+  for (int t = 0; t < T; ++t) {
+    const double *l = logits + (size_t)t * N;
+    double m = l[0];
+    for (int e = 1; e < N; ++e)
+      if (l[e] > m) m = l[e];
+    double s = 0.0;
+    for (int e = 0; e < N; ++e) s += exp(l[e] - m);
+    for (int e = 0; e < N; ++e) p[e] += exp(l[e] - m) / s;
+  }
+  double bal = 0.0;
+  for (int e = 0; e < N; ++e) {
+    p[e] = T > 0 ? p[e] / T : 0.0;
+    bal += freq[e] * p[e];
+  }
+  stats[5] = N * bal;
+  if (!prob) free(p);
+  return 0;
+}

@@ -393,3 +393,88 @@ def test_tiny_config_end_to_end_invariants():
     assert r["counts"].sum() == TINY.T * TINY.k
     np.testing.assert_allclose(r["topk_w"].sum(1), 1.0, atol=1e-14)
     assert np.all(np.isfinite(r["y"]))
+
+
+# ---------------------------------------------------------------- routing diagnostics
+
+def test_routing_entropy_uniform_128_experts_is_7_bits():
+    """[Sparse] 4.2: an even load over 128 experts has entropy log2(128) = 7 bits."""
+    g = json.load(open(os.path.join(GOLDEN, "router_entropy.json")))
+    r = oracle.routing_stats(np.full(g["N"], 11))
+    assert r["entropy_bits"] == pytest.approx(g["uniform_entropy_bits"], abs=1e-12)
+    assert r["entropy_max_bits"] == pytest.approx(g["uniform_entropy_bits"], abs=1e-12)
+    assert r["freq_cv"] == pytest.approx(0.0, abs=1e-12)
+    assert r["top3_share"] == pytest.approx(3 / 128, abs=1e-12)
+
+
+def test_routing_stats_closed_forms():
+    # every assignment to one expert: zero entropy, full share, std/mean = sqrt(N-1)
+    r = oracle.routing_stats(np.array([0, 0, 0, 9, 0, 0, 0, 0]))
+    assert r["entropy_bits"] == 0.0
+    assert r["max_share"] == 1.0 and r["top3_share"] == 1.0
+    assert r["top3"].tolist() == [3, 0, 1]          # then equal (zero) shares by lower id
+    assert r["freq_cv"] == pytest.approx(np.sqrt(7.0), rel=1e-12)
+    # two experts with the same load: one bit
+    r = oracle.routing_stats(np.array([0, 5, 0, 5]))
+    assert r["entropy_bits"] == pytest.approx(1.0, abs=1e-12)
+    assert r["top3"].tolist() == [1, 3, 0]
+    # shares 1/2, 1/4, 1/8, 1/8: 1.75 bits
+    r = oracle.routing_stats(np.array([8, 4, 2, 2]))
+    assert r["entropy_bits"] == pytest.approx(1.75, abs=1e-12)
+    assert r["top3_share"] == pytest.approx(0.875, abs=1e-12)
+    assert r["top3"].tolist() == [0, 1, 2]
+    # fewer than three experts: the missing ids are -1
+    r = oracle.routing_stats(np.array([3, 1]))
+    assert r["top3"].tolist() == [0, 1, -1]
+    # no assignments at all
+    r = oracle.routing_stats(np.zeros(4, dtype=np.int32))
+    assert r["entropy_bits"] == 0 and r["max_share"] == 0 and r["freq_cv"] == 0
+
+
+def test_routing_balance_closed_forms():
+    """[DSV4] balance statistic N * sum f_i p_i: 1 for an even load and even
+    probabilities, N when load and probability sit on one expert."""
+    N, T = 16, 32
+    r = oracle.routing_stats(np.full(N, 4), np.zeros((T, N)))
+    assert r["balance"] == pytest.approx(1.0, rel=1e-12)
+    assert np.allclose(r["prob_mean"], 1.0 / N, rtol=0, atol=1e-15)
+    lg = np.full((T, N), -1e4)
+    lg[:, 5] = 0.0
+    cnt = np.zeros(N, dtype=np.int32)
+    cnt[5] = T
+    r = oracle.routing_stats(cnt, lg)
+    assert r["balance"] == pytest.approx(N, rel=1e-12)
+    # half the load and half the probability on each of two experts: N/2
+    lg = np.full((T, N), -1e4)
+    lg[:, 2] = lg[:, 9] = 0.0
+    cnt = np.zeros(N, dtype=np.int32)
+    cnt[2] = cnt[9] = 7
+    r = oracle.routing_stats(cnt, lg)
+    assert r["balance"] == pytest.approx(N / 2, rel=1e-12)
+    assert r["prob_mean"][2] == pytest.approx(0.5, rel=1e-12)
+    # softmax probabilities: exp(ln 3) against 1 gives 3/4 and 1/4
+    lg = np.full((1, 2), 0.0)
+    lg[0, 0] = np.log(3.0)
+    r = oracle.routing_stats(np.array([1, 0]), lg)
+    assert r["prob_mean"].tolist() == pytest.approx([0.75, 0.25], rel=1e-12)
+    assert r["balance"] == pytest.approx(2 * 0.75, rel=1e-12)
+    assert np.isnan(oracle.routing_stats(np.array([1, 2]))["balance"])
+
+
+def test_routing_stats_invariances():
+    rng = np.random.default_rng(3)
+    N, T = 12, 40
+    lg = rng.normal(size=(T, N))
+    cnt = rng.integers(0, 50, size=N).astype(np.int32)
+    a = oracle.routing_stats(cnt, lg)
+    # a per-token shift of the logits leaves the probabilities unchanged
+    b = oracle.routing_stats(cnt, lg + rng.normal(size=(T, 1)) * 10)
+    assert np.allclose(a["prob_mean"], b["prob_mean"], rtol=1e-12, atol=0)
+    # relabelling the experts permutes the per-expert values, not the scalars
+    perm = rng.permutation(N)
+    c = oracle.routing_stats(cnt[perm], lg[:, perm])
+    assert np.allclose(c["freq"], a["freq"][perm]) and np.allclose(c["prob_mean"], a["prob_mean"][perm])
+    for key in ("entropy_bits", "top3_share", "max_share", "freq_cv", "balance"):
+        assert c[key] == pytest.approx(a[key], rel=1e-12)
+    assert a["prob_mean"].sum() == pytest.approx(1.0, rel=1e-12)
+    assert a["freq"].sum() == pytest.approx(1.0, rel=1e-12)

@@ -34,6 +34,12 @@ MUTANTS = [
     ("combine_keeps_dropped", "if (inv_pos_rows[(size_t)r * k + j] < 0) continue; /* dropped slot */", ""),
     ("combine_no_shared", "yr[q] += shared[(size_t)r * d + q];", ";"),
     ("combine_unweighted", "yr[q] += w * o[q];", "yr[q] += o[q];"),
+    ("entropy_natural_log", "h -= freq[e] * log2(freq[e]);", "h -= freq[e] * log(freq[e]);"),
+    ("cv_sample_std", "var /= N;", "var /= (N - 1);"),
+    ("top3_tie_higher_id", "if (best < 0 || freq[e] > freq[best]) best = e;",
+     "if (best < 0 || freq[e] >= freq[best]) best = e;"),
+    ("balance_without_N", "stats[5] = N * bal;", "stats[5] = bal;"),
+    ("prob_not_normalised", "p[e] += exp(l[e] - m) / s;", "p[e] += exp(l[e] - m);"),
 ]
 
 
