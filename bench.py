@@ -342,6 +342,11 @@ def run_ours(args, ws, rank, local):
                                                           y_perm=y_perm, A_max=A_max), reps),
         "combine": time_stage(lambda: B.moe_combine(y_perm, perm["inv_pos"], y=y), reps),
     }
+    # routing diagnostics from the router's logits and the pre-capacity counts
+    lg_buf = torch.empty((cfg.T, N), dtype=torch.float32, device=inp.x.device)
+    B.moe_router_topk(inp.x, inp.W_g, k, bias=inp.bias, logits=lg_buf)
+    stage_ms["routing_stats"] = time_stage(lambda: B.moe_routing_stats(perm["counts"], lg_buf),
+                                           reps)
     if cfg.fs > 0:
         sh_off = torch.tensor([0, cfg.T], dtype=torch.int32, device=inp.x.device)
         ys = torch.empty((cfg.T, cfg.d), dtype=inp.x.dtype, device=inp.x.device)

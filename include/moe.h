@@ -222,6 +222,44 @@ moe_status_t moe_forward_host_io(const moe_forward_args *args,
                                  void *workspace, size_t workspace_bytes,
                                  void *stream);
 
+/* ---------------------------------------------------------------------------
+ * Routing diagnostics (forward only): how evenly the router spreads the load.
+ * Source: "MoE稀疏激活原理与工程实践", 4.2 路由质量诊断 (selection frequency of
+ * each expert, entropy of that distribution in bits against log2 N, the three
+ * most chosen experts and their share, the largest single share, std/mean of
+ * the frequencies); "大模型MoE混合专家架构原理与DeepSeek-V4工程实践解析"
+ * (balance statistic N * sum_i f_i * p_i, p_i the mean routing probability).
+ *   counts [N] device int32: assignments per expert before any capacity
+ *     (moe_permute's or moe_forward's `counts`); f_i = counts_i / sum(counts).
+ *   logits [T,N] device fp32 or NULL (moe_router_topk's `logits`): p_i is the
+ *     mean over the T tokens of the softmax over all N logits.  NULL: no p_i,
+ *     balance = NaN.
+ *   stats: device pointer to one moe_routing_stats_t (output).
+ *   freq [N], prob_mean [N]: device fp32 outputs, each may be NULL
+ *     (prob_mean is not written when logits is NULL).
+ * Conventions: entropy takes 0 log 0 = 0; std is the population std; the
+ * three most chosen go by count, equal counts -> lower id, -1 past N; with no
+ * assignments every statistic is 0.  Deterministic (fixed reduction order),
+ * fp32.  Workspace: moe_routing_stats_workspace_size(T, N) bytes (0 when
+ * logits is NULL).  Argument errors return synchronously; N <= 1024.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  float entropy_bits;         /* -sum f_i log2 f_i                           */
+  float entropy_max_bits;     /* log2 N (an even load)                       */
+  float top3_share;           /* f of the three most chosen experts          */
+  float max_share;            /* largest f_i                                 */
+  float freq_cv;              /* std(f) / mean(f)                            */
+  float balance;              /* N * sum f_i p_i; NaN without logits         */
+  int32_t top3[3];            /* ids of the three most chosen (-1 past N)    */
+  int32_t assignments;        /* sum of counts                               */
+} moe_routing_stats_t;
+
+size_t moe_routing_stats_workspace_size(int T, int N);
+moe_status_t moe_routing_stats(const float *logits, const int32_t *counts, int T,
+                               int N, moe_routing_stats_t *stats, float *freq,
+                               float *prob_mean, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

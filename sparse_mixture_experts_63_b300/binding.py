@@ -25,7 +25,8 @@ EXPORTS = ("moe_status_string", "moe_last_error", "moe_version", "moe_launch_cou
            "moe_router_topk", "moe_permute_workspace_size", "moe_permute",
            "moe_permute_noalloc",
            "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
-           "moe_forward_workspace_size", "moe_forward", "moe_forward_host_io")
+           "moe_forward_workspace_size", "moe_forward", "moe_forward_host_io",
+           "moe_routing_stats_workspace_size", "moe_routing_stats")
 
 
 class MoEError(RuntimeError):
@@ -85,8 +86,11 @@ def lib():
         L.moe_forward_workspace_size.restype = sz
         L.moe_forward.argtypes = [ctypes.POINTER(moe_forward_args), vp, sz, vp]
         L.moe_forward_host_io.argtypes = [ctypes.POINTER(moe_forward_args), vp, vp, vp, sz, vp]
+        L.moe_routing_stats_workspace_size.argtypes = [ci, ci]
+        L.moe_routing_stats_workspace_size.restype = sz
+        L.moe_routing_stats.argtypes = [vp, vp, ci, ci, vp, vp, vp, vp, sz, vp]
         for n in ("moe_router_topk", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn",
-                  "moe_combine",
+                  "moe_combine", "moe_routing_stats",
                   "moe_forward", "moe_forward_host_io"):
             getattr(L, n).restype = ci
         _lib = L
@@ -219,6 +223,43 @@ def moe_expert_ffn(x_perm, offsets, W_gate, W_up, W_down, row_scale=None, y_perm
         _p(W_up), _p(W_down), _p(y_perm), _p(device_status), _p(ws), ws_bytes,
         _stream(stream)))
     return y_perm
+
+
+class moe_routing_stats_t(ctypes.Structure):
+    _fields_ = [("entropy_bits", ctypes.c_float), ("entropy_max_bits", ctypes.c_float),
+                ("top3_share", ctypes.c_float), ("max_share", ctypes.c_float),
+                ("freq_cv", ctypes.c_float), ("balance", ctypes.c_float),
+                ("top3", ctypes.c_int32 * 3), ("assignments", ctypes.c_int32)]
+
+
+def moe_routing_stats(counts, logits=None, stream=None):
+    """Routing diagnostics on the device.  counts [N] int32 (before capacity),
+    logits [T,N] fp32 or None.  Returns (stats, freq, prob_mean): stats a uint8
+    device tensor holding one moe_routing_stats_t (read it with
+    routing_stats_dict after a sync), freq [N] and prob_mean [N] (None without
+    logits) fp32 device tensors."""
+    _cuda(counts, logits)
+    N = counts.shape[0]
+    T = logits.shape[0] if logits is not None else 0
+    dev = counts.device
+    stats = torch.empty(ctypes.sizeof(moe_routing_stats_t), dtype=torch.uint8, device=dev)
+    freq = torch.empty(N, dtype=torch.float32, device=dev)
+    prob = torch.empty(N, dtype=torch.float32, device=dev) if logits is not None else None
+    ws_bytes = lib().moe_routing_stats_workspace_size(T, N) if logits is not None else 0
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    _check("moe_routing_stats", lib().moe_routing_stats(
+        _p(logits), _p(counts), T, N, _p(stats), _p(freq), _p(prob), _p(ws), ws_bytes,
+        _stream(stream)))
+    return stats, freq, prob
+
+
+def routing_stats_dict(stats):
+    """moe_routing_stats_t from the device buffer returned by moe_routing_stats."""
+    raw = bytes(stats.cpu().numpy().tobytes())
+    st = moe_routing_stats_t.from_buffer_copy(raw)
+    return dict(entropy_bits=st.entropy_bits, entropy_max_bits=st.entropy_max_bits,
+                top3_share=st.top3_share, max_share=st.max_share, freq_cv=st.freq_cv,
+                balance=st.balance, top3=list(st.top3), assignments=st.assignments)
 
 
 def moe_combine(y_perm, inv_pos, shared_y=None, y=None, y_dtype=torch.float32, stream=None):

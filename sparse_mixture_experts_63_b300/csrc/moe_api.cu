@@ -274,6 +274,29 @@ moe_status_t moe_expert_ffn(const void *x_perm, const int32_t *offsets, const fl
                            static_cast<cudaStream_t>(stream));
 }
 
+size_t moe_routing_stats_workspace_size(int T, int N) {
+  if (T < 0 || N < 1) return 0;
+  return routing_stats_workspace_bytes(T, N);
+}
+
+moe_status_t moe_routing_stats(const float *logits, const int32_t *counts, int T, int N,
+                               moe_routing_stats_t *stats, float *freq, float *prob_mean,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+  CHECK_ARG(T >= 0 && N >= 1 && N <= 1024, "bad sizes T=%d N=%d (N <= 1024)", T, N);
+  CHECK_ARG(counts && stats, "counts and stats are required");
+  if (logits && T > 0) {
+    const size_t need = routing_stats_workspace_bytes(T, N);
+    if (!workspace || workspace_bytes < need) {
+      set_error("moe_routing_stats: workspace %zu bytes, needs %zu", workspace_bytes, need);
+      return MOE_ERR_WORKSPACE;
+    }
+  }
+  moe_status_t s = check_device();
+  if (s != MOE_OK) return s;
+  return launch_routing_stats(logits, counts, T, N, stats, freq, prob_mean, workspace,
+                              static_cast<cudaStream_t>(stream));
+}
+
 moe_status_t moe_combine(const void *y_perm, moe_dtype_t y_perm_dtype, const int32_t *inv_pos,
                          int T, int k, int d, const void *shared_y, void *y, moe_dtype_t y_dtype,
                          void *stream) {

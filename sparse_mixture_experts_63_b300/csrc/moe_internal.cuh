@@ -89,6 +89,10 @@ moe_status_t launch_expert_ffn(const void *x_perm, const int32_t *offsets,
                                const void *W_up, const void *W_down, void *y_perm,
                                int32_t *device_status, void *workspace, cudaStream_t stream);
 
+size_t routing_stats_workspace_bytes(int T, int N);
+moe_status_t launch_routing_stats(const float *logits, const int32_t *counts, int T, int N,
+                                  moe_routing_stats_t *stats, float *freq, float *prob_mean,
+                                  void *workspace, cudaStream_t stream);
 moe_status_t launch_combine(const void *y_perm, moe_dtype_t y_perm_dtype,
                             const int32_t *inv_pos, int T, int k, int d,
                             const void *shared_y, void *y, moe_dtype_t y_dtype,

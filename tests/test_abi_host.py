@@ -105,3 +105,14 @@ def test_stage_entry_points_reject_bad_arguments(lib):
     # combine: d not a multiple of 8
     assert lib.moe_combine(4096, 1, 4096, 4, 2, 60, None, 4096, 0, None) == 1
     assert "d=60" in B.lib().moe_last_error().decode()
+
+
+def test_routing_stats_rejects_bad_arguments(lib):
+    # N above 1024, missing counts or stats, workspace too small for the logits pass
+    assert lib.moe_routing_stats(None, 4096, 16, 2048, 4096, None, None, None, 0, None) == 1
+    assert lib.moe_routing_stats(None, None, 16, 8, 4096, None, None, None, 0, None) == 1
+    assert lib.moe_routing_stats(None, 4096, 16, 8, None, None, None, None, 0, None) == 1
+    need = lib.moe_routing_stats_workspace_size(1000, 64)
+    assert need >= 4 * 64 * 4            # ceil(1000 / 256) chunks x 64 experts, fp32
+    assert lib.moe_routing_stats(4096, 4096, 1000, 64, 4096, None, None, None, need - 1,
+                                 None) == 3

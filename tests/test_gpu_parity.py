@@ -287,3 +287,70 @@ def test_host_io_variant_matches_device_call():
     B.moe_forward_host_io(a, x_host, y_host, layer.workspace(a, inp.x.device))
     torch.cuda.synchronize()
     assert torch.equal(y_host, y_dev.cpu())
+
+
+def _stats_close(got, ref, rel=2e-5):
+    for key in ("entropy_bits", "entropy_max_bits", "top3_share", "max_share", "freq_cv"):
+        assert got[key] == pytest.approx(ref[key], rel=rel, abs=1e-6), key
+    if np.isnan(ref["balance"]):
+        assert np.isnan(got["balance"])
+    else:
+        assert got["balance"] == pytest.approx(ref["balance"], rel=rel), "balance"
+    assert got["top3"] == ref["top3"].tolist()
+
+
+@pytest.mark.parametrize("T,N,skew,with_logits", [
+    (1000, 8, 1.0, True), (8192, 256, 0.5, True), (4096, 128, 3.0, True), (513, 1024, 1.0, True),
+    (300, 2, 0.0, True), (1, 1, 0.0, True), (0, 16, 0.0, False), (2049, 64, 2.0, False)])
+def test_routing_stats_stage(T, N, skew, with_logits):
+    """Synthetic counts and logits (test inputs) on both sides; counts with ties."""
+    rng = np.random.default_rng(T + N)
+    p = np.exp(skew * rng.normal(size=N))
+    counts = rng.multinomial(2 * max(T, 1), p / p.sum()).astype(np.int32)
+    half = N // 2
+    counts[half:2 * half] = counts[:half]            # equal counts: the tie rule decides
+    logits = (rng.normal(size=(T, N)) * 2).astype(np.float32) if with_logits else None
+    st, freq, prob = B.moe_routing_stats(torch.from_numpy(counts).cuda(),
+                                         None if logits is None else torch.from_numpy(logits).cuda())
+    torch.cuda.synchronize()
+    got = B.routing_stats_dict(st)
+    ref = oracle.routing_stats(counts, None if logits is None else logits.astype(np.float64))
+    _stats_close(got, ref)
+    assert got["assignments"] == int(counts.sum())
+    np.testing.assert_allclose(freq.cpu().numpy(), ref["freq"], rtol=1e-6, atol=0)
+    if with_logits:
+        np.testing.assert_allclose(prob.cpu().numpy(), ref["prob_mean"], rtol=2e-5, atol=1e-9)
+
+
+def test_routing_stats_no_assignments_and_one_expert():
+    z = torch.zeros(8, dtype=torch.int32, device="cuda")
+    st, _, _ = B.moe_routing_stats(z)
+    got = B.routing_stats_dict(st)
+    assert got["entropy_bits"] == 0 and got["max_share"] == 0 and got["freq_cv"] == 0
+    assert got["top3"] == [0, 1, 2]
+    one = torch.tensor([0, 0, 0, 9, 0, 0, 0, 0], dtype=torch.int32, device="cuda")
+    got = B.routing_stats_dict(B.moe_routing_stats(one)[0])
+    assert got["entropy_bits"] == 0 and got["max_share"] == 1 and got["top3"] == [3, 0, 1]
+    assert got["freq_cv"] == pytest.approx(np.sqrt(7.0), rel=1e-6)
+
+
+@pytest.mark.parametrize("name", ["mixtral_small", "deepseek_small", "capacity_small"])
+def test_routing_stats_on_a_layer(name):
+    """Router logits and pre-capacity counts from the library, against the
+    oracle's statistics of the oracle's own routing of the same inputs."""
+    cfg = REDUCED[name]
+    inp = make_inputs(cfg, device=_cuda())
+    logits = torch.empty((cfg.T, cfg.N), dtype=torch.float32, device="cuda")
+    idx, w = B.moe_router_topk(inp.x, inp.W_g, cfg.k, bias=inp.bias, logits=logits)
+    C = oracle.capacity(cfg.cf, cfg.T, cfg.k, cfg.N)
+    perm = B.moe_permute(idx, cfg.N, capacity=C)
+    st, _, prob = B.moe_routing_stats(perm["counts"], logits)
+    torch.cuda.synchronize()
+    got = B.routing_stats_dict(st)
+    lo = oracle.router_logits(inp.x.cpu(), inp.W_g.cpu(), None if inp.bias is None else inp.bias.cpu())
+    idx_o, _ = oracle.topk_softmax(lo, cfg.k)
+    g = oracle.group(idx_o, cfg.N, C)
+    np.testing.assert_array_equal(perm["counts"].cpu().numpy(), g["counts"])
+    ref = oracle.routing_stats(g["counts"], lo)
+    _stats_close(got, ref, rel=1e-4)
+    np.testing.assert_allclose(prob.cpu().numpy(), ref["prob_mean"], rtol=1e-4, atol=1e-8)
