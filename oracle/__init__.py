@@ -41,12 +41,13 @@ def _load(path=None):
         lib.oracle_expert_rows.argtypes = [ci, ci, ci, vp, vp, vp, ci, vp, ci, f64p, ci]
         lib.oracle_combine_rows.argtypes = [ci, ci, ci, i32p, f64p, f64p, f64p, f64p]
         lib.oracle_routing_stats.argtypes = [ci, ci, f64p, i32p, f64p, i32p, f64p, f64p]
+        lib.oracle_reroute.argtypes = [ci, ci, ci, ci, ci, i32p, f64p, i32p, i32p, i32p, f64p]
         lib.oracle_moe_forward.argtypes = (
             [ci] * 6 + [vp, vp, f32p, vp, vp, vp, ci, vp, vp, vp, cd, f64p, f64p,
                         i32p, f64p, i32p, i32p, i32p, i32p, ci])
         for name in ("oracle_router_logits", "oracle_topk_softmax", "oracle_capacity",
                      "oracle_group", "oracle_expert_rows", "oracle_combine_rows",
-                     "oracle_moe_forward", "oracle_routing_stats"):
+                     "oracle_moe_forward", "oracle_routing_stats", "oracle_reroute"):
             getattr(lib, name).restype = ci
         _lib = lib
     return _lib
@@ -298,6 +299,30 @@ def routing_stats(counts, logits=None):
     return dict(freq=freq, prob_mean=prob, entropy_bits=stats[0], entropy_max_bits=stats[1],
                 top3=top3, top3_share=stats[2], max_share=stats[3], freq_cv=stats[4],
                 balance=stats[5])
+
+
+def reroute(cand, k, R, N, capacity_rows, logits=None):
+    """Capacity overflow re-routed to the next-best expert (see moe_oracle.c,
+    oracle_reroute).  cand [T, k+R] the tokens' experts by rank; logits [T,N]
+    (fp64) for the final gate weights.  Returns dict final_cand [T,k]
+    (candidate index per slot), placed [T,k] bool, final_idx [T,k] (the slot's
+    expert; -1 when dropped), rerouted, final_w [T,k] (None without logits)."""
+    lib = _load()
+    c = _i32(cand)
+    T = c.shape[0]
+    assert c.shape[1] == k + R
+    lg = None if logits is None else np.ascontiguousarray(logits, dtype=np.float64)
+    fc = np.empty((T, k), dtype=np.int32)
+    pl = np.empty((T, k), dtype=np.int32)
+    rr = np.zeros(1, dtype=np.int32)
+    fw = np.empty((T, k), dtype=np.float64) if lg is not None else None
+    _check(lib.oracle_reroute(T, N, k, R, int(capacity_rows), c.ctypes.data, _p(lg),
+                              fc.ctypes.data, pl.ctypes.data, rr.ctypes.data, _p(fw)),
+           "oracle_reroute")
+    fi = np.take_along_axis(c, fc.astype(np.int64), 1)
+    fi[pl == 0] = -1
+    return dict(final_cand=fc, placed=pl.astype(bool), final_idx=fi, rerouted=int(rr[0]),
+                final_w=fw)
 
 
 def near_tie_tokens(logits, k, rel=1e-4):

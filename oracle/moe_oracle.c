@@ -480,3 +480,94 @@ int oracle_routing_stats(int T, int N, const double *logits, const int32_t *coun
   if (!prob) free(p);
   return 0;
 }
+
+/*
+ * Capacity overflow re-routed to the next-best expert.
+ *
+ * [MoE-Sparse] 2.2 (专家容量的硬约束): once an expert's queue holds its
+ * capacity, a token that selects it is re-routed to its next-best expert.
+ * Readings: the first pass is the capacity rule above (rank by token index
+ * < C); then, in each of R rounds, every slot still without an expert
+ * proposes its token's next-ranked expert not yet tried by the token (ranks
+ * k, k+1, ... of the token's candidates, consumed in slot order whether the
+ * proposal is granted or not), and each expert grants its remaining room to
+ * that round's proposals in (token, slot) order.  A slot still unplaced after
+ * R rounds is dropped.  A slot keeps the candidate it was finally granted
+ * (or, if dropped, its first choice).
+ *
+ * Gate weights (reading): the softmax over the logits of the token's k final
+ * experts -- the same rule as without re-routing, applied to the final
+ * selection; a dropped slot keeps its first choice's logit in the denominator
+ * and contributes nothing to the output (weights are not renormalised).
+ *
+ * cand [T][k+R]: each token's experts by rank (distinct); logits [T][N] or
+ * NULL.  Outputs: final_cand [T][k] candidate index of each slot's expert,
+ * placed [T][k], *rerouted = slots placed in rounds >= 1, final_w [T][k]
+ * (written when logits is given).
+ */
+int oracle_reroute(int T, int N, int k, int R, int capacity, const int32_t *cand,
+                   const double *logits, int32_t *final_cand, int32_t *placed,
+                   int32_t *rerouted, double *final_w) {
+  if (T < 0 || N < 1 || k < 1 || R < 0 || capacity < 1) return 1;
+  const int kr = k + R;
+  int32_t *used = (int32_t *)calloc((size_t)N, sizeof(int32_t));
+  int32_t *ptr = (int32_t *)malloc(sizeof(int32_t) * ((size_t)T + 1));
+  int32_t *prop = (int32_t *)malloc(sizeof(int32_t) * ((size_t)T * k + 1));
+  if (!used || !ptr || !prop) { free(used); free(ptr); free(prop); return 2; }
+  *rerouted = 0;
+  /* first pass: the token's own top-k, by token index */
+  for (int t = 0; t < T; ++t) {
+    ptr[t] = k;
+    for (int j = 0; j < k; ++j) {
+      const int e = cand[(size_t)t * kr + j];
+      final_cand[(size_t)t * k + j] = j;
+      placed[(size_t)t * k + j] = 0;
+      if (e >= 0 && e < N && used[e] < capacity) {
+        used[e]++;
+        placed[(size_t)t * k + j] = 1;
+      }
+    }
+  }
+  for (int r = 1; r <= R; ++r) {
+    /* proposals: each unplaced slot takes its token's next untried candidate */
+    for (int t = 0; t < T; ++t)
+      for (int j = 0; j < k; ++j) {
+        size_t a = (size_t)t * k + j;
+        prop[a] = -1;
+        if (!placed[a] && ptr[t] < kr) prop[a] = ptr[t]++;
+      }
+    /* grants: remaining room, in (token, slot) order */
+    for (int t = 0; t < T; ++t)
+      for (int j = 0; j < k; ++j) {
+        size_t a = (size_t)t * k + j;
+        if (prop[a] < 0) continue;
+        const int e = cand[(size_t)t * kr + prop[a]];
+        if (e >= 0 && e < N && used[e] < capacity) {
+          used[e]++;
+          placed[a] = 1;
+          final_cand[a] = prop[a];
+          (*rerouted)++;
+        }
+      }
+  }
+  if (logits && final_w) {
+    for (int t = 0; t < T; ++t) {
+      double lmax = -INFINITY, denom = 0.0;
+      for (int j = 0; j < k; ++j) {
+        const int e = cand[(size_t)t * kr + final_cand[(size_t)t * k + j]];
+        const double l = logits[(size_t)t * N + e];
+        if (l > lmax) lmax = l;
+      }
+      for (int j = 0; j < k; ++j) {
+        const int e = cand[(size_t)t * kr + final_cand[(size_t)t * k + j]];
+        denom += exp(logits[(size_t)t * N + e] - lmax);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int e = cand[(size_t)t * kr + final_cand[(size_t)t * k + j]];
+        final_w[(size_t)t * k + j] = exp(logits[(size_t)t * N + e] - lmax) / denom;
+      }
+    }
+  }
+  free(used); free(ptr); free(prop);
+  return 0;
+}

@@ -478,3 +478,68 @@ def test_routing_stats_invariances():
         assert c[key] == pytest.approx(a[key], rel=1e-12)
     assert a["prob_mean"].sum() == pytest.approx(1.0, rel=1e-12)
     assert a["freq"].sum() == pytest.approx(1.0, rel=1e-12)
+
+
+# ---------------------------------------------------------------- overflow re-routing
+
+def test_reroute_hand_examples():
+    """[Sparse] 2.2: a token whose expert is full goes to its next-best expert."""
+    cand = np.array([[0, 1]] * 4 + [[0, 2]] * 2, dtype=np.int32)
+    r = oracle.reroute(cand, 1, 1, 3, 2)
+    assert r["final_idx"].ravel().tolist() == [0, 0, 1, 1, 2, 2]
+    assert r["rerouted"] == 4
+    # capacity 1: token 1 takes expert 1, tokens 2 and 3 find it full, token 4 takes 2
+    r = oracle.reroute(cand, 1, 1, 3, 1)
+    assert r["final_idx"].ravel().tolist() == [0, 1, -1, -1, 2, -1]
+    assert r["rerouted"] == 2
+    # two rounds: the second untried candidate is used once the first was full
+    cand = np.array([[0, 1, 2]] * 3, dtype=np.int32)
+    r = oracle.reroute(cand, 1, 2, 3, 1)
+    assert r["final_idx"].ravel().tolist() == [0, 1, 2]
+    # a token's two overflowing slots propose different candidates
+    cand = np.array([[0, 1, 2, 3], [0, 1, 2, 3]], dtype=np.int32)
+    r = oracle.reroute(cand, 2, 2, 4, 1)
+    assert r["final_idx"].tolist() == [[0, 1], [2, 3]]
+
+
+def test_reroute_gate_weights_closed_form():
+    """Weights are the softmax over the final experts' logits: with logits
+    2, ln 3, 0 and expert 0 full, slot 0 moves to expert 2 -> 1/4 and 3/4."""
+    lg = np.array([[2.0, np.log(3.0), 0.0], [2.0, np.log(3.0), 0.0]])
+    cand = np.array([[0, 1, 2], [0, 1, 2]], dtype=np.int32)
+    r = oracle.reroute(cand, 2, 1, 3, 1, logits=lg)
+    assert r["final_idx"].tolist() == [[0, 1], [2, -1]]
+    assert r["final_w"][1].tolist() == pytest.approx([0.25, 0.75], rel=1e-12)
+    # token 0 kept its top-2: the plain softmax over the two
+    _, w = oracle.topk_softmax(lg[:1], 2)
+    assert r["final_w"][0].tolist() == pytest.approx(w[0].tolist(), rel=1e-12)
+
+
+@pytest.mark.parametrize("T,N,k,R,cap,seed", [(300, 8, 2, 2, 40, 1), (500, 16, 3, 3, 60, 2),
+                                              (64, 4, 1, 3, 5, 3), (200, 32, 2, 0, 9, 4)])
+def test_reroute_invariants(T, N, k, R, cap, seed):
+    rng = np.random.default_rng(seed)
+    lg = rng.normal(size=(T, N)) + np.linspace(2, -2, N)      # skewed towards low ids
+    cand, _ = oracle.topk_softmax(lg, k + R)
+    r = oracle.reroute(cand, k, R, N, cap, logits=lg)
+    fi, pl = r["final_idx"], r["placed"]
+    # no expert over capacity; a token's final experts are distinct candidates of its own
+    assert np.bincount(fi[pl], minlength=N).max() <= cap
+    for t in range(T):
+        got = fi[t][pl[t]]
+        assert len(set(got.tolist())) == got.size
+        assert set(got.tolist()) <= set(cand[t].tolist())
+    # the first pass is the plain capacity rule
+    g = oracle.group(cand[:, :k], N, cap)
+    first = (g["inv_pos"] >= 0)
+    assert (pl | ~first).all() and (r["final_cand"][first] < k).all()
+    assert (r["final_cand"][first] == np.nonzero(first)[1]).all()
+    # re-routed slots are exactly the placed slots beyond the first pass
+    assert r["rerouted"] == int(pl.sum() - first.sum())
+    if R == 0:
+        assert r["rerouted"] == 0 and (pl == first).all()
+    # unlimited capacity: nothing moves
+    u = oracle.reroute(cand, k, R, N, T * k)
+    assert u["rerouted"] == 0 and (u["final_idx"] == cand[:, :k]).all()
+    # weights: a softmax over the k final experts
+    assert np.allclose(r["final_w"].sum(1), 1.0)

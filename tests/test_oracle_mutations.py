@@ -40,6 +40,14 @@ MUTANTS = [
      "if (best < 0 || freq[e] >= freq[best]) best = e;"),
     ("balance_without_N", "stats[5] = N * bal;", "stats[5] = bal;"),
     ("prob_not_normalised", "p[e] += exp(l[e] - m) / s;", "p[e] += exp(l[e] - m);"),
+    ("reroute_same_candidate", "if (!placed[a] && ptr[t] < kr) prop[a] = ptr[t]++;",
+     "if (!placed[a] && ptr[t] < kr) prop[a] = ptr[t];"),
+    ("reroute_capacity_off_by_one",
+     "if (e >= 0 && e < N && used[e] < capacity) {\n          used[e]++;\n          placed[a] = 1;",
+     "if (e >= 0 && e < N && used[e] <= capacity) {\n          used[e]++;\n          placed[a] = 1;"),
+    ("reroute_weights_first_choice",
+     "const int e = cand[(size_t)t * kr + final_cand[(size_t)t * k + j]];\n        final_w",
+     "const int e = cand[(size_t)t * kr + j];\n        final_w"),
 ]
 
 
