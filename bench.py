@@ -58,6 +58,9 @@ def parse():
                     help="override N (smaller profiling cases with the same per-expert shape)")
     ap.add_argument("--ffn-dim", type=int, default=0,
                     help="override f (e.g. tiny experts to profile the router alone)")
+    ap.add_argument("--reroute", type=int, default=0,
+                    help="re-route capacity overflow to the next-best expert in R rounds "
+                         "(layers with a capacity factor only)")
     ap.add_argument("--forward-only", action="store_true",
                     help="time moe_forward only (no stage, end-to-end or CPU legs)")
     return ap.parse_args()
@@ -266,7 +269,7 @@ def run_ours(args, ws, rank, local):
     y_dtype = torch.float32 if args.y_dtype == "f32" else torch.bfloat16
     layer = B.MoELayer(inp.W_g, inp.W_gate, inp.W_up, inp.W_down, cfg.k, bias=inp.bias,
                        Ws_gate=inp.Ws_gate, Ws_up=inp.Ws_up, Ws_down=inp.Ws_down,
-                       capacity_factor=cfg.cf, y_dtype=y_dtype)
+                       capacity_factor=cfg.cf, y_dtype=y_dtype, reroute_rounds=args.reroute)
     y = torch.empty((cfg.T, cfg.d), dtype=y_dtype, device=dev)
     outs = layer.outputs_for(cfg.T, dev)
     a = layer.args(inp.x, y, outs)
@@ -342,6 +345,10 @@ def run_ours(args, ws, rank, local):
                                                           y_perm=y_perm, A_max=A_max), reps),
         "combine": time_stage(lambda: B.moe_combine(y_perm, perm["inv_pos"], y=y), reps),
     }
+    if args.reroute > 0:
+        cand, cand_w = B.moe_router_topk(inp.x, inp.W_g, k + args.reroute, bias=inp.bias)
+        stage_ms["permute_reroute"] = time_stage(
+            lambda: B.moe_permute_reroute(cand, cand_w, N, k, cap, x=inp.x), reps)
     # routing diagnostics from the router's logits and the pre-capacity counts
     lg_buf = torch.empty((cfg.T, N), dtype=torch.float32, device=inp.x.device)
     B.moe_router_topk(inp.x, inp.W_g, k, bias=inp.bias, logits=lg_buf)
@@ -412,7 +419,9 @@ def run_ours(args, ws, rank, local):
         "vs_baseline": None,
         "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
         "data": "synthetic (seeded Gaussian x and N(0,1/fan_in) weights of the workload's shape)",
-        "config": {"workload": cfg_desc(cfg), "T": cfg.T, "d": cfg.d, "f": cfg.f, "N": N,
+        "config": {"workload": cfg_desc(cfg) + (f", overflow re-routed in {args.reroute} rounds"
+                                                 if args.reroute else ""),
+                   "reroute_rounds": args.reroute, "T": cfg.T, "d": cfg.d, "f": cfg.f, "N": N,
                    "k": k, "fs": cfg.fs, "capacity_factor": cfg.cf, "bias_std": cfg.bias_std,
                    "y_dtype": args.y_dtype, "parallelism": f"replicas x{ws} (no exchange)",
                    "l2": "256 MB L2 flush write between steps, outside the timed events; "
@@ -441,6 +450,7 @@ def run_ours(args, ws, rank, local):
                         if unit == "TFLOP/s" else {})},
         "stages_ms": {k_: round(v, 4) for k_, v in stage_ms.items()},
         "routing": {"kept_rows": A, "dropped": int(outs["dropped"].item()),
+                    "rerouted": int(outs["rerouted"].item()), "reroute_rounds": args.reroute,
                     "touched_experts": touched, "max_rows_per_expert": int(kept.max().item()),
                     "min_rows_per_expert": int(kept.min().item())},
         "e2e": {"value": round(ws * cfg.T / (e2e_max / 1e3), 1), "unit": "tokens/s",

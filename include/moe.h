@@ -148,6 +148,43 @@ moe_status_t moe_permute_noalloc(const int32_t *topk_idx, const float *topk_w,
                                  int32_t *device_status, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * Step 4b: dispatch with capacity overflow RE-ROUTED to the next-best expert.
+ * Source: "MoE稀疏激活原理与工程实践", 2.2 (专家容量的硬约束: a token whose
+ * selected expert already holds its capacity goes to its next-best expert).
+ *   cand_idx [T,k+R] int32: each token's experts by rank (moe_router_topk
+ *     with k+R); cand_w [T,k+R] fp32: the router's softmax over those k+R.
+ *   First pass: each expert keeps its first `capacity` assignments by token
+ *   index (as moe_permute).  Then R rounds: every slot still without an
+ *   expert proposes its token's next untried candidate (ranks k, k+1, ...,
+ *   taken in slot order, used up whether granted or not); each expert grants
+ *   its remaining room to the round's proposals in (token, slot) order.  A
+ *   slot unplaced after R rounds is dropped.
+ *   final_idx [T,k] out: each slot's expert, -1 if dropped.
+ *   final_w [T,k] out: softmax over the token's final experts' logits (the
+ *     k+R softmax renormalised over them; a dropped slot keeps its first
+ *     choice in the denominator and contributes nothing).
+ *   demand [N] out (may be NULL): first-choice assignments per expert before
+ *     the capacity (the router's selection frequency).
+ *   counts, offsets, perm_token, row_scale, inv_pos, x_perm, dropped: as
+ *     moe_permute, over the final selection (counts = placed per expert).
+ *   rerouted: scalar out (may be NULL), slots placed in rounds >= 1.
+ *   capacity >= 1, 0 <= R, k + R <= N <= 1024.  Deterministic.
+ *   Workspace: moe_permute_reroute_workspace_size(T, N, k, R).
+ * ------------------------------------------------------------------------- */
+size_t moe_permute_reroute_workspace_size(int T, int N, int k, int R);
+moe_status_t moe_permute_reroute(const int32_t *cand_idx, const float *cand_w,
+                                 const void *x, moe_dtype_t dtype, int T, int d,
+                                 int N, int k, int R, int capacity,
+                                 int32_t *final_idx, float *final_w,
+                                 int32_t *demand, int32_t *counts,
+                                 int32_t *offsets, int32_t *perm_token,
+                                 float *row_scale, int32_t *inv_pos,
+                                 void *x_perm, int32_t *dropped,
+                                 int32_t *rerouted, int32_t *device_status,
+                                 void *workspace, size_t workspace_bytes,
+                                 void *stream);
+
+/* ---------------------------------------------------------------------------
  * Step 5: grouped expert FFN (SwiGLU) over permuted rows.
  *   x_perm [A_max,d] (dtype): rows of expert e are offsets[e]..offsets[e+1]-1.
  *   offsets [N+1] device int32 (from moe_permute); offsets[N] <= A_max.
@@ -206,6 +243,11 @@ typedef struct moe_forward_args {
   int32_t *inv_pos;           /* [T,k] optional output                       */
   int32_t *dropped;           /* scalar optional output                      */
   int32_t *device_status;     /* scalar, OR-ed MOE_DEV_* bits, optional      */
+  int reroute_rounds;         /* 0: overflow dropped; R > 0 (with a capacity):
+                                 overflow re-routed in R rounds, see
+                                 moe_permute_reroute; topk_idx/topk_w then
+                                 hold the final selection (-1 = dropped)     */
+  int32_t *rerouted;          /* scalar optional output: slots re-routed     */
 } moe_forward_args;
 
 size_t moe_forward_workspace_size(const moe_forward_args *args);

@@ -26,7 +26,8 @@ EXPORTS = ("moe_status_string", "moe_last_error", "moe_version", "moe_launch_cou
            "moe_permute_noalloc",
            "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
            "moe_forward_workspace_size", "moe_forward", "moe_forward_host_io",
-           "moe_routing_stats_workspace_size", "moe_routing_stats")
+           "moe_routing_stats_workspace_size", "moe_routing_stats",
+           "moe_permute_reroute_workspace_size", "moe_permute_reroute")
 
 
 class MoEError(RuntimeError):
@@ -48,7 +49,8 @@ class moe_forward_args(ctypes.Structure):
                 ("topk_idx", ctypes.c_void_p), ("topk_w", ctypes.c_void_p),
                 ("counts", ctypes.c_void_p), ("offsets", ctypes.c_void_p),
                 ("inv_pos", ctypes.c_void_p), ("dropped", ctypes.c_void_p),
-                ("device_status", ctypes.c_void_p)]
+                ("device_status", ctypes.c_void_p), ("reroute_rounds", ctypes.c_int),
+                ("rerouted", ctypes.c_void_p)]
 
 
 _lib = None
@@ -89,8 +91,12 @@ def lib():
         L.moe_routing_stats_workspace_size.argtypes = [ci, ci]
         L.moe_routing_stats_workspace_size.restype = sz
         L.moe_routing_stats.argtypes = [vp, vp, ci, ci, vp, vp, vp, vp, sz, vp]
+        L.moe_permute_reroute_workspace_size.argtypes = [ci, ci, ci, ci]
+        L.moe_permute_reroute_workspace_size.restype = sz
+        L.moe_permute_reroute.argtypes = ([vp, vp, vp, ci, ci, ci, ci, ci, ci, ci] + [vp] * 13 +
+                                          [sz, vp])
         for n in ("moe_router_topk", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn",
-                  "moe_combine", "moe_routing_stats",
+                  "moe_combine", "moe_routing_stats", "moe_permute_reroute",
                   "moe_forward", "moe_forward_host_io"):
             getattr(L, n).restype = ci
         _lib = L
@@ -262,6 +268,42 @@ def routing_stats_dict(stats):
                 balance=st.balance, top3=list(st.top3), assignments=st.assignments)
 
 
+def moe_permute_reroute(cand_idx, cand_w, N, k, capacity, x=None, demand=False,
+                        device_status=None, stream=None):
+    """Dispatch with capacity overflow re-routed (cand_idx/cand_w [T, k+R] from
+    moe_router_topk with k+R).  Returns dict final_idx, final_w, counts,
+    offsets, perm_token, row_scale, inv_pos, x_perm (if x), dropped, rerouted,
+    demand (if asked)."""
+    _cuda(cand_idx, cand_w, x)
+    T, kr = cand_idx.shape
+    R = kr - k
+    dev = cand_idx.device
+    d = x.shape[1] if x is not None else 0
+    A = T * k
+    out = dict(final_idx=torch.empty((T, k), dtype=torch.int32, device=dev),
+               final_w=torch.empty((T, k), dtype=torch.float32, device=dev),
+               counts=torch.empty(N, dtype=torch.int32, device=dev),
+               offsets=torch.empty(N + 1, dtype=torch.int32, device=dev),
+               perm_token=torch.empty(max(A, 1), dtype=torch.int32, device=dev),
+               row_scale=torch.empty(max(A, 1), dtype=torch.float32, device=dev),
+               inv_pos=torch.empty((T, k), dtype=torch.int32, device=dev),
+               dropped=torch.zeros(1, dtype=torch.int32, device=dev),
+               rerouted=torch.zeros(1, dtype=torch.int32, device=dev))
+    if demand:
+        out["demand"] = torch.empty(N, dtype=torch.int32, device=dev)
+    if x is not None:
+        out["x_perm"] = torch.empty((max(A, 1), d), dtype=x.dtype, device=dev)
+    ws_bytes = lib().moe_permute_reroute_workspace_size(T, N, k, R)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    _check("moe_permute_reroute", lib().moe_permute_reroute(
+        _p(cand_idx), _p(cand_w), _p(x), _dt(x) if x is not None else 1, T, d, N, k, R,
+        int(capacity), _p(out["final_idx"]), _p(out["final_w"]), _p(out.get("demand")),
+        _p(out["counts"]), _p(out["offsets"]), _p(out["perm_token"]), _p(out["row_scale"]),
+        _p(out["inv_pos"]), _p(out.get("x_perm")), _p(out["dropped"]), _p(out["rerouted"]),
+        _p(device_status), _p(ws), ws_bytes, _stream(stream)))
+    return out
+
+
 def moe_combine(y_perm, inv_pos, shared_y=None, y=None, y_dtype=torch.float32, stream=None):
     _cuda(y_perm, inv_pos, shared_y, y)
     T, k = inv_pos.shape
@@ -276,7 +318,7 @@ def moe_combine(y_perm, inv_pos, shared_y=None, y=None, y_dtype=torch.float32, s
 
 def make_forward_args(x, W_g, W_gate, W_up, W_down, k, y, bias=None, Ws_gate=None,
                       Ws_up=None, Ws_down=None, capacity_factor=0.0, outputs=None,
-                      device_status=None):
+                      device_status=None, reroute_rounds=0):
     _cuda(x, W_g, W_gate, W_up, W_down, y, bias, Ws_gate, Ws_up, Ws_down)
     T, d = x.shape
     N, _, f = W_gate.shape
@@ -292,6 +334,8 @@ def make_forward_args(x, W_g, W_gate, W_up, W_down, k, y, bias=None, Ws_gate=Non
     for key in ("logits", "topk_idx", "topk_w", "counts", "offsets", "inv_pos", "dropped"):
         setattr(a, key, _p(o.get(key)))
     a.device_status = _p(device_status)
+    a.reroute_rounds = int(reroute_rounds)
+    a.rerouted = _p(o.get("rerouted"))
     return a
 
 
@@ -323,7 +367,8 @@ class MoELayer:
     """
 
     def __init__(self, W_g, W_gate, W_up, W_down, k, bias=None, Ws_gate=None, Ws_up=None,
-                 Ws_down=None, capacity_factor=0.0, y_dtype=torch.float32):
+                 Ws_down=None, capacity_factor=0.0, y_dtype=torch.float32, reroute_rounds=0):
+        self.reroute_rounds = reroute_rounds
         self.W_g, self.W_gate, self.W_up, self.W_down = W_g, W_gate, W_up, W_down
         self.k, self.bias, self.cf, self.y_dtype = k, bias, capacity_factor, y_dtype
         self.Ws_gate, self.Ws_up, self.Ws_down = Ws_gate, Ws_up, Ws_down
@@ -339,6 +384,7 @@ class MoELayer:
                  offsets=torch.empty(N + 1, dtype=torch.int32, device=device),
                  inv_pos=torch.empty((T, k), dtype=torch.int32, device=device),
                  dropped=torch.zeros(1, dtype=torch.int32, device=device),
+                 rerouted=torch.zeros(1, dtype=torch.int32, device=device),
                  device_status=torch.zeros(1, dtype=torch.int32, device=device))
         if logits:
             o["logits"] = torch.empty((T, N), dtype=torch.float32, device=device)
@@ -348,7 +394,8 @@ class MoELayer:
         return make_forward_args(x, self.W_g, self.W_gate, self.W_up, self.W_down, self.k, y,
                                  bias=self.bias, Ws_gate=self.Ws_gate, Ws_up=self.Ws_up,
                                  Ws_down=self.Ws_down, capacity_factor=self.cf,
-                                 outputs=outputs, device_status=outputs.get("device_status"))
+                                 outputs=outputs, device_status=outputs.get("device_status"),
+                                 reroute_rounds=self.reroute_rounds)
 
     def workspace(self, args, device):
         n = moe_forward_workspace_size(args)

@@ -90,6 +90,9 @@ struct ForwardLayout {
   int32_t *topk_idx, *counts, *offsets, *inv_pos, *perm_token, *dropped, *sh_offsets;
   float *topk_w, *row_scale;
   void *x_perm, *y_perm, *ffn_ws, *perm_ws, *ys, *sh_ffn_ws;
+  int32_t *cand;     // [T, k+R] router candidates (re-routing only)
+  float *cand_w;     // [T, k+R]
+  void *rr_ws;       // re-routing workspace
   size_t bytes;
 };
 
@@ -112,6 +115,12 @@ ForwardLayout layout_forward(const moe_forward_args *a, void *ws) {
   L.y_perm = c.take_bytes((size_t)A_max * a->d * es);
   L.ffn_ws = c.take_bytes(ffn_workspace_bytes((int)A_max, a->d, a->f, a->N, a->dtype));
   L.perm_ws = c.take_bytes(permute_workspace_bytes(a->T, a->N, a->k));
+  if (a->reroute_rounds > 0) {
+    const size_t tkr = (size_t)a->T * (a->k + a->reroute_rounds);
+    L.cand = c.take<int32_t>(tkr);
+    L.cand_w = c.take<float>(tkr);
+    L.rr_ws = c.take_bytes(reroute_workspace_bytes(a->T, a->N, a->k));
+  }
   if (a->fs > 0) {
     L.sh_offsets = c.take<int32_t>(2);
     L.ys = c.take_bytes((size_t)a->T * a->d * es);
@@ -274,6 +283,47 @@ moe_status_t moe_expert_ffn(const void *x_perm, const int32_t *offsets, const fl
                            static_cast<cudaStream_t>(stream));
 }
 
+size_t moe_permute_reroute_workspace_size(int T, int N, int k, int R) {
+  if (T < 0 || N < 1 || k < 1 || R < 0) return 0;
+  return reroute_workspace_bytes(T, N, k);
+}
+
+moe_status_t moe_permute_reroute(const int32_t *cand_idx, const float *cand_w, const void *x,
+                                 moe_dtype_t dtype, int T, int d, int N, int k, int R,
+                                 int capacity, int32_t *final_idx, float *final_w,
+                                 int32_t *demand, int32_t *counts, int32_t *offsets,
+                                 int32_t *perm_token, float *row_scale, int32_t *inv_pos,
+                                 void *x_perm, int32_t *dropped, int32_t *rerouted,
+                                 int32_t *device_status, void *workspace,
+                                 size_t workspace_bytes, void *stream) {
+  CHECK_ARG(dtype_ok(dtype), "dtype %d is not MOE_F32 or MOE_BF16", (int)dtype);
+  CHECK_ARG(T >= 0 && N >= 1 && k >= 1 && R >= 0 && k + R <= N && capacity >= 1,
+            "bad sizes T=%d N=%d k=%d R=%d capacity=%d (need k+R <= N, capacity >= 1)", T, N,
+            k, R, capacity);
+  CHECK_ARG(counts && offsets && perm_token && inv_pos && final_idx && final_w &&
+                (T == 0 || (cand_idx && cand_w)),
+            "required pointer is NULL");
+  if (x_perm) {
+    CHECK_ARG(x && d >= 8 && d % 8 == 0, "x_perm needs x and d %% 8 == 0 (d=%d)", d);
+    CHECK_ARG(aligned16(x) && aligned16(x_perm), "x / x_perm must be 16-byte aligned");
+  }
+  if (N > 1024) {
+    set_error("moe_permute_reroute supports N <= 1024");
+    return MOE_ERR_UNSUPPORTED;
+  }
+  const size_t need = reroute_workspace_bytes(T, N, k);
+  if (!workspace || workspace_bytes < need) {
+    set_error("moe_permute_reroute: workspace %zu bytes, needs %zu", workspace_bytes, need);
+    return MOE_ERR_WORKSPACE;
+  }
+  moe_status_t s = check_device();
+  if (s != MOE_OK) return s;
+  return launch_permute_reroute(cand_idx, cand_w, x, dtype, T, d, N, k, R, capacity, final_idx,
+                                final_w, demand, counts, offsets, perm_token, row_scale,
+                                inv_pos, x_perm, dropped, rerouted, device_status, workspace,
+                                static_cast<cudaStream_t>(stream));
+}
+
 size_t moe_routing_stats_workspace_size(int T, int N) {
   if (T < 0 || N < 1) return 0;
   return routing_stats_workspace_bytes(T, N);
@@ -331,6 +381,16 @@ static moe_status_t validate_forward(const moe_forward_args *a) {
     set_error("N <= 256 and k <= 32 are supported (got N=%d k=%d)", a->N, a->k);
     return MOE_ERR_UNSUPPORTED;
   }
+  CHECK_ARG(a->reroute_rounds >= 0, "reroute_rounds=%d must be >= 0", a->reroute_rounds);
+  if (a->reroute_rounds > 0) {
+    CHECK_ARG(a->capacity_factor > 0, "re-routing needs a capacity (capacity_factor > 0)");
+    CHECK_ARG(a->k + a->reroute_rounds <= a->N, "k + reroute_rounds = %d exceeds N = %d",
+              a->k + a->reroute_rounds, a->N);
+    if (a->k + a->reroute_rounds > 32) {
+      set_error("k + reroute_rounds <= 32 is supported (got %d)", a->k + a->reroute_rounds);
+      return MOE_ERR_UNSUPPORTED;
+    }
+  }
   return MOE_OK;
 }
 
@@ -358,13 +418,27 @@ moe_status_t moe_forward(const moe_forward_args *a, void *workspace, size_t work
   const int cap = moe_capacity(a->capacity_factor, a->T, a->k, a->N);
   const int A_max = (int)routed_rows_max(a->T, a->N, a->k, cap);
 
-  s = launch_router_topk(a->x, a->W_g, a->router_bias, a->dtype, a->T, a->d, a->N, a->k,
-                         a->logits, L.topk_idx, L.topk_w, a->device_status, stream);
-  if (s != MOE_OK) return s;
-  s = launch_permute(L.topk_idx, L.topk_w, a->x, a->dtype, a->T, a->d, a->N, a->k, cap,
-                     L.counts, L.offsets, L.perm_token, L.row_scale, L.inv_pos, L.x_perm,
-                     L.dropped, a->device_status, L.perm_ws, stream);
-  if (s != MOE_OK) return s;
+  if (a->reroute_rounds > 0) {
+    // the router ranks k+R candidates; the dispatch re-routes overflow to them
+    const int kr = a->k + a->reroute_rounds;
+    s = launch_router_topk(a->x, a->W_g, a->router_bias, a->dtype, a->T, a->d, a->N, kr,
+                           a->logits, L.cand, L.cand_w, a->device_status, stream);
+    if (s != MOE_OK) return s;
+    s = launch_permute_reroute(L.cand, L.cand_w, a->x, a->dtype, a->T, a->d, a->N, a->k,
+                               a->reroute_rounds, cap, L.topk_idx, L.topk_w, nullptr, L.counts,
+                               L.offsets, L.perm_token, L.row_scale, L.inv_pos, L.x_perm,
+                               L.dropped, a->rerouted, a->device_status, L.rr_ws, stream);
+    if (s != MOE_OK) return s;
+  } else {
+    s = launch_router_topk(a->x, a->W_g, a->router_bias, a->dtype, a->T, a->d, a->N, a->k,
+                           a->logits, L.topk_idx, L.topk_w, a->device_status, stream);
+    if (s != MOE_OK) return s;
+    s = launch_permute(L.topk_idx, L.topk_w, a->x, a->dtype, a->T, a->d, a->N, a->k, cap,
+                       L.counts, L.offsets, L.perm_token, L.row_scale, L.inv_pos, L.x_perm,
+                       L.dropped, a->device_status, L.perm_ws, stream);
+    if (s != MOE_OK) return s;
+    if (a->rerouted) MOE_CUDA_TRY(cudaMemsetAsync(a->rerouted, 0, sizeof(int32_t), stream));
+  }
   s = launch_expert_ffn(L.x_perm, L.offsets, L.row_scale, A_max, a->d, a->f, a->N, cap,
                         a->dtype, a->W_gate, a->W_up, a->W_down, L.y_perm, a->device_status,
                         L.ffn_ws, stream);

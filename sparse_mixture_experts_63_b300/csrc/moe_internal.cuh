@@ -78,7 +78,8 @@ moe_status_t launch_permute(const int32_t *topk_idx, const float *topk_w, const 
                             int32_t *counts, int32_t *offsets, int32_t *perm_token,
                             float *row_scale, int32_t *inv_pos, void *x_perm,
                             int32_t *dropped, int32_t *device_status, void *workspace,
-                            cudaStream_t stream);
+                            cudaStream_t stream,
+                            bool neg_one_drops = false);
 
 size_t ffn_workspace_bytes(int A_max, int d, int f, int N, moe_dtype_t dtype);
 // capacity: rows per expert the dispatch kept at most (0 = unknown/none); a
@@ -89,6 +90,15 @@ moe_status_t launch_expert_ffn(const void *x_perm, const int32_t *offsets,
                                const void *W_up, const void *W_down, void *y_perm,
                                int32_t *device_status, void *workspace, cudaStream_t stream);
 
+size_t reroute_workspace_bytes(int T, int N, int k);
+moe_status_t launch_permute_reroute(const int32_t *cand, const float *cand_w, const void *x,
+                                    moe_dtype_t dtype, int T, int d, int N, int k, int R,
+                                    int capacity, int32_t *final_idx, float *final_w,
+                                    int32_t *demand, int32_t *counts, int32_t *offsets,
+                                    int32_t *perm_token, float *row_scale, int32_t *inv_pos,
+                                    void *x_perm, int32_t *dropped, int32_t *rerouted,
+                                    int32_t *device_status, void *workspace,
+                                    cudaStream_t stream);
 size_t routing_stats_workspace_bytes(int T, int N);
 moe_status_t launch_routing_stats(const float *logits, const int32_t *counts, int T, int N,
                                   moe_routing_stats_t *stats, float *freq, float *prob_mean,

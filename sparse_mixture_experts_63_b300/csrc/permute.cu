@@ -27,10 +27,12 @@ constexpr int kChunkTokens = 256;  // tokens per chunk (CTA) in hist / scatter
 constexpr int kThreads = 256;
 constexpr int kMaxN = 1024;
 
+// neg_one_drops: an id of -1 marks a slot already known to be dropped (no
+// report); any other id outside [0, N) is reported as a bad expert id.
 __global__ void __launch_bounds__(kThreads) permute_hist(const int32_t *__restrict__ topk_idx,
                                                          int T, int N, int k,
                                                          int32_t *__restrict__ hist,
-                                                         int32_t *status) {
+                                                         int32_t *status, int neg_one_drops) {
   extern __shared__ int32_t sh_hist[];  // [N]
   for (int e = threadIdx.x; e < N; e += blockDim.x) sh_hist[e] = 0;
   __syncthreads();
@@ -41,7 +43,7 @@ __global__ void __launch_bounds__(kThreads) permute_hist(const int32_t *__restri
     int e = topk_idx[a];
     if (e >= 0 && e < N)
       atomicAdd(&sh_hist[e], 1);
-    else
+    else if (!(neg_one_drops && e == -1))
       bad = true;
   }
   if (bad) report(status, MOE_DEV_BAD_EXPERT_ID);
@@ -197,7 +199,8 @@ moe_status_t launch_permute(const int32_t *topk_idx, const float *topk_w, const 
                             moe_dtype_t dtype, int T, int d, int N, int k, int capacity,
                             int32_t *counts, int32_t *offsets, int32_t *perm_token,
                             float *row_scale, int32_t *inv_pos, void *x_perm, int32_t *dropped,
-                            int32_t *device_status, void *workspace, cudaStream_t stream) {
+                            int32_t *device_status, void *workspace, cudaStream_t stream,
+                            bool neg_one_drops) {
   if (N > kMaxN) {
     set_error("moe_permute: N=%d above %d", N, kMaxN);
     return MOE_ERR_UNSUPPORTED;
@@ -205,8 +208,8 @@ moe_status_t launch_permute(const int32_t *topk_idx, const float *topk_w, const 
   int32_t *hist = static_cast<int32_t *>(workspace);
   const int nchunks = (T + kChunkTokens - 1) / kChunkTokens;
   if (nchunks > 0) {
-    permute_hist<<<nchunks, kThreads, N * sizeof(int32_t), stream>>>(topk_idx, T, N, k, hist,
-                                                                     device_status);
+    permute_hist<<<nchunks, kThreads, N * sizeof(int32_t), stream>>>(
+        topk_idx, T, N, k, hist, device_status, neg_one_drops ? 1 : 0);
     MOE_LAUNCH_CHECK();
   }
   permute_scan<<<1, kMaxN, 0, stream>>>(hist, nchunks, T, N, k, capacity, counts, offsets,

@@ -116,3 +116,28 @@ def test_routing_stats_rejects_bad_arguments(lib):
     assert need >= 4 * 64 * 4            # ceil(1000 / 256) chunks x 64 experts, fp32
     assert lib.moe_routing_stats(4096, 4096, 1000, 64, 4096, None, None, None, need - 1,
                                  None) == 3
+
+
+def test_permute_reroute_rejects_bad_arguments(lib):
+    p = 4096
+    # capacity 0 (re-routing needs one), k + R > N, workspace too small
+    assert lib.moe_permute_reroute(p, p, None, 1, 16, 64, 8, 2, 1, 0, p, p, None, p, p, p, p, p,
+                                   None, None, None, None, p, 1 << 20, None) == 1
+    assert lib.moe_permute_reroute(p, p, None, 1, 16, 64, 8, 2, 7, 5, p, p, None, p, p, p, p, p,
+                                   None, None, None, None, p, 1 << 20, None) == 1
+    need = lib.moe_permute_reroute_workspace_size(16, 8, 2, 2)
+    assert need > 0
+    assert lib.moe_permute_reroute(p, p, None, 1, 16, 64, 8, 2, 2, 5, p, p, None, p, p, p, p, p,
+                                   None, None, None, None, p, need - 1, None) == 3
+
+
+def test_forward_reroute_needs_capacity(lib):
+    a = B.moe_forward_args()
+    a.T, a.d, a.f, a.N, a.k, a.dtype, a.y_dtype = 16, 64, 64, 8, 2, 1, 0
+    a.x = a.W_g = a.W_gate = a.W_up = a.W_down = a.y = 4096
+    a.reroute_rounds = 2
+    assert lib.moe_forward_workspace_size(ctypes.byref(a)) == 0      # no capacity factor
+    a.capacity_factor = 1.0
+    assert lib.moe_forward_workspace_size(ctypes.byref(a)) > 0
+    a.reroute_rounds = 7                                             # k + R > N
+    assert lib.moe_forward_workspace_size(ctypes.byref(a)) == 0
