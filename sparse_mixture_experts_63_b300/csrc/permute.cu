@@ -149,6 +149,92 @@ __global__ void __launch_bounds__(kThreads) permute_scatter(
   }
 }
 
+// All of hist, scan and scatter in one CTA when every token fits one chunk
+// (T <= 256) and N <= 256: the same order and ranks as the three kernels
+// (assignments in index order = token order), without their launch gaps --
+// decode-sized batches spent most of the dispatch time between launches.
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallMaxN = 256;
+
+__global__ void __launch_bounds__(kSmallThreads) permute_small(
+    const int32_t *__restrict__ topk_idx, const float *__restrict__ topk_w, int T, int N, int k,
+    int capacity, int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+    int32_t *__restrict__ perm_token, float *__restrict__ row_scale,
+    int32_t *__restrict__ inv_pos, int32_t *__restrict__ dropped, int32_t *status,
+    int neg_one_drops) {
+  constexpr int kWarps = kSmallThreads / 32;
+  __shared__ int32_t hist[kSmallMaxN];
+  __shared__ int32_t off_s[kSmallMaxN + 1];
+  __shared__ int32_t running[kSmallMaxN];
+  __shared__ int32_t warp_cnt[kWarps * kSmallMaxN];
+  const int A = T * k;
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    hist[e] = 0;
+    running[e] = 0;
+  }
+  __syncthreads();
+  bool bad = false;
+  for (int a = threadIdx.x; a < A; a += blockDim.x) {
+    const int e = topk_idx[a];
+    if (e >= 0 && e < N)
+      atomicAdd(&hist[e], 1);
+    else if (!(neg_one_drops && e == -1))
+      bad = true;
+  }
+  if (bad) report(status, MOE_DEV_BAD_EXPERT_ID);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int32_t acc = 0;
+    for (int e = 0; e < N; ++e) {
+      const int32_t c = hist[e];
+      counts[e] = c;
+      off_s[e] = acc;
+      offsets[e] = acc;
+      acc += (capacity > 0 && c > capacity) ? capacity : c;
+    }
+    off_s[N] = acc;
+    offsets[N] = acc;
+    if (dropped) *dropped = A - acc;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x % 32, w = threadIdx.x / 32;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int base = 0; base < A; base += kSmallThreads) {
+    for (int q = threadIdx.x; q < kWarps * N; q += blockDim.x) warp_cnt[q] = 0;
+    __syncthreads();
+    const int a = base + threadIdx.x;
+    const int e = (a < A) ? topk_idx[a] : -1;
+    const bool valid = (e >= 0 && e < N);
+    const int key = valid ? e : -1 - (int)threadIdx.x;
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    const int rank_in_warp = __popc(peers & lt_mask);
+    const bool last_of_group = (peers >> lane) == 1u;
+    if (valid && last_of_group) warp_cnt[w * N + e] = rank_in_warp + 1;
+    __syncthreads();
+    if (valid) {
+      int32_t r = running[e] + rank_in_warp;
+      for (int w2 = 0; w2 < w; ++w2) r += warp_cnt[w2 * N + e];
+      if (capacity > 0 && r >= capacity) {
+        inv_pos[a] = -1;
+      } else {
+        const int32_t p = off_s[e] + r;
+        inv_pos[a] = p;
+        perm_token[p] = a / k;
+        if (row_scale) row_scale[p] = topk_w[a];
+      }
+    } else if (a < A) {
+      inv_pos[a] = -1;
+    }
+    __syncthreads();
+    for (int q = threadIdx.x; q < N; q += blockDim.x) {
+      int32_t s2 = 0;
+      for (int w2 = 0; w2 < kWarps; ++w2) s2 += warp_cnt[w2 * N + q];
+      running[q] += s2;
+    }
+    __syncthreads();
+  }
+}
+
 // One warp per token (grid-stride): the row is read once, four 16-byte
 // vectors per lane in flight, and written to the position of each kept slot
 // (inv_pos < 0: dropped).  Slots are taken 32 at a time (one per lane).
@@ -207,6 +293,12 @@ moe_status_t launch_permute(const int32_t *topk_idx, const float *topk_w, const 
   }
   int32_t *hist = static_cast<int32_t *>(workspace);
   const int nchunks = (T + kChunkTokens - 1) / kChunkTokens;
+  if (nchunks == 1 && N <= kSmallMaxN) {
+    permute_small<<<1, kSmallThreads, 0, stream>>>(topk_idx, topk_w, T, N, k, capacity, counts,
+                                                   offsets, perm_token, row_scale, inv_pos,
+                                                   dropped, device_status, neg_one_drops ? 1 : 0);
+    MOE_LAUNCH_CHECK();
+  } else {
   if (nchunks > 0) {
     permute_hist<<<nchunks, kThreads, N * sizeof(int32_t), stream>>>(
         topk_idx, T, N, k, hist, device_status, neg_one_drops ? 1 : 0);
@@ -221,6 +313,7 @@ moe_status_t launch_permute(const int32_t *topk_idx, const float *topk_w, const 
                                                          hist, offsets, perm_token, row_scale,
                                                          inv_pos);
     MOE_LAUNCH_CHECK();
+  }
   }
   if (x_perm && T > 0) {
     const size_t row_bytes = (size_t)d * (dtype == MOE_BF16 ? 2 : 4);

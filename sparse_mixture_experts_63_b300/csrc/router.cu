@@ -90,9 +90,18 @@ __global__ void __launch_bounds__(256) router_small_n(const T *__restrict__ x,
                                                       int32_t *status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   T *ws = reinterpret_cast<T *>(smem_raw);  // [d][NP], zero-padded experts
-  for (int i = threadIdx.x; i < d * NP; i += blockDim.x) {
-    int r = i / NP, c = i % NP;
-    ws[i] = c < N ? Wg[(size_t)r * N + c] : from_f32<T>(0.f);
+  if (N == NP && (reinterpret_cast<uintptr_t>(Wg) & 15) == 0) {
+    // no padding: a straight copy in 16-byte vectors, several in flight
+    const uint4 *src = reinterpret_cast<const uint4 *>(Wg);
+    uint4 *dst = reinterpret_cast<uint4 *>(ws);
+    const int n16 = (int)((size_t)d * NP * sizeof(T) / 16);
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = __ldg(src + i);
+  } else {
+    for (int i = threadIdx.x; i < d * NP; i += blockDim.x) {
+      int r = i / NP, c = i % NP;
+      ws[i] = c < N ? Wg[(size_t)r * N + c] : from_f32<T>(0.f);
+    }
   }
   __syncthreads();
   const int lane = threadIdx.x % kWarp;
@@ -246,19 +255,31 @@ moe_status_t launch_typed(const void *x, const void *W_g, const float *bias, int
       int warps = 8;
       int grid = (T_ + warps - 1) / warps;
       if (grid > 148 * 8) grid = 148 * 8;
+      // the shared-memory opt-in is set once per kernel variant (a driver
+      // call on every launch cost more than the kernel at decode sizes)
+      static int smem_set[3] = {0, 0, 0};
       if (NP == 8) {
-        MOE_CUDA_TRY(cudaFuncSetAttribute(router_small_n<T, 8>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        if (smem_set[0] < (int)smem) {
+          MOE_CUDA_TRY(cudaFuncSetAttribute(router_small_n<T, 8>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
+          smem_set[0] = 200 * 1024;
+        }
         router_small_n<T, 8><<<grid, 256, smem, stream>>>(xp, wp, bias, T_, d, N, k, logits,
                                                           topk_idx, topk_w, status);
       } else if (NP == 16) {
-        MOE_CUDA_TRY(cudaFuncSetAttribute(router_small_n<T, 16>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        if (smem_set[1] < (int)smem) {
+          MOE_CUDA_TRY(cudaFuncSetAttribute(router_small_n<T, 16>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
+          smem_set[1] = 200 * 1024;
+        }
         router_small_n<T, 16><<<grid, 256, smem, stream>>>(xp, wp, bias, T_, d, N, k, logits,
                                                            topk_idx, topk_w, status);
       } else {
-        MOE_CUDA_TRY(cudaFuncSetAttribute(router_small_n<T, 32>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        if (smem_set[2] < (int)smem) {
+          MOE_CUDA_TRY(cudaFuncSetAttribute(router_small_n<T, 32>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
+          smem_set[2] = 200 * 1024;
+        }
         router_small_n<T, 32><<<grid, 256, smem, stream>>>(xp, wp, bias, T_, d, N, k, logits,
                                                            topk_idx, topk_w, status);
       }
@@ -289,8 +310,12 @@ moe_status_t launch_router_topk(const void *x, const void *W_g, const float *bia
                                 moe_dtype_t dtype, int T, int d, int N, int k, float *logits,
                                 int32_t *topk_idx, float *topk_w, int32_t *device_status,
                                 cudaStream_t stream) {
-  if (dtype == MOE_BF16) {
-    // Tensor cores when the expert count suits them (N % 8 == 0, N <= 256).
+  // Tensor cores when the expert count suits them (N % 8 == 0, N <= 256) and
+  // the batch fills more than a few 128-token tiles; a decode-sized batch
+  // (T <= 512) with few experts (N <= 32) takes the CUDA-core kernel, which
+  // gives every token its own warp instead of one latency-bound tile.
+  const bool small_batch = T <= 512 && N <= 32;
+  if (dtype == MOE_BF16 && !small_batch) {
     moe_status_t s = launch_router_tc(x, W_g, bias, T, d, N, k, logits, topk_idx, topk_w,
                                       device_status, stream);
     if (s != MOE_ERR_UNSUPPORTED) return s;

@@ -115,7 +115,9 @@ def test_router_ties_and_nan():
 @pytest.mark.parametrize("T,N,k,cap,skew", [(1000, 8, 2, 0, 0.0), (2049, 256, 8, 0, 0.5),
                                             (4096, 128, 2, 80, 3.0), (300, 4, 4, 0, 0.0),
                                             (777, 32, 3, 50, 2.0), (1, 8, 2, 0, 0.0),
-                                            (513, 64, 1, 1, 0.0)])
+                                            (513, 64, 1, 1, 0.0), (256, 256, 8, 0, 0.5),
+                                            (200, 32, 3, 5, 2.0), (64, 1024, 2, 0, 1.0),
+                                            (32, 8, 2, 0, 0.0)])
 def test_permute_stage_bit_exact(T, N, k, cap, skew):
     rng = np.random.default_rng(T + N)
     p = np.exp(skew * rng.normal(size=N)); p /= p.sum()
@@ -454,3 +456,35 @@ def test_layer_with_reroute(name, R):
     parity.assert_y_close(y[torch.as_tensor(sel, device=y.device)].float().cpu().numpy(), y_o,
                           cfg.dtype)
     print(name, R, "rerouted", ref["rerouted"], "dropped", int(out["dropped"].item()))
+
+
+@pytest.mark.parametrize("name", ["capacity_small", "deepseek_small"])
+def test_forward_captures_into_a_cuda_graph(name):
+    """moe_forward only enqueues work (no sync, no host read-back), so it can
+    be captured into a CUDA graph; a replay gives the direct call's output."""
+    cfg = REDUCED[name]
+    inp = make_inputs(cfg, device=_cuda())
+    layer = B.MoELayer(inp.W_g, inp.W_gate, inp.W_up, inp.W_down, cfg.k, bias=inp.bias,
+                       Ws_gate=inp.Ws_gate, Ws_up=inp.Ws_up, Ws_down=inp.Ws_down,
+                       capacity_factor=cfg.cf)
+    y = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device="cuda")
+    o = layer.outputs_for(cfg.T, y.device)
+    a = layer.args(inp.x, y, o)
+    ws = layer.workspace(a, y.device)
+    B.moe_forward(a, ws)
+    torch.cuda.synchronize()
+    y_direct = y.clone()
+    y.zero_()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        B.moe_forward(a, ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        B.moe_forward(a, ws)
+    y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_direct)
