@@ -24,6 +24,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import torch
@@ -75,7 +76,8 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        self.path = os.path.join(tempfile.gettempdir(),
+                                 f"moe_bench_clocks_gpu{gpu_index}_{os.getpid()}.csv")
 
     def start(self):
         try:
@@ -141,12 +143,19 @@ def barrier(ws):
 
 
 def reduce_max(v, ws):
+    """The slowest rank's value (NCCL on GPUs, gloo on CPU)."""
     if ws == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_value(ws, tokens_per_rank, ms_max):
+    """tokens/s of the whole job: every rank's batch over the slowest rank's time."""
+    return ws * tokens_per_rank / (ms_max / 1e3)
 
 
 def cfg_desc(cfg):
@@ -391,7 +400,7 @@ def run_ours(args, ws, rank, local):
     work = RL.layer_work(cfg.T, cfg.d, cfg.f, N, k, A, touched, cfg.fs, esz)
     pk = RL.peaks()
     t_roof, bound, t_flop, t_bytes = RL.roofline_time_s(work, pk)
-    value = ws * cfg.T / (ms_max / 1e3)
+    value = whole_job_value(ws, cfg.T, ms_max)
 
     # dominant kernel: the grouped expert FFN (gate/up + SwiGLU, down + gate scale)
     ffn_ms = stage_ms["expert_ffn"]
