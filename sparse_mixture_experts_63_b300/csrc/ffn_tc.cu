@@ -626,43 +626,45 @@ int raster_group(int K) {
   return (int)(g < 1 ? 1 : g > 64 ? 64 : g);
 }
 
-// Co-resident CTA pairs on this device (one pair per two SMs at most).
+// Co-resident CTA pairs on this device (one pair per two SMs at most),
+// asked once per device.
 int max_pairs() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * (sms / 2));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int c = 0;
-    if (cudaOccupancyMaxActiveClusters(&c, grouped_gemm_tc, &cfg) != cudaSuccess || c <= 0) {
-      cudaGetLastError();
-      c = sms / 2;
-    }
-    n = c < sms / 2 ? c : sms / 2;
+  static int cached[kMaxDevicesCached] = {};
+  const int dev = current_device();
+  if (dev < kMaxDevicesCached && cached[dev]) return cached[dev];
+  int sms = 148;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * (sms / 2));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int c = 0;
+  if (cudaOccupancyMaxActiveClusters(&c, grouped_gemm_tc, &cfg) != cudaSuccess || c <= 0) {
+    cudaGetLastError();
+    c = sms / 2;
   }
+  const int n = c < sms / 2 ? c : sms / 2;
+  if (dev < kMaxDevicesCached) cached[dev] = n;
   return n;
 }
 
 moe_status_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap *b,
                          const TcParams &p, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
+  static bool attr_set[kMaxDevicesCached] = {};
+  const int dev = current_device();
+  if (dev >= kMaxDevicesCached || !attr_set[dev]) {
     MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
     MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc,
                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 0));
-    attr_set = true;
+    if (dev < kMaxDevicesCached) attr_set[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];

@@ -73,6 +73,15 @@ moe_status_t launch_router_topk(const void *x, const void *W_g, const float *bia
                                 int32_t *device_status, cudaStream_t stream);
 
 size_t permute_workspace_bytes(int T, int N, int k);
+// Launch attributes and occupancy answers are per device; a process may drive
+// several GPUs, so the launchers remember them per device index.
+constexpr int kMaxDevicesCached = 64;
+inline int current_device() {
+  int d = 0;
+  cudaGetDevice(&d);
+  return d;
+}
+
 moe_status_t launch_permute(const int32_t *topk_idx, const float *topk_w, const void *x,
                             moe_dtype_t dtype, int T, int d, int N, int k, int capacity,
                             int32_t *counts, int32_t *offsets, int32_t *perm_token,

@@ -112,18 +112,35 @@ __global__ void __launch_bounds__(256) router_small_n(const T *__restrict__ x,
     float acc[NP];
 #pragma unroll
     for (int c = 0; c < NP; ++c) acc[c] = 0.f;
-    for (int i0 = lane * 8; i0 < d; i0 += kWarp * 8) {
-      float xv[8];
-      load8(xr + i0, xv);
+    // four 16-byte loads of x in flight per lane before the math (one at a
+    // time, a decode-sized batch waited on DRAM latency 16 times per token)
+    constexpr int kX = 4;
+    for (int i0 = lane * 8; i0 < d; i0 += kWarp * 8 * kX) {
+      float xv[kX][8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const T *wr = ws + (size_t)(i0 + u) * NP;
+      for (int q = 0; q < kX; ++q) {
+        const int ii = i0 + q * kWarp * 8;
+        if (ii < d) {
+          load8(xr + ii, xv[q]);
+        } else {
 #pragma unroll
-        for (int c = 0; c < NP; c += 8) {
-          float wv[8];
-          load8(wr + c, wv);
+          for (int u = 0; u < 8; ++u) xv[q][u] = 0.f;
+        }
+      }
 #pragma unroll
-          for (int q = 0; q < 8; ++q) acc[c + q] = fmaf(xv[u], wv[q], acc[c + q]);
+      for (int q = 0; q < kX; ++q) {
+        const int ii = i0 + q * kWarp * 8;
+        if (ii >= d) break;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const T *wr = ws + (size_t)(ii + u) * NP;
+#pragma unroll
+          for (int c = 0; c < NP; c += 8) {
+            float wv[8];
+            load8(wr + c, wv);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) acc[c + r] = fmaf(xv[q][u], wv[r], acc[c + r]);
+          }
         }
       }
     }
@@ -146,6 +163,75 @@ __global__ void __launch_bounds__(256) router_small_n(const T *__restrict__ x,
     nan_seen |= warp_topk_softmax<1>(v, e, k, lane, topk_idx + (size_t)t * k,
                                      topk_w + (size_t)t * k);
   }
+  if (nan_seen) report(status, MOE_DEV_NAN_LOGIT);
+}
+
+// ---------------------------------------------------------------------------
+// Decode-sized batches (T <= 512, N <= 32): one CTA of kDecWarps warps per
+// token, the warps splitting d; W_g is read from L2 (it is small and every
+// token's CTA reads it), x once.  Lane partials are summed over the warp, the
+// warps' sums in warp order in shared memory, then warp 0 ranks.  Each lane
+// keeps all its 16-byte loads of a step in flight, so a token waits on memory
+// a few times, not once per step of d.
+// ---------------------------------------------------------------------------
+constexpr int kDecWarps = 4;
+
+template <typename T, int NP>
+__global__ void __launch_bounds__(kDecWarps * 32) router_decode(
+    const T *__restrict__ x, const T *__restrict__ Wg, const float *__restrict__ bias, int Tn,
+    int d, int N, int k, float *logits, int32_t *topk_idx, float *topk_w, int32_t *status) {
+  __shared__ float part[kDecWarps][NP];
+  const int t = blockIdx.x;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const T *xr = x + (size_t)t * d;
+  float acc[NP];
+#pragma unroll
+  for (int c = 0; c < NP; ++c) acc[c] = 0.f;
+  const bool vec = (N == NP) && ((reinterpret_cast<uintptr_t>(Wg) & 15) == 0);
+  // lane (warp w) takes 8 consecutive columns of d at i0 = 8 * (w * 32 + lane) + step
+#pragma unroll 4
+  for (int i0 = 8 * (warp * 32 + lane); i0 < d; i0 += 8 * 32 * kDecWarps) {
+    float xv[8];
+    load8(xr + i0, xv);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const T *wr = Wg + (size_t)(i0 + u) * N;
+      if (vec) {
+#pragma unroll
+        for (int c = 0; c < NP; c += 8) {
+          float wv[8];
+          load8(wr + c, wv);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[c + q] = fmaf(xv[u], wv[q], acc[c + q]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < NP; ++c)
+          if (c < N) acc[c] = fmaf(xv[u], to_f32(wr[c]), acc[c]);
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < NP; ++c) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], off);
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int c = 0; c < NP; ++c) part[warp][c] = acc[c];
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  float mine = 0.f;
+  if (lane < N) {
+    for (int w = 0; w < kDecWarps; ++w) mine += part[w][lane];
+    if (bias) mine += bias[lane];
+    if (logits) logits[(size_t)t * N + lane] = mine;
+  }
+  float v[1] = {mine};
+  int e[1] = {lane < N ? lane : -1};
+  const bool nan_seen = warp_topk_softmax<1>(v, e, k, lane, topk_idx + (size_t)t * k,
+                                             topk_w + (size_t)t * k);
   if (nan_seen) report(status, MOE_DEV_NAN_LOGIT);
 }
 
@@ -248,6 +334,19 @@ moe_status_t launch_typed(const void *x, const void *W_g, const float *bias, int
   const T *xp = static_cast<const T *>(x);
   const T *wp = static_cast<const T *>(W_g);
   if (T_ == 0) return MOE_OK;
+  if (T_ <= 512 && N <= 32 && d % 8 == 0) {
+    if (N <= 8)
+      router_decode<T, 8><<<T_, kDecWarps * 32, 0, stream>>>(xp, wp, bias, T_, d, N, k, logits,
+                                                             topk_idx, topk_w, status);
+    else if (N <= 16)
+      router_decode<T, 16><<<T_, kDecWarps * 32, 0, stream>>>(xp, wp, bias, T_, d, N, k, logits,
+                                                              topk_idx, topk_w, status);
+    else
+      router_decode<T, 32><<<T_, kDecWarps * 32, 0, stream>>>(xp, wp, bias, T_, d, N, k, logits,
+                                                              topk_idx, topk_w, status);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+  }
   if (N <= 32) {
     int NP = N <= 8 ? 8 : (N <= 16 ? 16 : 32);
     size_t smem = (size_t)d * NP * sizeof(T);
@@ -257,28 +356,30 @@ moe_status_t launch_typed(const void *x, const void *W_g, const float *bias, int
       if (grid > 148 * 8) grid = 148 * 8;
       // the shared-memory opt-in is set once per kernel variant (a driver
       // call on every launch cost more than the kernel at decode sizes)
-      static int smem_set[3] = {0, 0, 0};
+      static bool smem_set[kMaxDevicesCached][3] = {};
+      const int dev = current_device();
+      bool *done = dev < kMaxDevicesCached ? smem_set[dev] : nullptr;
       if (NP == 8) {
-        if (smem_set[0] < (int)smem) {
+        if (!done || !done[0]) {
           MOE_CUDA_TRY(cudaFuncSetAttribute(router_small_n<T, 8>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
-          smem_set[0] = 200 * 1024;
+          if (done) done[0] = true;
         }
         router_small_n<T, 8><<<grid, 256, smem, stream>>>(xp, wp, bias, T_, d, N, k, logits,
                                                           topk_idx, topk_w, status);
       } else if (NP == 16) {
-        if (smem_set[1] < (int)smem) {
+        if (!done || !done[1]) {
           MOE_CUDA_TRY(cudaFuncSetAttribute(router_small_n<T, 16>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
-          smem_set[1] = 200 * 1024;
+          if (done) done[1] = true;
         }
         router_small_n<T, 16><<<grid, 256, smem, stream>>>(xp, wp, bias, T_, d, N, k, logits,
                                                            topk_idx, topk_w, status);
       } else {
-        if (smem_set[2] < (int)smem) {
+        if (!done || !done[2]) {
           MOE_CUDA_TRY(cudaFuncSetAttribute(router_small_n<T, 32>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
-          smem_set[2] = 200 * 1024;
+          if (done) done[2] = true;
         }
         router_small_n<T, 32><<<grid, 256, smem, stream>>>(xp, wp, bias, T_, d, N, k, logits,
                                                            topk_idx, topk_w, status);

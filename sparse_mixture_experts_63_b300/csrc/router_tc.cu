@@ -352,11 +352,12 @@ template <int KMAX>
 moe_status_t launch_k(const CUtensorMap &tx, const CUtensorMap &tw, const RParams &p, int tiles,
                       cudaStream_t stream) {
   constexpr int smem = kStageRegion + 2 * KMAX * kBM * 4 + 1024;   // stages + candidate lists
-  static bool attr = false;
-  if (!attr) {
+  static bool attr[kMaxDevicesCached] = {};
+  const int dev = current_device();
+  if (dev >= kMaxDevicesCached || !attr[dev]) {
     MOE_CUDA_TRY(cudaFuncSetAttribute(router_tc_kernel<KMAX>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-    attr = true;
+    if (dev < kMaxDevicesCached) attr[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attrs[1];
