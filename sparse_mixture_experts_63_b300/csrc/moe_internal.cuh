@@ -90,6 +90,11 @@ moe_status_t launch_permute(const int32_t *topk_idx, const float *topk_w, const 
                             cudaStream_t stream,
                             bool neg_one_drops = false);
 
+// Copies each token's row of x to the positions inv_pos gives its slots
+// (-1: dropped), in token order; nothing when x_perm is null.
+moe_status_t launch_copy_rows(const void *x, moe_dtype_t dtype, const int32_t *inv_pos, int T,
+                              int d, int k, void *x_perm, cudaStream_t stream);
+
 size_t ffn_workspace_bytes(int A_max, int d, int f, int N, moe_dtype_t dtype);
 // capacity: rows per expert the dispatch kept at most (0 = unknown/none); a
 // tiling hint only.

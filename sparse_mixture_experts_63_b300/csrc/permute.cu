@@ -315,6 +315,11 @@ moe_status_t launch_permute(const int32_t *topk_idx, const float *topk_w, const 
     MOE_LAUNCH_CHECK();
   }
   }
+  return launch_copy_rows(x, dtype, inv_pos, T, d, k, x_perm, stream);
+}
+
+moe_status_t launch_copy_rows(const void *x, moe_dtype_t dtype, const int32_t *inv_pos, int T,
+                              int d, int k, void *x_perm, cudaStream_t stream) {
   if (x_perm && T > 0) {
     const size_t row_bytes = (size_t)d * (dtype == MOE_BF16 ? 2 : 4);
     const int vecs = (int)(row_bytes / 16);

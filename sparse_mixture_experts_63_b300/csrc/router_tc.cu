@@ -65,11 +65,6 @@ struct RParams {
 };
 
 __device__ __forceinline__ float rank_key(float v) { return isnan(v) ? -INFINITY : v; }
-__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
-  float ka = rank_key(va), kb = rank_key(vb);
-  if (ka != kb) return ka > kb;
-  return ia < ib;
-}
 
 __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
   float v;
@@ -95,7 +90,8 @@ __device__ __forceinline__ void insert_sorted(float (&bv)[KMAX], int (&bi)[KMAX]
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) {
     const float kj = rank_key(bv[j]);
-    // same order as ranks_before, written without branches
+    // rank order: larger key first (NaN lowest), equal keys by lower index;
+    // written without branches
     gt[j] = (j < k) & ((kv > kj) | ((kv == kj) & (e < bi[j])));
   }
 #pragma unroll

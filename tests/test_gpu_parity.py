@@ -367,9 +367,15 @@ def _reroute_inputs(T, N, k, R, skew, seed):
     return lg, cand.astype(np.int32), w.astype(np.float32)
 
 
+# N <= 512 with every 256-token chunk resident at once: one cooperative
+# launch (40000 tokens = 157 chunks, more than one CTA on some SMs); N = 600:
+# the round-by-round launches.
 @pytest.mark.parametrize("T,N,k,R,cap,skew", [(1000, 8, 2, 2, 200, 1.0), (4096, 128, 2, 2, 80, 1.0),
                                               (777, 32, 3, 4, 50, 2.0), (300, 4, 1, 3, 60, 1.5),
-                                              (513, 64, 1, 1, 1, 0.0), (1, 8, 2, 2, 1, 0.0)])
+                                              (513, 64, 1, 1, 1, 0.0), (1, 8, 2, 2, 1, 0.0),
+                                              (40000, 64, 2, 3, 700, 1.5),
+                                              (3000, 512, 4, 2, 12, 1.0),
+                                              (2000, 600, 2, 2, 5, 1.0)])
 def test_permute_reroute_stage(T, N, k, R, cap, skew):
     lg, cand, cw = _reroute_inputs(T, N, k, R, skew, T + N + R)
     d = 64
@@ -458,15 +464,17 @@ def test_layer_with_reroute(name, R):
     print(name, R, "rerouted", ref["rerouted"], "dropped", int(out["dropped"].item()))
 
 
-@pytest.mark.parametrize("name", ["capacity_small", "deepseek_small"])
-def test_forward_captures_into_a_cuda_graph(name):
+@pytest.mark.parametrize("name,R", [("capacity_small", 0), ("deepseek_small", 0),
+                                    ("capacity_small", 2)])
+def test_forward_captures_into_a_cuda_graph(name, R):
     """moe_forward only enqueues work (no sync, no host read-back), so it can
-    be captured into a CUDA graph; a replay gives the direct call's output."""
+    be captured into a CUDA graph; a replay gives the direct call's output.
+    With re-routing the graph holds the cooperative single-launch rounds."""
     cfg = REDUCED[name]
     inp = make_inputs(cfg, device=_cuda())
     layer = B.MoELayer(inp.W_g, inp.W_gate, inp.W_up, inp.W_down, cfg.k, bias=inp.bias,
                        Ws_gate=inp.Ws_gate, Ws_up=inp.Ws_up, Ws_down=inp.Ws_down,
-                       capacity_factor=cfg.cf)
+                       capacity_factor=cfg.cf, reroute_rounds=R)
     y = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device="cuda")
     o = layer.outputs_for(cfg.T, y.device)
     a = layer.args(inp.x, y, o)
