@@ -20,7 +20,7 @@ from . import build as _build
 
 _lib = None
 
-F32, BF16 = 0, 1
+F32, BF16, F64 = 0, 1, 2
 
 
 def _load(path=None):
@@ -42,6 +42,12 @@ def _load(path=None):
         lib.oracle_combine_rows.argtypes = [ci, ci, ci, i32p, f64p, f64p, f64p, f64p]
         lib.oracle_routing_stats.argtypes = [ci, ci, f64p, i32p, f64p, i32p, f64p, f64p]
         lib.oracle_reroute.argtypes = [ci, ci, ci, ci, ci, i32p, f64p, i32p, i32p, i32p, f64p]
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_long, vp, f64p]
+        lib.oracle_e4m3_decode.restype = None
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_long, f32p, vp]
+        lib.oracle_e4m3_encode.restype = None
+        lib.oracle_quantize_rows_e4m3.argtypes = [ci, ci, ci, vp, vp, f32p]
+        lib.oracle_quantize_weights_e4m3.argtypes = [ci, ci, ci, ci, vp, vp, f32p]
         lib.oracle_moe_forward.argtypes = (
             [ci] * 6 + [vp, vp, f32p, vp, vp, vp, ci, vp, vp, vp, cd, f64p, f64p,
                         i32p, f64p, i32p, i32p, i32p, i32p, ci])
@@ -73,13 +79,15 @@ class _Buf:
                 self.dtype = BF16
             elif a.dtype == torch.float32:
                 self.dtype = F32
+            elif a.dtype == torch.float64:
+                self.dtype = F64
             else:
                 self.dtype = None
             self.keep = a
             self.ptr = a.data_ptr()
         else:
             a = np.ascontiguousarray(a)
-            self.dtype = F32 if a.dtype == np.float32 else None
+            self.dtype = {np.dtype(np.float32): F32, np.dtype(np.float64): F64}.get(a.dtype)
             self.keep = a
             self.ptr = a.ctypes.data
 
@@ -338,3 +346,83 @@ def near_tie_tokens(logits, k, rel=1e-4):
     return np.abs(a - b) < rel * scale
 
 
+
+
+# --------------------------------------------------------------------------
+# FP8 E4M3 expert weights and activations (absmax scales; see moe_oracle.c)
+# --------------------------------------------------------------------------
+def e4m3_decode(codes):
+    """Values (fp64) of E4M3 codes (uint8 array of any shape)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_e4m3_decode(c.size, c.ctypes.data, out.ctypes.data)
+    return out
+
+
+def e4m3_encode(values):
+    """Nearest E4M3 codes (ties to even, saturating at 448) of fp32 values."""
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().oracle_e4m3_encode(v.size, v.ctypes.data, out.ctypes.data)
+    return out
+
+
+def quantize_rows_e4m3(x):
+    """Per-row absmax E4M3: x [R,C] -> (codes uint8 [R,C], scales float32 [R])."""
+    b = _Buf(x)
+    assert b.dtype in (F32, BF16)
+    R, C = b.keep.shape
+    q = np.empty((R, C), dtype=np.uint8)
+    sc = np.empty(R, dtype=np.float32)
+    _check(_load().oracle_quantize_rows_e4m3(R, C, b.dtype, b.ptr, q.ctypes.data,
+                                             sc.ctypes.data), "oracle_quantize_rows_e4m3")
+    return q, sc
+
+
+def quantize_weights_e4m3(W):
+    """Per-output-channel absmax E4M3 of gate/up weights W [N,d,f]:
+    (codes uint8 [N,f,d], scales float32 [N,f])."""
+    b = _Buf(W)
+    assert b.dtype in (F32, BF16)
+    N, d, f = b.keep.shape
+    q = np.empty((N, f, d), dtype=np.uint8)
+    sc = np.empty((N, f), dtype=np.float32)
+    _check(_load().oracle_quantize_weights_e4m3(N, d, f, b.dtype, b.ptr, q.ctypes.data,
+                                                sc.ctypes.data), "oracle_quantize_weights_e4m3")
+    return q, sc
+
+
+def dequantize_e4m3(codes, scales):
+    """decode(codes) * scale, one scale per leading-axis row (exact in fp64)."""
+    return e4m3_decode(codes) * np.asarray(scales, dtype=np.float64)[..., None]
+
+
+def expert_rows_fp8(qg_e, sg_e, qu_e, su_e, W_down_e, xq_rows, sx_rows, nthreads=None):
+    """SwiGLU expert with E4M3 gate/up weights (codes [f,d], scales [f]) on E4M3
+    token rows (codes [R,d], scales [R]); the down projection W_down_e [f,d]
+    as given.  Every value is the exact dequantised one; fp64 throughout."""
+    wg = np.ascontiguousarray(dequantize_e4m3(qg_e, sg_e).T)
+    wu = np.ascontiguousarray(dequantize_e4m3(qu_e, su_e).T)
+    wd = W_down_e.detach().cpu().double().contiguous() if isinstance(W_down_e, torch.Tensor) \
+        else np.ascontiguousarray(W_down_e, dtype=np.float64)
+    xr = dequantize_e4m3(xq_rows, sx_rows)
+    return expert_rows(wg, wu, wd, xr, nthreads)
+
+
+def forward_rows_fp8(xq_rows, sx_rows, topk_idx_rows, topk_w_rows, inv_pos_rows,
+                     fetch_expert_fp8, nthreads=None):
+    """Layer output for a subset of tokens with E4M3 gate/up weights and token
+    rows: fetch_expert_fp8(e) -> (qg [f,d], sg [f], qu [f,d], su [f], W_down [f,d]).
+    Experts one at a time (each dequantised expert is held in fp64).
+    Returns y [R,d] fp64."""
+    idx = _i32(topk_idx_rows)
+    inv = _i32(inv_pos_rows)
+    R, k = idx.shape
+    d = xq_rows.shape[1]
+    out = np.zeros((R, k, d), dtype=np.float64)
+    for e in sorted(set(int(v) for v in idx[inv >= 0].ravel())):
+        rows, slots = np.nonzero((idx == e) & (inv >= 0))
+        qg, sg, qu, su, wd = fetch_expert_fp8(e)
+        out[rows, slots] = expert_rows_fp8(qg, sg, qu, su, wd, xq_rows[rows], sx_rows[rows],
+                                           nthreads)
+    return combine_rows(inv, topk_w_rows, out)

@@ -26,7 +26,9 @@
  *   - capacity C = ceil(cf * T * k / N); an assignment is kept iff its 0-based
  *     rank among the assignments of its expert, ordered by token index, is < C;
  *     a dropped slot contributes zero and the kept weights are not renormalised;
- *   - the optional shared expert is added with weight 1, outside the softmax.
+ *   - the optional shared expert is added with weight 1, outside the softmax;
+ *   - low-precision expert weights are calibration-free FP8 E4M3 with one
+ *     absmax scale per output channel (gate/up) and per token row (x).
  *
  * Parity pins for this file live in tests/test_oracle.py.  The fp64 values of
  * the expert FFN have no printed worked example on the pages; they are pinned
@@ -38,11 +40,12 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F64 = 2 };
 
-/* Widen element i of a float32 or bf16 array to double, exactly. */
+/* Widen element i of a float32, bf16 or double array to double, exactly. */
 static double elem(const void *p, int dtype, size_t i) {
   if (dtype == ORACLE_F32) return (double)((const float *)p)[i];
+  if (dtype == ORACLE_F64) return ((const double *)p)[i];
   uint32_t bits = ((uint32_t)((const uint16_t *)p)[i]) << 16;
   float f;
   memcpy(&f, &bits, sizeof f);
@@ -569,5 +572,99 @@ int oracle_reroute(int T, int N, int k, int R, int capacity, const int32_t *cand
     }
   }
   free(used); free(ptr); free(prop);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Low-precision expert weights: FP8 E4M3 with absmax scales.                 */
+/* [MoE-DSV4] "MoE模型推理部署与显存优化实战" (inference is bound by memory     */
+/* bandwidth; the third remedy is quantising the weights to fewer bits, with  */
+/* FP8 named for the cached activations); [MoE-Sparse] 4.3 (weights cut from  */
+/* 16-bit to fewer bits to shrink memory).  Reading: calibration-free FP8     */
+/* E4M3 (OCP 8-bit floating point: 1 sign, 4 exponent bits with bias 7, 3     */
+/* mantissa bits, no infinities, S.1111.111 = NaN, largest finite 448).       */
+/* A vector v (one token's row of x, or one output channel of a gate/up       */
+/* weight matrix over d) is stored as codes q = E4M3(v * (448 / amax|v|)),    */
+/* rounded to nearest with ties to an even mantissa and saturated at 448,     */
+/* and one fp32 scale amax / 448 (both factors formed in fp32; an all-zero    */
+/* vector takes scale 1).  Its value is decode(q) * scale.                    */
+/* ------------------------------------------------------------------------- */
+
+/* Value of an E4M3 code, from the format's definition. */
+static double e4m3_value(uint8_t c) {
+  const int s = c >> 7, e = (c >> 3) & 0xF, m = c & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);          /* subnormal: m/8 * 2^-6 */
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7); /* normal: (1 + m/8) * 2^(e-7) */
+  return s ? -v : v;
+}
+
+/* Nearest finite E4M3 code to v (|v| > 448 -> +-448), ties to the code with
+ * an even mantissa; found by comparing v against every finite magnitude. */
+static uint8_t e4m3_encode(float vf) {
+  const double v = (double)vf;
+  const uint8_t sign = (v < 0.0 || (v == 0.0 && signbit(v))) ? 0x80 : 0;
+  const double a = fabs(v);
+  if (isnan(v)) return (uint8_t)(sign | 0x7F);
+  if (isinf(v)) return (uint8_t)(sign | 0x7E);
+  uint8_t best = 0;
+  double best_err = INFINITY;
+  for (int c = 0; c <= 0x7E; ++c) {          /* finite non-negative codes */
+    const double err = fabs(e4m3_value((uint8_t)c) - a);
+    if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+      best = (uint8_t)c;
+      best_err = err;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+void oracle_e4m3_decode(long n, const uint8_t *codes, double *out) {
+  for (long i = 0; i < n; ++i) out[i] = e4m3_value(codes[i]);
+}
+
+void oracle_e4m3_encode(long n, const float *v, uint8_t *codes) {
+  for (long i = 0; i < n; ++i) codes[i] = e4m3_encode(v[i]);
+}
+
+/* One vector of n elements at stride `stride` (element i at p[i * stride]):
+ * codes to q[i * qstride], scale to *scale. */
+static void quantize_vector(const void *p, int dtype, size_t base, size_t stride, int n,
+                            uint8_t *q, size_t qstride, float *scale) {
+  float amax = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    const float a = fabsf((float)elem(p, dtype, base + (size_t)i * stride));
+    if (a > amax) amax = a;
+  }
+  const float inv = amax > 0.0f ? 448.0f / amax : 1.0f;
+  *scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+  for (int i = 0; i < n; ++i) {
+    const float v = (float)elem(p, dtype, base + (size_t)i * stride) * inv;
+    q[(size_t)i * qstride] = e4m3_encode(v);
+  }
+}
+
+/* Rows of x [R, C]: codes [R, C], scales [R]. */
+int oracle_quantize_rows_e4m3(int R, int C, int dtype, const void *x, uint8_t *q,
+                              float *scale) {
+  if (R < 0 || C < 1 || (R > 0 && (!x || !q || !scale))) return 1;
+  for (int r = 0; r < R; ++r)
+    quantize_vector(x, dtype, (size_t)r * C, 1, C, q + (size_t)r * C, 1, scale + r);
+  return 0;
+}
+
+/* Gate/up weights W [N, d, f] per output channel j (a column over d):
+ * codes [N, f, d] (channel-major: each channel's d codes contiguous),
+ * scales [N, f]. */
+int oracle_quantize_weights_e4m3(int N, int d, int f, int dtype, const void *W, uint8_t *q,
+                                 float *scale) {
+  if (N < 1 || d < 1 || f < 1 || !W || !q || !scale) return 1;
+  for (int e = 0; e < N; ++e)
+    for (int j = 0; j < f; ++j)
+      quantize_vector(W, dtype, (size_t)e * d * f + j, (size_t)f, d,
+                      q + ((size_t)e * f + j) * d, 1, scale + (size_t)e * f + j);
   return 0;
 }

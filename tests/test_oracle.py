@@ -543,3 +543,121 @@ def test_reroute_invariants(T, N, k, R, cap, seed):
     assert u["rerouted"] == 0 and (u["final_idx"] == cand[:, :k]).all()
     # weights: a softmax over the k final experts
     assert np.allclose(r["final_w"].sum(1), 1.0)
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3 expert weights and activations
+# ---------------------------------------------------------------------------
+def test_e4m3_decode_spec_values():
+    """Values the OCP 8-bit floating-point definition fixes for E4M3 (bias 7,
+    subnormals m/8 * 2^-6, largest finite 448, S.1111.111 = NaN)."""
+    cases = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0,
+             0x3C: 1.5, 0x40: 2.0, 0x77: 240.0, 0x78: 256.0, 0x7E: 448.0, 0xFE: -448.0,
+             0xB8: -1.0, 0x81: -(2.0 ** -9)}
+    got = oracle.e4m3_decode(np.array(list(cases), dtype=np.uint8))
+    assert got.tolist() == list(cases.values())
+    assert np.isnan(oracle.e4m3_decode(np.array([0x7F, 0xFF], dtype=np.uint8))).all()
+
+
+def test_e4m3_decode_matches_torch_float8():
+    """Every code against torch's own float8_e4m3fn type (a library routine)."""
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    got = oracle.e4m3_decode(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+
+
+def test_e4m3_encode_matches_torch_rounding():
+    """Round to nearest, ties to even, against torch's float32 -> float8_e4m3fn
+    cast: random magnitudes over the whole finite range and every midpoint
+    between neighbouring codes (the tie cases)."""
+    rng = np.random.default_rng(7)
+    mags = np.exp2(rng.uniform(-12, np.log2(448.0), 20000))
+    v = (mags * rng.choice([-1.0, 1.0], mags.size)).astype(np.float32)
+    vals = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)
+    v = np.concatenate([v, mids, -mids, np.float32([0.0, 448.0, -448.0])])
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = oracle.e4m3_encode(v)
+    np.testing.assert_array_equal(got, ref)
+    # two ties by hand: 1.0625 lies between 1.0 (m=0) and 1.125 (m=1) -> 1.0;
+    # 1.1875 between 1.125 (m=1) and 1.25 (m=2) -> 1.25
+    assert oracle.e4m3_encode(np.float32([1.0625, 1.1875])).tolist() == [0x38, 0x3A]
+
+
+def test_e4m3_encode_saturates():
+    v = np.float32([449.0, 464.0, 1e6, -1e6, np.inf, -np.inf])
+    assert oracle.e4m3_encode(v).tolist() == [0x7E, 0x7E, 0x7E, 0xFE, 0x7E, 0xFE]
+
+
+def test_quantize_rows_e4m3_exact_and_bounded():
+    rng = np.random.default_rng(3)
+    # rows that are codes times a power of two come back exactly
+    codes = rng.integers(0, 0x7E, size=(5, 96)).astype(np.uint8)
+    codes[:, 7] = 0x7E                                    # each row's absmax is 448
+    codes ^= rng.integers(0, 2, size=codes.shape).astype(np.uint8) << 7
+    s = 2.0 ** rng.integers(-6, 4, size=5)
+    x = torch.from_numpy(oracle.e4m3_decode(codes) * s[:, None]).to(torch.bfloat16)
+    assert torch.equal(x.double(), torch.from_numpy(oracle.e4m3_decode(codes) * s[:, None]))
+    q, sc = oracle.quantize_rows_e4m3(x)
+    np.testing.assert_array_equal(q, codes)
+    np.testing.assert_array_equal(sc, (448.0 * s / 448.0).astype(np.float32))
+    # random rows: the absmax element takes +-448; every element within half a
+    # step of E4M3 (relative 2^-4 in the normal range, 2^-10 absolute below it)
+    x = (torch.randn(64, 300, generator=torch.Generator().manual_seed(5)) * 3).to(torch.bfloat16)
+    q, sc = oracle.quantize_rows_e4m3(x)
+    xv = x.double().numpy()
+    am = np.abs(xv).argmax(1)
+    assert (q[np.arange(64), am] & 0x7F == 0x7E).all()
+    v = (x.float().numpy() * (np.float32(448.0) / np.abs(x.float().numpy()).max(1))[:, None])
+    err = np.abs(oracle.e4m3_decode(q) - v)
+    step = np.where(np.abs(v) >= 2.0 ** -6, np.exp2(np.floor(np.log2(np.maximum(np.abs(v),
+                                                                                 1e-30))) - 3),
+                    2.0 ** -9)
+    assert (err <= step / 2 + 1e-12).all()
+    # an all-zero row: codes 0, scale 1
+    q0, s0 = oracle.quantize_rows_e4m3(torch.zeros(2, 16))
+    assert (q0 == 0).all() and (s0 == 1.0).all()
+
+
+def test_quantize_weights_e4m3_per_output_channel():
+    """W [N,d,f] -> codes [N,f,d]: output channel j of expert e is column j of
+    W[e] over d, quantised with its own absmax."""
+    rng = np.random.default_rng(11)
+    N, d, f = 3, 40, 24
+    codes = rng.integers(0, 0x7E, size=(N, f, d)).astype(np.uint8)
+    codes[:, :, 5] = 0x7E
+    s = 2.0 ** rng.integers(-8, 0, size=(N, f))
+    W = np.transpose(oracle.e4m3_decode(codes) * s[..., None], (0, 2, 1))   # [N,d,f]
+    q, sc = oracle.quantize_weights_e4m3(torch.from_numpy(W).to(torch.bfloat16))
+    np.testing.assert_array_equal(q, codes)
+    np.testing.assert_array_equal(sc, s.astype(np.float32))
+
+
+def test_fp8_expert_equals_bf16_expert_on_representable_values():
+    """When x and the gate/up weights are exactly E4M3 values times their
+    scales, the FP8 expert is the bf16 expert: the dequantised operands, the
+    scales' axes (per token row, per output channel) and the SwiGLU are fed
+    through unchanged."""
+    rng = np.random.default_rng(21)
+    R, d, f = 9, 48, 32
+    cx = rng.integers(0, 0x7E, size=(R, d)).astype(np.uint8) | \
+        (rng.integers(0, 2, size=(R, d)).astype(np.uint8) << 7)
+    cx[:, 0] = 0x7E
+    sx = 2.0 ** rng.integers(-9, -6, size=R)
+    x = torch.from_numpy(oracle.e4m3_decode(cx) * sx[:, None]).to(torch.bfloat16)
+    Ws = []
+    for _ in range(2):
+        c = rng.integers(0, 0x7E, size=(f, d)).astype(np.uint8) | \
+            (rng.integers(0, 2, size=(f, d)).astype(np.uint8) << 7)
+        c[:, 3] = 0x7E
+        s = 2.0 ** rng.integers(-12, -9, size=f)
+        Ws.append(torch.from_numpy((oracle.e4m3_decode(c) * s[:, None]).T.copy()).to(torch.bfloat16))
+    Wd = (torch.randn(f, d, generator=torch.Generator().manual_seed(2)) * 0.1).to(torch.bfloat16)
+    ref = oracle.expert_rows(Ws[0], Ws[1], Wd, x)
+    qx, sxq = oracle.quantize_rows_e4m3(x)
+    qw = [oracle.quantize_weights_e4m3(W[None]) for W in Ws]
+    got = oracle.expert_rows_fp8(qw[0][0][0], qw[0][1][0], qw[1][0][0], qw[1][1][0], Wd, qx, sxq)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
