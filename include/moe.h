@@ -205,6 +205,41 @@ moe_status_t moe_expert_ffn(const void *x_perm, const int32_t *offsets,
                             size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * Low-precision expert weights: FP8 E4M3 with absmax scales.
+ * Source: "大模型MoE混合专家架构原理与DeepSeek-V4工程实践解析", section
+ * MoE模型推理部署与显存优化实战 (decoding is bound by the bytes of weights
+ * read; storing them in fewer bits is the remedy); "MoE稀疏激活原理与工程实践",
+ * 4.3.  Format: OCP E4M3 (largest finite 448).  A vector v is stored as
+ * E4M3(v * (448 / amax|v|)) (nearest even, saturating) and the fp32 scale
+ * amax / 448 (an all-zero vector: scale 1).
+ *
+ * moe_quantize_weights_e4m3: gate or up weights W [N,d,f] bf16, one scale per
+ *   output channel (a column over d): Wq [N,f,d] codes (channel-major, so the
+ *   GEMM reads it K-major), scale [N,f].  d % 16 == 0.  An offline step.
+ * moe_quantize_rows_e4m3: rows x [R,C] bf16, one scale per row: q [R,C],
+ *   scale [R].  C % 16 == 0.
+ * moe_expert_ffn_fp8: moe_expert_ffn with E4M3 gate/up: xq_perm [A_max,d]
+ *   codes of the permuted token rows (moe_permute on the quantised rows),
+ *   row p's scale = x_scale[perm_token[p]] (x_scale [T] per token);
+ *   g = (xq . Wq_gate[e][j]) * x_scale * wscale_gate[e][j], u likewise,
+ *   h = SiLU(g) * u rounded to bf16, y_perm = row_scale * (h W_down) as in
+ *   moe_expert_ffn.  Workspace: moe_expert_ffn_workspace_size(.., MOE_BF16).
+ * ------------------------------------------------------------------------- */
+moe_status_t moe_quantize_weights_e4m3(const void *W, int N, int d, int f,
+                                       uint8_t *Wq, float *scale, void *stream);
+moe_status_t moe_quantize_rows_e4m3(const void *x, int R, int C, uint8_t *q,
+                                    float *scale, void *stream);
+moe_status_t moe_expert_ffn_fp8(const uint8_t *xq_perm, const float *x_scale,
+                                const int32_t *perm_token,
+                                const int32_t *offsets, const float *row_scale,
+                                int A_max, int d, int f, int N,
+                                const uint8_t *Wq_gate, const float *wscale_gate,
+                                const uint8_t *Wq_up, const float *wscale_up,
+                                const void *W_down, void *y_perm,
+                                int32_t *device_status, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
  * Step 6: combine.  y[t] = sum_{j<k, inv_pos[t,j] >= 0} y_perm[inv_pos[t,j]]
  *                          (+ shared_y[t]), summed in fp32 in that order.
  *   y_perm [*,d] and shared_y [T,d] (NULL = none) in y_perm_dtype;
@@ -248,6 +283,14 @@ typedef struct moe_forward_args {
                                  moe_permute_reroute; topk_idx/topk_w then
                                  hold the final selection (-1 = dropped)     */
   int32_t *rerouted;          /* scalar optional output: slots re-routed     */
+  /* FP8 gate/up (optional, bf16 layers): when set, the routed experts'
+   * gate/up projections run in E4M3 from these (W_gate/W_up may be NULL);
+   * x is quantised per token row on the fly; W_down stays bf16.  See
+   * moe_quantize_weights_e4m3.                                             */
+  const uint8_t *Wq_gate;     /* [N,f,d] E4M3 codes                          */
+  const float *wscale_gate;   /* [N,f] channel scales                        */
+  const uint8_t *Wq_up;       /* [N,f,d]                                     */
+  const float *wscale_up;     /* [N,f]                                       */
 } moe_forward_args;
 
 size_t moe_forward_workspace_size(const moe_forward_args *args);

@@ -47,7 +47,7 @@ def _load(path=None):
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_long, f32p, vp]
         lib.oracle_e4m3_encode.restype = None
         lib.oracle_quantize_rows_e4m3.argtypes = [ci, ci, ci, vp, vp, f32p]
-        lib.oracle_quantize_weights_e4m3.argtypes = [ci, ci, ci, ci, vp, vp, f32p]
+        lib.oracle_quantize_weights_e4m3.argtypes = [ci, ci, ci, ci, vp, vp, f32p, ci]
         lib.oracle_moe_forward.argtypes = (
             [ci] * 6 + [vp, vp, f32p, vp, vp, vp, ci, vp, vp, vp, cd, f64p, f64p,
                         i32p, f64p, i32p, i32p, i32p, i32p, ci])
@@ -379,7 +379,7 @@ def quantize_rows_e4m3(x):
     return q, sc
 
 
-def quantize_weights_e4m3(W):
+def quantize_weights_e4m3(W, nthreads=None):
     """Per-output-channel absmax E4M3 of gate/up weights W [N,d,f]:
     (codes uint8 [N,f,d], scales float32 [N,f])."""
     b = _Buf(W)
@@ -388,7 +388,8 @@ def quantize_weights_e4m3(W):
     q = np.empty((N, f, d), dtype=np.uint8)
     sc = np.empty((N, f), dtype=np.float32)
     _check(_load().oracle_quantize_weights_e4m3(N, d, f, b.dtype, b.ptr, q.ctypes.data,
-                                                sc.ctypes.data), "oracle_quantize_weights_e4m3")
+                                                sc.ctypes.data, nthreads or default_threads()),
+           "oracle_quantize_weights_e4m3")
     return q, sc
 
 
@@ -410,11 +411,12 @@ def expert_rows_fp8(qg_e, sg_e, qu_e, su_e, W_down_e, xq_rows, sx_rows, nthreads
 
 
 def forward_rows_fp8(xq_rows, sx_rows, topk_idx_rows, topk_w_rows, inv_pos_rows,
-                     fetch_expert_fp8, nthreads=None):
+                     fetch_expert_fp8, shared=None, x_rows=None, nthreads=None):
     """Layer output for a subset of tokens with E4M3 gate/up weights and token
     rows: fetch_expert_fp8(e) -> (qg [f,d], sg [f], qu [f,d], su [f], W_down [f,d]).
-    Experts one at a time (each dequantised expert is held in fp64).
-    Returns y [R,d] fp64."""
+    Experts one at a time (each dequantised expert is held in fp64).  The
+    shared expert (Ws_gate, Ws_up, Ws_down), when given, runs in the layer's
+    own precision on x_rows.  Returns y [R,d] fp64."""
     idx = _i32(topk_idx_rows)
     inv = _i32(inv_pos_rows)
     R, k = idx.shape
@@ -425,4 +427,7 @@ def forward_rows_fp8(xq_rows, sx_rows, topk_idx_rows, topk_w_rows, inv_pos_rows,
         qg, sg, qu, su, wd = fetch_expert_fp8(e)
         out[rows, slots] = expert_rows_fp8(qg, sg, qu, su, wd, xq_rows[rows], sx_rows[rows],
                                            nthreads)
-    return combine_rows(inv, topk_w_rows, out)
+    sh = None
+    if shared is not None:
+        sh = expert_rows(shared[0], shared[1], shared[2], x_rows, nthreads)
+    return combine_rows(inv, topk_w_rows, out, sh)

@@ -603,23 +603,26 @@ static double e4m3_value(uint8_t c) {
 }
 
 /* Nearest finite E4M3 code to v (|v| > 448 -> +-448), ties to the code with
- * an even mantissa; found by comparing v against every finite magnitude. */
+ * an even mantissa.  The finite non-negative codes 0x00..0x7E have increasing
+ * values, so a bisection finds the last code whose value is <= |v|; the
+ * answer is that code or the next one, whichever is nearer. */
 static uint8_t e4m3_encode(float vf) {
   const double v = (double)vf;
   const uint8_t sign = (v < 0.0 || (v == 0.0 && signbit(v))) ? 0x80 : 0;
   const double a = fabs(v);
   if (isnan(v)) return (uint8_t)(sign | 0x7F);
-  if (isinf(v)) return (uint8_t)(sign | 0x7E);
-  uint8_t best = 0;
-  double best_err = INFINITY;
-  for (int c = 0; c <= 0x7E; ++c) {          /* finite non-negative codes */
-    const double err = fabs(e4m3_value((uint8_t)c) - a);
-    if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
-      best = (uint8_t)c;
-      best_err = err;
-    }
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+  int lo = 0, hi = 0x7E;                       /* value(lo) <= a < value(hi) */
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) / 2;
+    if (e4m3_value((uint8_t)mid) <= a) lo = mid; else hi = mid;
   }
-  return (uint8_t)(sign | best);
+  const double dlo = a - e4m3_value((uint8_t)lo), dhi = e4m3_value((uint8_t)hi) - a;
+  int c;
+  if (dlo < dhi) c = lo;
+  else if (dhi < dlo) c = hi;
+  else c = (lo & 1) == 0 ? lo : hi;            /* tie: even mantissa */
+  return (uint8_t)(sign | c);
 }
 
 void oracle_e4m3_decode(long n, const uint8_t *codes, double *out) {
@@ -658,13 +661,27 @@ int oracle_quantize_rows_e4m3(int R, int C, int dtype, const void *x, uint8_t *q
 
 /* Gate/up weights W [N, d, f] per output channel j (a column over d):
  * codes [N, f, d] (channel-major: each channel's d codes contiguous),
- * scales [N, f]. */
+ * scales [N, f].  Channels are independent; they are split over threads. */
+typedef struct {
+  int d, f, dtype;
+  const void *W;
+  uint8_t *q;
+  float *scale;
+} qw_ctx;
+
+static void quantize_channels(long lo, long hi, void *p) {
+  qw_ctx *c = (qw_ctx *)p;
+  for (long ch = lo; ch < hi; ++ch) {
+    const long e = ch / c->f, j = ch % c->f;
+    quantize_vector(c->W, c->dtype, (size_t)e * c->d * c->f + j, (size_t)c->f, c->d,
+                    c->q + (size_t)ch * c->d, 1, c->scale + ch);
+  }
+}
+
 int oracle_quantize_weights_e4m3(int N, int d, int f, int dtype, const void *W, uint8_t *q,
-                                 float *scale) {
+                                 float *scale, int nthreads) {
   if (N < 1 || d < 1 || f < 1 || !W || !q || !scale) return 1;
-  for (int e = 0; e < N; ++e)
-    for (int j = 0; j < f; ++j)
-      quantize_vector(W, dtype, (size_t)e * d * f + j, (size_t)f, d,
-                      q + ((size_t)e * f + j) * d, 1, scale + (size_t)e * f + j);
+  qw_ctx c = {d, f, dtype, W, q, scale};
+  parallel_for((long)N * f, nthreads, quantize_channels, &c);
   return 0;
 }

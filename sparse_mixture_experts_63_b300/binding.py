@@ -27,7 +27,8 @@ EXPORTS = ("moe_status_string", "moe_last_error", "moe_version", "moe_launch_cou
            "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
            "moe_forward_workspace_size", "moe_forward", "moe_forward_host_io",
            "moe_routing_stats_workspace_size", "moe_routing_stats",
-           "moe_permute_reroute_workspace_size", "moe_permute_reroute")
+           "moe_permute_reroute_workspace_size", "moe_permute_reroute",
+           "moe_quantize_weights_e4m3", "moe_quantize_rows_e4m3", "moe_expert_ffn_fp8")
 
 
 class MoEError(RuntimeError):
@@ -50,7 +51,9 @@ class moe_forward_args(ctypes.Structure):
                 ("counts", ctypes.c_void_p), ("offsets", ctypes.c_void_p),
                 ("inv_pos", ctypes.c_void_p), ("dropped", ctypes.c_void_p),
                 ("device_status", ctypes.c_void_p), ("reroute_rounds", ctypes.c_int),
-                ("rerouted", ctypes.c_void_p)]
+                ("rerouted", ctypes.c_void_p), ("Wq_gate", ctypes.c_void_p),
+                ("wscale_gate", ctypes.c_void_p), ("Wq_up", ctypes.c_void_p),
+                ("wscale_up", ctypes.c_void_p)]
 
 
 _lib = None
@@ -95,7 +98,12 @@ def lib():
         L.moe_permute_reroute_workspace_size.restype = sz
         L.moe_permute_reroute.argtypes = ([vp, vp, vp, ci, ci, ci, ci, ci, ci, ci] + [vp] * 13 +
                                           [sz, vp])
+        L.moe_quantize_weights_e4m3.argtypes = [vp, ci, ci, ci, vp, vp, vp]
+        L.moe_quantize_rows_e4m3.argtypes = [vp, ci, ci, vp, vp, vp]
+        L.moe_expert_ffn_fp8.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, vp, vp, vp, vp, vp,
+                                         vp, vp, vp, sz, vp]
         for n in ("moe_router_topk", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn",
+                  "moe_quantize_weights_e4m3", "moe_quantize_rows_e4m3", "moe_expert_ffn_fp8",
                   "moe_combine", "moe_routing_stats", "moe_permute_reroute",
                   "moe_forward", "moe_forward_host_io"):
             getattr(L, n).restype = ci
@@ -231,6 +239,50 @@ def moe_expert_ffn(x_perm, offsets, W_gate, W_up, W_down, row_scale=None, y_perm
     return y_perm
 
 
+def quantize_weights_e4m3(W, stream=None):
+    """Gate or up weights W [N,d,f] bf16 -> (codes uint8 [N,f,d], scales fp32 [N,f]),
+    E4M3 with one absmax scale per output channel."""
+    _cuda(W)
+    N, d, f = W.shape
+    q = torch.empty((N, f, d), dtype=torch.uint8, device=W.device)
+    sc = torch.empty((N, f), dtype=torch.float32, device=W.device)
+    _check("moe_quantize_weights_e4m3", lib().moe_quantize_weights_e4m3(
+        _p(W), N, d, f, _p(q), _p(sc), _stream(stream)))
+    return q, sc
+
+
+def quantize_rows_e4m3(x, stream=None):
+    """Rows x [R,C] bf16 -> (codes uint8 [R,C], scales fp32 [R]), E4M3 per row."""
+    _cuda(x)
+    R, C = x.shape
+    q = torch.empty((R, C), dtype=torch.uint8, device=x.device)
+    sc = torch.empty(max(R, 1), dtype=torch.float32, device=x.device)
+    _check("moe_quantize_rows_e4m3", lib().moe_quantize_rows_e4m3(
+        _p(x), R, C, _p(q), _p(sc), _stream(stream)))
+    return q, sc[:R]
+
+
+def moe_expert_ffn_fp8(xq_perm, x_scale, perm_token, offsets, Wq_gate, wscale_gate, Wq_up,
+                       wscale_up, W_down, row_scale=None, y_perm=None, device_status=None,
+                       stream=None, A_max=None):
+    """moe_expert_ffn with E4M3 gate/up (codes [N,f,d] + channel scales [N,f]) on
+    E4M3 permuted token rows xq_perm [A_max,d] (row p's scale x_scale[perm_token[p]])."""
+    _cuda(xq_perm, x_scale, perm_token, offsets, Wq_gate, wscale_gate, Wq_up, wscale_up, W_down,
+          row_scale, y_perm)
+    A = xq_perm.shape[0] if A_max is None else A_max
+    d = xq_perm.shape[1]
+    N, f, _ = Wq_gate.shape
+    if y_perm is None:
+        y_perm = torch.empty((max(A, 1), d), dtype=W_down.dtype, device=xq_perm.device)
+    ws_bytes = lib().moe_expert_ffn_workspace_size(A, d, f, N, MOE_BF16)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=xq_perm.device)
+    _check("moe_expert_ffn_fp8", lib().moe_expert_ffn_fp8(
+        _p(xq_perm), _p(x_scale), _p(perm_token), _p(offsets), _p(row_scale), A, d, f, N,
+        _p(Wq_gate), _p(wscale_gate), _p(Wq_up), _p(wscale_up), _p(W_down), _p(y_perm),
+        _p(device_status), _p(ws), ws_bytes, _stream(stream)))
+    return y_perm
+
+
 class moe_routing_stats_t(ctypes.Structure):
     _fields_ = [("entropy_bits", ctypes.c_float), ("entropy_max_bits", ctypes.c_float),
                 ("top3_share", ctypes.c_float), ("max_share", ctypes.c_float),
@@ -318,7 +370,7 @@ def moe_combine(y_perm, inv_pos, shared_y=None, y=None, y_dtype=torch.float32, s
 
 def make_forward_args(x, W_g, W_gate, W_up, W_down, k, y, bias=None, Ws_gate=None,
                       Ws_up=None, Ws_down=None, capacity_factor=0.0, outputs=None,
-                      device_status=None, reroute_rounds=0):
+                      device_status=None, reroute_rounds=0, fp8_gate_up=None):
     _cuda(x, W_g, W_gate, W_up, W_down, y, bias, Ws_gate, Ws_up, Ws_down)
     T, d = x.shape
     N, _, f = W_gate.shape
@@ -336,6 +388,9 @@ def make_forward_args(x, W_g, W_gate, W_up, W_down, k, y, bias=None, Ws_gate=Non
     a.device_status = _p(device_status)
     a.reroute_rounds = int(reroute_rounds)
     a.rerouted = _p(o.get("rerouted"))
+    if fp8_gate_up is not None:   # (Wq_gate, wscale_gate, Wq_up, wscale_up)
+        _cuda(*fp8_gate_up)
+        a.Wq_gate, a.wscale_gate, a.Wq_up, a.wscale_up = (_p(t) for t in fp8_gate_up)
     return a
 
 
@@ -363,12 +418,20 @@ class MoELayer:
     """Convenience holder: the layer's weights plus a reusable workspace.
 
     ``layer(x)`` returns y [T,d] (fp32 by default) and keeps the routing
-    outputs of the last call in ``layer.last``.
+    outputs of the last call in ``layer.last``.  ``fp8=True`` quantises the
+    routed experts' gate/up weights to E4M3 once (per-channel scales) and runs
+    those projections in FP8 (x quantised per token on the fly).
     """
 
     def __init__(self, W_g, W_gate, W_up, W_down, k, bias=None, Ws_gate=None, Ws_up=None,
-                 Ws_down=None, capacity_factor=0.0, y_dtype=torch.float32, reroute_rounds=0):
+                 Ws_down=None, capacity_factor=0.0, y_dtype=torch.float32, reroute_rounds=0,
+                 fp8=False):
         self.reroute_rounds = reroute_rounds
+        self.fp8 = None
+        if fp8:
+            qg, sg = quantize_weights_e4m3(W_gate)
+            qu, su = quantize_weights_e4m3(W_up)
+            self.fp8 = (qg, sg, qu, su)
         self.W_g, self.W_gate, self.W_up, self.W_down = W_g, W_gate, W_up, W_down
         self.k, self.bias, self.cf, self.y_dtype = k, bias, capacity_factor, y_dtype
         self.Ws_gate, self.Ws_up, self.Ws_down = Ws_gate, Ws_up, Ws_down
@@ -395,7 +458,7 @@ class MoELayer:
                                  bias=self.bias, Ws_gate=self.Ws_gate, Ws_up=self.Ws_up,
                                  Ws_down=self.Ws_down, capacity_factor=self.cf,
                                  outputs=outputs, device_status=outputs.get("device_status"),
-                                 reroute_rounds=self.reroute_rounds)
+                                 reroute_rounds=self.reroute_rounds, fp8_gate_up=self.fp8)
 
     def workspace(self, args, device):
         n = moe_forward_workspace_size(args)

@@ -115,6 +115,12 @@ struct TcParams {
   int wide;                // 1: tiles over 256 rows run as two sub-tiles
   int stages;              // pipeline stages (kStageRegion / stage_bytes)
   int stage_bytes;         // kABytes + token rows of a stage (both sub-tiles)
+  // FP8 gate/up (E4M3 weights and token rows, K-major): D is multiplied by
+  // the output channel's scale and the token's scale before SwiGLU
+  const float *wscale_g;   // [N, f] gate channel scales
+  const float *wscale_u;   // [N, f] up channel scales
+  const float *xscale;     // [T] token scales
+  const int32_t *perm_token;  // [A] token of each permuted row
 };
 
 // Token sub-tiles of a tile: rows [row0, row0 + rows0) and, for a wide tile
@@ -306,6 +312,21 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams &p, const TileInfo
   }
 }
 
+// FP8 GEMM1: D of a 32-column chunk (permuted rows row0 .. row0 + 31, of
+// which `valid` hold rows) times this thread's channel scale and each
+// column's token scale.
+__device__ __forceinline__ void scale_chunk(const TcParams &p, int row0, int valid, int lane,
+                                            float wsc, uint32_t (&r)[32]) {
+  const float sxl = lane < valid ? p.xscale[p.perm_token[row0 + lane]] : 0.f;
+#pragma unroll
+  for (int c = 0; c < 32; ++c)
+    r[c] = __float_as_uint(__uint_as_float(r[c]) * (wsc * __shfl_sync(0xffffffffu, sxl, c)));
+}
+
+// FP8: GEMM1 with E4M3 weights [N, f, d] and token rows, both K-major, 128 K
+// per stage (the same 128-byte rows as 64 bf16), kind::f8f6f4 MMAs, and the
+// channel x token scales applied to D before SwiGLU.
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
@@ -362,7 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = prefix[p.N];
-  const int kblocks = (p.K + kBK - 1) / kBK;
+  constexpr int kKStage = FP8 ? 128 : kBK;        // K elements per stage (128 B rows)
+  const int kblocks = (p.K + kKStage - 1) / kKStage;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
@@ -401,10 +423,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           unsigned char *st = stage0 + s * p.stage_bytes;
           if (rank == 0) tc::mbar_arrive_expect_tx(&full[s], tx);
           const uint32_t fb = full_leader0 + 8u * s;
-          tc::tma_load_3d_pair(st, &tmA0, fb, m0, kb * kBK, ti.e, pol_w);
-          tc::tma_load_3d_pair(st + kAChunkBytes, &tmA1, fb, m1, kb * kBK, ti.e, pol_w);
-          tc::tma_load_2d_pair(st + kABytes, tb0, fb, kb * kBK, brow0, pol_x);
-          if (n1) tc::tma_load_2d_pair(st + kABytes + kSubBytes, tb1, fb, kb * kBK, brow1, pol_x);
+          const int kc = kb * kKStage;
+          if (FP8) {   // K-major weights W[N][M][K]: coordinates (k, m, e)
+            tc::tma_load_3d_pair(st, &tmA0, fb, kc, m0, ti.e, pol_w);
+            tc::tma_load_3d_pair(st + kAChunkBytes, &tmA1, fb, kc, m1, ti.e, pol_w);
+          } else {     // MN-major weights W[N][K][M]: coordinates (m, k, e)
+            tc::tma_load_3d_pair(st, &tmA0, fb, m0, kc, ti.e, pol_w);
+            tc::tma_load_3d_pair(st + kAChunkBytes, &tmA1, fb, m1, kc, ti.e, pol_w);
+          }
+          tc::tma_load_2d_pair(st + kABytes, tb0, fb, kc, brow0, pol_x);
+          if (n1) tc::tma_load_2d_pair(st + kABytes + kSubBytes, tb1, fb, kc, brow1, pol_x);
           ++issued;
           if (++s == p.stages) { s = 0; ph ^= 1; }
         }
@@ -429,7 +457,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (rank == 0 && lane == 0) {
       const uint32_t stage0 = tc::smem_u32(smem + Smem::stages);
       // descriptors of stage 0; stage s adds (s * stage_bytes) >> 4 to the start field
-      const uint64_t a_desc0 = tc::sdesc_sw128(stage0, kAChunkBytes, 1024);   // MN-major A
+      // A MN-major (bf16) or K-major (FP8: 128 rows of 128 B, 8-row atoms)
+      const uint64_t a_desc0 = FP8 ? tc::sdesc_sw128(stage0, 16, 1024)
+                                   : tc::sdesc_sw128(stage0, kAChunkBytes, 1024);
       const uint64_t b_desc0 = tc::sdesc_sw128(stage0 + kABytes, 16, 1024);   // K-major B
       int s = 0;
       uint32_t ph = 0;
@@ -441,8 +471,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TileInfo ti = decode_tile(p, prefix, t);
         const bool two = ti.rows1 > 0;
         const int n0 = mma_n(ti.rows0), n1 = two ? mma_n(ti.rows1) : 0;
-        const uint32_t idesc0 = tc::idesc_bf16(2 * kBM, n0, /*a_mn=*/1, /*b_mn=*/0);
-        const uint32_t idesc1 = two ? tc::idesc_bf16(2 * kBM, n1, 1, 0) : 0u;
+        const uint32_t idesc0 = FP8 ? tc::idesc_e4m3(2 * kBM, n0)
+                                    : tc::idesc_bf16(2 * kBM, n0, /*a_mn=*/1, /*b_mn=*/0);
+        const uint32_t idesc1 = !two ? 0u
+                                : FP8 ? tc::idesc_e4m3(2 * kBM, n1)
+                                      : tc::idesc_bf16(2 * kBM, n1, 1, 0);
         const int c0 = ring_take(pos, n0);
         const int c1 = two ? ring_take(pos, n1) : c0;
         // every chunk of the sub-tiles must have been loaded by the epilogue
@@ -472,18 +505,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tc_fence_after();
           const uint64_t off = (uint64_t)((s * p.stage_bytes) >> 4);
           const uint64_t ad = a_desc0 + off, bd = b_desc0 + off;
-          // A MN-major: 16 k-rows = two 1024-B atoms further (+128 in 16-B units);
-          // B K-major: 16 k = 32 B further inside the 128-B swizzled row (+2).
-          tc::mma_f16_pair(d0, ad, bd, idesc0, kb > 0 ? 1u : 0u);
-          tc::mma_f16_pair(d0, ad + 128, bd + 2, idesc0, 1u);
-          tc::mma_f16_pair(d0, ad + 256, bd + 4, idesc0, 1u);
-          tc::mma_f16_pair(d0, ad + 384, bd + 6, idesc0, 1u);
-          if (two) {
-            const uint64_t bd1 = bd + (kSubBytes >> 4);   // second sub-tile's token rows
-            tc::mma_f16_pair(d1, ad, bd1, idesc1, kb > 0 ? 1u : 0u);
-            tc::mma_f16_pair(d1, ad + 128, bd1 + 2, idesc1, 1u);
-            tc::mma_f16_pair(d1, ad + 256, bd1 + 4, idesc1, 1u);
-            tc::mma_f16_pair(d1, ad + 384, bd1 + 6, idesc1, 1u);
+          if (FP8) {
+            // both K-major: 32 k of 8 bits = 32 B further inside the 128-B rows (+2)
+            tc::mma_f8_pair(d0, ad, bd, idesc0, kb > 0 ? 1u : 0u);
+            tc::mma_f8_pair(d0, ad + 2, bd + 2, idesc0, 1u);
+            tc::mma_f8_pair(d0, ad + 4, bd + 4, idesc0, 1u);
+            tc::mma_f8_pair(d0, ad + 6, bd + 6, idesc0, 1u);
+            if (two) {
+              const uint64_t bd1 = bd + (kSubBytes >> 4);
+              tc::mma_f8_pair(d1, ad, bd1, idesc1, kb > 0 ? 1u : 0u);
+              tc::mma_f8_pair(d1, ad + 2, bd1 + 2, idesc1, 1u);
+              tc::mma_f8_pair(d1, ad + 4, bd1 + 4, idesc1, 1u);
+              tc::mma_f8_pair(d1, ad + 6, bd1 + 6, idesc1, 1u);
+            }
+          } else {
+            // A MN-major: 16 k-rows = two 1024-B atoms further (+128 in 16-B units);
+            // B K-major: 16 k = 32 B further inside the 128-B swizzled row (+2).
+            tc::mma_f16_pair(d0, ad, bd, idesc0, kb > 0 ? 1u : 0u);
+            tc::mma_f16_pair(d0, ad + 128, bd + 2, idesc0, 1u);
+            tc::mma_f16_pair(d0, ad + 256, bd + 4, idesc0, 1u);
+            tc::mma_f16_pair(d0, ad + 384, bd + 6, idesc0, 1u);
+            if (two) {
+              const uint64_t bd1 = bd + (kSubBytes >> 4);   // second sub-tile's token rows
+              tc::mma_f16_pair(d1, ad, bd1, idesc1, kb > 0 ? 1u : 0u);
+              tc::mma_f16_pair(d1, ad + 128, bd1 + 2, idesc1, 1u);
+              tc::mma_f16_pair(d1, ad + 256, bd1 + 4, idesc1, 1u);
+              tc::mma_f16_pair(d1, ad + 384, bd1 + 6, idesc1, 1u);
+            }
           }
           tc::mma_commit_pair(&empty[s], 0x3);  // frees the stage in both CTAs
           if (++s == p.stages) { s = 0; ph ^= 1; }
@@ -513,6 +561,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = cid; t < total_tiles && go_on; t += ncl) {
       const TileInfo ti = decode_tile(p, prefix, t);
       const int nsub = ti.rows1 > 0 ? 2 : 1;
+      float wsc = 1.f;   // FP8: this thread's output channel scale (gate or up)
+      if (FP8) {
+        const int fch = ti.pair * 128 + (int)rank * 64 + (lane_grp & 1) * 32 + lane;
+        const float *ws = lane_grp < 2 ? p.wscale_g : p.wscale_u;
+        wsc = fch < p.M ? ws[(size_t)ti.e * p.M + fch] : 0.f;
+      }
       for (int sub = 0; sub < nsub; ++sub) {
         const int srow0 = ti.row0 + (sub ? ti.rows0 : 0);   // first permuted row of the sub-tile
         const int srows = sub ? ti.rows1 : ti.rows0;
@@ -556,6 +610,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             tc::mbar_arrive_cluster_relaxed(tc::mapa_shared(&col_free[c0 + c2], 0));
             if (pair) tc::mbar_arrive_cluster_relaxed(tc::mapa_shared(&col_free[c0 + c2 + 1], 0));
+          }
+          if (FP8) {
+            scale_chunk(p, srow0 + c2 * 32, srows - c2 * 32, lane, wsc, ra);
+            if (pair) scale_chunk(p, srow0 + (c2 + 1) * 32, srows - (c2 + 1) * 32, lane, wsc, rb);
           }
           epilogue_chunk(p, ti, rank, lane_grp, lane, etid, xbuf, obuf, obi, srow0, srows, c2, ra);
           if (pair)
@@ -606,6 +664,30 @@ bool make_weight_map(CUtensorMap *m, const void *W, int N, int K, int M) {
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// FP8 weights Wq[N][M][K] (K contiguous, E4M3 bytes), box 128(K) x 64(M) x 1.
+bool make_weight_map_k8(CUtensorMap *m, const void *Wq, int N, int M, int K) {
+  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)M, (cuuint64_t)N};
+  cuuint64_t strides[2] = {(cuuint64_t)K, (cuuint64_t)M * K};
+  cuuint32_t box[3] = {128, 64, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(Wq), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// FP8 token rows Xq[rows][K] (E4M3 bytes), box 128(K) x box_rows.
+bool make_rows_map_u8(CUtensorMap *m, const void *Xq, int rows, int K, int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K};
+  cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(Xq), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Token rows X[rows][K] (K contiguous), box 64(K) x box_rows.
 bool make_rows_map(CUtensorMap *m, const void *X, int rows, int K, int box_rows) {
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
@@ -646,7 +728,8 @@ int max_pairs() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int c = 0;
-  if (cudaOccupancyMaxActiveClusters(&c, grouped_gemm_tc, &cfg) != cudaSuccess || c <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&c, grouped_gemm_tc<false>, &cfg) != cudaSuccess ||
+      c <= 0) {
     cudaGetLastError();
     c = sms / 2;
   }
@@ -655,14 +738,15 @@ int max_pairs() {
   return n;
 }
 
+template <bool FP8>
 moe_status_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap *b,
                          const TcParams &p, cudaStream_t stream) {
   static bool attr_set[kMaxDevicesCached] = {};
   const int dev = current_device();
   if (dev >= kMaxDevicesCached || !attr_set[dev]) {
-    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc,
+    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc<FP8>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
-    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc,
+    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc<FP8>,
                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 0));
     if (dev < kMaxDevicesCached) attr_set[dev] = true;
   }
@@ -678,9 +762,66 @@ moe_status_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUt
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, grouped_gemm_tc, a0, a1, b[0], b[1], b[2], b[3], p));
+  MOE_CUDA_TRY(
+      cudaLaunchKernelEx(&cfg, grouped_gemm_tc<FP8>, a0, a1, b[0], b[1], b[2], b[3], p));
   MOE_LAUNCH_CHECK();
   return MOE_OK;
+}
+
+}  // namespace
+
+namespace {
+
+struct TileCfg {
+  int tile_cap, wide, stages, stage_bytes;
+};
+
+// Token tile width: the expected largest expert (1.25x the average rows, or
+// the capacity when that is smaller) rounded up to 64/128/256, so narrow
+// layers fit more, smaller stages.  Layers whose experts run ~250-320 rows
+// (many experts just over 256) take wide tiles instead, which keep such an
+// expert in one tile.
+TileCfg tile_config(int A_max, int N, int capacity) {
+  const long avg_rows = ((long)A_max + N - 1) / N;
+  long exp_rows = avg_rows + avg_rows / 4;
+  if (capacity > 0 && capacity < exp_rows) exp_rows = capacity;
+  TileCfg c;
+  c.wide = (exp_rows > 256 && avg_rows <= 320) ? 1 : 0;
+  c.tile_cap = c.wide ? kWideTile : exp_rows > 128 ? 256 : exp_rows > 64 ? 128 : 64;
+  c.stage_bytes = c.wide ? kABytes + 2 * kSubBytes : kABytes + (c.tile_cap / 2) * kBK * 2;
+  c.stages = kStageRegion / c.stage_bytes;
+  if (c.stages > kMaxStages) c.stages = kMaxStages;
+  return c;
+}
+
+moe_status_t check_ffn_launch(int N) {
+  if (!encode_fn()) {
+    set_error("cuTensorMapEncodeTiled unavailable from the driver");
+    return MOE_ERR_CUDA;
+  }
+  if (N > kMaxExperts) {
+    set_error("tensor-core FFN supports N <= %d experts", kMaxExperts);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+// GEMM2 (down projection + gate scale) of either form: h [A_max, f] bf16.
+moe_status_t launch_down(const int32_t *offsets, const float *row_scale, int A_max, int d,
+                         int f, int N, const TileCfg &tc_, const void *W_down, void *h,
+                         void *y_perm, int32_t *device_status, cudaStream_t stream) {
+  CUtensorMap wd, bh[kNumBoxes];
+  bool ok = make_weight_map(&wd, W_down, N, f, d);
+  const int box_rows[kNumBoxes] = {32, 64, 80, 128};
+  for (int i = 0; i < kNumBoxes; ++i) ok = ok && make_rows_map(&bh[i], h, A_max, f, box_rows[i]);
+  if (!ok) {
+    set_error("tensor map encoding failed (alignment or size)");
+    return MOE_ERR_INVALID_ARG;
+  }
+  TcParams p2{offsets, N, f, d, (d + 255) / 256, 0, static_cast<__nv_bfloat16 *>(y_perm), d,
+              row_scale, device_status, raster_group(f), tc_.tile_cap, tc_.wide, tc_.stages,
+              tc_.stage_bytes};
+  return launch_gemm<false>(wd, wd, bh, p2, stream);
 }
 
 }  // namespace
@@ -691,46 +832,55 @@ moe_status_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, const flo
                            const void *W_up, const void *W_down, void *h, void *y_perm,
                            int32_t *device_status, cudaStream_t stream) {
   if (A_max == 0) return MOE_OK;
-  if (!encode_fn()) {
-    set_error("cuTensorMapEncodeTiled unavailable from the driver");
-    return MOE_ERR_CUDA;
-  }
-  if (N > kMaxExperts) {
-    set_error("tensor-core FFN supports N <= %d experts", kMaxExperts);
-    return MOE_ERR_UNSUPPORTED;
-  }
-  CUtensorMap wg, wu, wd, bx[kNumBoxes], bh[kNumBoxes];
-  bool ok = make_weight_map(&wg, W_gate, N, d, f) && make_weight_map(&wu, W_up, N, d, f) &&
-            make_weight_map(&wd, W_down, N, f, d);
+  moe_status_t s = check_ffn_launch(N);
+  if (s != MOE_OK) return s;
+  CUtensorMap wg, wu, bx[kNumBoxes];
+  bool ok = make_weight_map(&wg, W_gate, N, d, f) && make_weight_map(&wu, W_up, N, d, f);
   const int box_rows[kNumBoxes] = {32, 64, 80, 128};
-  for (int i = 0; i < kNumBoxes; ++i) {
-    ok = ok && make_rows_map(&bx[i], x_perm, A_max, d, box_rows[i]) &&
-         make_rows_map(&bh[i], h, A_max, f, box_rows[i]);
-  }
+  for (int i = 0; i < kNumBoxes; ++i)
+    ok = ok && make_rows_map(&bx[i], x_perm, A_max, d, box_rows[i]);
   if (!ok) {
     set_error("tensor map encoding failed (alignment or size)");
     return MOE_ERR_INVALID_ARG;
   }
-  // Token tile width: the expected largest expert (1.25x the average rows, or
-  // the capacity when that is smaller) rounded up to 64/128/256, so narrow
-  // layers fit more, smaller stages.  Layers whose experts run ~250-320 rows
-  // (many experts just over 256) take wide tiles instead, which keep such an
-  // expert in one tile.
-  const long avg_rows = ((long)A_max + N - 1) / N;
-  long exp_rows = avg_rows + avg_rows / 4;
-  if (capacity > 0 && capacity < exp_rows) exp_rows = capacity;
-  const int wide = (exp_rows > 256 && avg_rows <= 320) ? 1 : 0;
-  const int tile_cap = wide ? kWideTile : exp_rows > 128 ? 256 : exp_rows > 64 ? 128 : 64;
-  const int stage_bytes = wide ? kABytes + 2 * kSubBytes : kABytes + (tile_cap / 2) * kBK * 2;
-  int stages = kStageRegion / stage_bytes;
-  if (stages > kMaxStages) stages = kMaxStages;
+  const TileCfg c = tile_config(A_max, N, capacity);
   TcParams p1{offsets, N, d, f, (f + 127) / 128, 1, static_cast<__nv_bfloat16 *>(h), f, nullptr,
-              device_status, raster_group(d), tile_cap, wide, stages, stage_bytes};
-  moe_status_t s = launch_gemm(wg, wu, bx, p1, stream);
+              device_status, raster_group(d), c.tile_cap, c.wide, c.stages, c.stage_bytes};
+  s = launch_gemm<false>(wg, wu, bx, p1, stream);
   if (s != MOE_OK) return s;
-  TcParams p2{offsets, N, f, d, (d + 255) / 256, 0, static_cast<__nv_bfloat16 *>(y_perm), d,
-              row_scale, device_status, raster_group(f), tile_cap, wide, stages, stage_bytes};
-  return launch_gemm(wd, wd, bh, p2, stream);
+  return launch_down(offsets, row_scale, A_max, d, f, N, c, W_down, h, y_perm, device_status,
+                     stream);
+}
+
+// The same with E4M3 gate/up: xq_perm [A_max, d] E4M3 token rows (scale of
+// permuted row p: x_scale[perm_token[p]]), Wq_gate / Wq_up [N, f, d] E4M3
+// with channel scales [N, f]; h and the down projection stay bf16.
+moe_status_t launch_ffn_tc_fp8(const void *xq_perm, const float *x_scale,
+                               const int32_t *perm_token, const int32_t *offsets,
+                               const float *row_scale, int A_max, int d, int f, int N,
+                               int capacity, const void *Wq_gate, const float *sw_gate,
+                               const void *Wq_up, const float *sw_up, const void *W_down, void *h,
+                               void *y_perm, int32_t *device_status, cudaStream_t stream) {
+  if (A_max == 0) return MOE_OK;
+  moe_status_t s = check_ffn_launch(N);
+  if (s != MOE_OK) return s;
+  CUtensorMap wg, wu, bx[kNumBoxes];
+  bool ok = make_weight_map_k8(&wg, Wq_gate, N, f, d) && make_weight_map_k8(&wu, Wq_up, N, f, d);
+  const int box_rows[kNumBoxes] = {32, 64, 80, 128};
+  for (int i = 0; i < kNumBoxes; ++i)
+    ok = ok && make_rows_map_u8(&bx[i], xq_perm, A_max, d, box_rows[i]);
+  if (!ok) {
+    set_error("tensor map encoding failed (alignment or size)");
+    return MOE_ERR_INVALID_ARG;
+  }
+  const TileCfg c = tile_config(A_max, N, capacity);
+  TcParams p1{offsets, N, d, f, (f + 127) / 128, 1, static_cast<__nv_bfloat16 *>(h), f, nullptr,
+              device_status, raster_group(d), c.tile_cap, c.wide, c.stages, c.stage_bytes,
+              sw_gate, sw_up, x_scale, perm_token};
+  s = launch_gemm<true>(wg, wu, bx, p1, stream);
+  if (s != MOE_OK) return s;
+  return launch_down(offsets, row_scale, A_max, d, f, N, c, W_down, h, y_perm, device_status,
+                     stream);
 }
 
 }  // namespace moe

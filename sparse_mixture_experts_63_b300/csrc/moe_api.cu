@@ -90,6 +90,8 @@ struct ForwardLayout {
   int32_t *topk_idx, *counts, *offsets, *inv_pos, *perm_token, *dropped, *sh_offsets;
   float *topk_w, *row_scale;
   void *x_perm, *y_perm, *ffn_ws, *perm_ws, *ys, *sh_ffn_ws;
+  uint8_t *xq;       // [T, d] E4M3 token rows (FP8 gate/up only)
+  float *xs;         // [T] their scales
   int32_t *cand;     // [T, k+R] router candidates (re-routing only)
   float *cand_w;     // [T, k+R]
   void *rr_ws;       // re-routing workspace
@@ -111,7 +113,11 @@ ForwardLayout layout_forward(const moe_forward_args *a, void *ws) {
   L.dropped = a->dropped ? a->dropped : c.take<int32_t>(1);
   L.perm_token = c.take<int32_t>(tk);
   L.row_scale = c.take<float>(tk);
-  L.x_perm = c.take_bytes((size_t)A_max * a->d * es);
+  L.x_perm = c.take_bytes((size_t)A_max * a->d * es);   // E4M3 rows use the first half
+  if (a->Wq_gate) {
+    L.xq = static_cast<uint8_t *>(c.take_bytes((size_t)a->T * a->d));
+    L.xs = c.take<float>(a->T);
+  }
   L.y_perm = c.take_bytes((size_t)A_max * a->d * es);
   L.ffn_ws = c.take_bytes(ffn_workspace_bytes((int)A_max, a->d, a->f, a->N, a->dtype));
   L.perm_ws = c.take_bytes(permute_workspace_bytes(a->T, a->N, a->k));
@@ -283,6 +289,56 @@ moe_status_t moe_expert_ffn(const void *x_perm, const int32_t *offsets, const fl
                            static_cast<cudaStream_t>(stream));
 }
 
+moe_status_t moe_quantize_weights_e4m3(const void *W, int N, int d, int f, uint8_t *Wq,
+                                       float *scale, void *stream) {
+  CHECK_ARG(N >= 1 && d >= 16 && f >= 1 && d % 16 == 0, "bad sizes N=%d d=%d f=%d (d %% 16 == 0)",
+            N, d, f);
+  CHECK_ARG(W && Wq && scale, "required pointer is NULL");
+  CHECK_ARG(aligned16(Wq), "Wq must be 16-byte aligned");
+  moe_status_t s = check_device();
+  if (s != MOE_OK) return s;
+  return launch_quantize_weights_e4m3(W, N, d, f, Wq, scale, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_quantize_rows_e4m3(const void *x, int R, int C, uint8_t *q, float *scale,
+                                    void *stream) {
+  CHECK_ARG(R >= 0 && C >= 16 && C % 16 == 0, "bad sizes R=%d C=%d (C %% 16 == 0)", R, C);
+  CHECK_ARG(R == 0 || (x && q && scale), "required pointer is NULL");
+  CHECK_ARG(aligned16(x) && aligned16(q), "x and q must be 16-byte aligned");
+  moe_status_t s = check_device();
+  if (s != MOE_OK) return s;
+  return launch_quantize_rows_e4m3(x, R, C, q, scale, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_expert_ffn_fp8(const uint8_t *xq_perm, const float *x_scale,
+                                const int32_t *perm_token, const int32_t *offsets,
+                                const float *row_scale, int A_max, int d, int f, int N,
+                                const uint8_t *Wq_gate, const float *wscale_gate,
+                                const uint8_t *Wq_up, const float *wscale_up,
+                                const void *W_down, void *y_perm, int32_t *device_status,
+                                void *workspace, size_t workspace_bytes, void *stream) {
+  CHECK_ARG(A_max >= 0 && d >= 16 && f >= 8 && N >= 1, "bad sizes A_max=%d d=%d f=%d N=%d",
+            A_max, d, f, N);
+  CHECK_ARG(d % 16 == 0 && f % 8 == 0, "d=%d must be a multiple of 16 and f=%d of 8", d, f);
+  CHECK_ARG(offsets && Wq_gate && Wq_up && wscale_gate && wscale_up && W_down,
+            "required pointer is NULL");
+  CHECK_ARG(A_max == 0 || (xq_perm && x_scale && perm_token && y_perm),
+            "required pointer is NULL");
+  CHECK_ARG(aligned16(xq_perm) && aligned16(y_perm) && aligned16(Wq_gate) && aligned16(Wq_up) &&
+                aligned16(W_down),
+            "tensors must be 16-byte aligned");
+  size_t need = ffn_workspace_bytes(A_max, d, f, N, MOE_BF16);
+  if (need > 0 && (!workspace || workspace_bytes < need)) {
+    set_error("moe_expert_ffn_fp8: workspace %zu bytes, needs %zu", workspace_bytes, need);
+    return MOE_ERR_WORKSPACE;
+  }
+  moe_status_t s = check_device();
+  if (s != MOE_OK) return s;
+  return launch_ffn_tc_fp8(xq_perm, x_scale, perm_token, offsets, row_scale, A_max, d, f, N, 0,
+                           Wq_gate, wscale_gate, Wq_up, wscale_up, W_down, workspace, y_perm,
+                           device_status, static_cast<cudaStream_t>(stream));
+}
+
 size_t moe_permute_reroute_workspace_size(int T, int N, int k, int R) {
   if (T < 0 || N < 1 || k < 1 || R < 0) return 0;
   return reroute_workspace_bytes(T, N, k);
@@ -369,8 +425,16 @@ static moe_status_t validate_forward(const moe_forward_args *a) {
   CHECK_ARG(a->k >= 1 && a->k <= a->N, "k=%d must satisfy 1 <= k <= N=%d", a->k, a->N);
   CHECK_ARG(a->d % 8 == 0 && a->f % 8 == 0, "d=%d and f=%d must be multiples of 8", a->d, a->f);
   CHECK_ARG(a->fs >= 0 && a->fs % 8 == 0, "fs=%d must be a non-negative multiple of 8", a->fs);
-  CHECK_ARG(a->x && a->W_g && a->W_gate && a->W_up && a->W_down && a->y,
+  const bool fp8 = a->Wq_gate || a->Wq_up || a->wscale_gate || a->wscale_up;
+  CHECK_ARG(a->x && a->W_g && (fp8 || (a->W_gate && a->W_up)) && a->W_down && a->y,
             "required pointer is NULL");
+  if (fp8) {
+    CHECK_ARG(a->Wq_gate && a->Wq_up && a->wscale_gate && a->wscale_up,
+              "FP8 gate/up needs Wq_gate, Wq_up, wscale_gate and wscale_up");
+    CHECK_ARG(a->dtype == MOE_BF16, "FP8 gate/up needs a bf16 layer");
+    CHECK_ARG(a->d % 16 == 0, "FP8 gate/up needs d %% 16 == 0 (d=%d)", a->d);
+    CHECK_ARG(aligned16(a->Wq_gate) && aligned16(a->Wq_up), "tensors must be 16-byte aligned");
+  }
   CHECK_ARG(a->fs == 0 || (a->Ws_gate && a->Ws_up && a->Ws_down), "shared weights are NULL");
   CHECK_ARG(aligned16(a->x) && aligned16(a->y) && aligned16(a->W_gate) && aligned16(a->W_up) &&
                 aligned16(a->W_down) && aligned16(a->Ws_gate) && aligned16(a->Ws_up) &&
@@ -417,6 +481,12 @@ moe_status_t moe_forward(const moe_forward_args *a, void *workspace, size_t work
   ForwardLayout L = layout_forward(a, workspace);
   const int cap = moe_capacity(a->capacity_factor, a->T, a->k, a->N);
   const int A_max = (int)routed_rows_max(a->T, a->N, a->k, cap);
+  const bool fp8 = a->Wq_gate != nullptr;
+  void *x_perm = fp8 ? nullptr : L.x_perm;   // FP8: the quantised rows are copied later
+  if (fp8) {
+    s = launch_quantize_rows_e4m3(a->x, a->T, a->d, L.xq, L.xs, stream);
+    if (s != MOE_OK) return s;
+  }
 
   if (a->reroute_rounds > 0) {
     // the router ranks k+R candidates; the dispatch re-routes overflow to them
@@ -426,7 +496,7 @@ moe_status_t moe_forward(const moe_forward_args *a, void *workspace, size_t work
     if (s != MOE_OK) return s;
     s = launch_permute_reroute(L.cand, L.cand_w, a->x, a->dtype, a->T, a->d, a->N, a->k,
                                a->reroute_rounds, cap, L.topk_idx, L.topk_w, nullptr, L.counts,
-                               L.offsets, L.perm_token, L.row_scale, L.inv_pos, L.x_perm,
+                               L.offsets, L.perm_token, L.row_scale, L.inv_pos, x_perm,
                                L.dropped, a->rerouted, a->device_status, L.rr_ws, stream);
     if (s != MOE_OK) return s;
   } else {
@@ -434,14 +504,23 @@ moe_status_t moe_forward(const moe_forward_args *a, void *workspace, size_t work
                            a->logits, L.topk_idx, L.topk_w, a->device_status, stream);
     if (s != MOE_OK) return s;
     s = launch_permute(L.topk_idx, L.topk_w, a->x, a->dtype, a->T, a->d, a->N, a->k, cap,
-                       L.counts, L.offsets, L.perm_token, L.row_scale, L.inv_pos, L.x_perm,
+                       L.counts, L.offsets, L.perm_token, L.row_scale, L.inv_pos, x_perm,
                        L.dropped, a->device_status, L.perm_ws, stream);
     if (s != MOE_OK) return s;
     if (a->rerouted) MOE_CUDA_TRY(cudaMemsetAsync(a->rerouted, 0, sizeof(int32_t), stream));
   }
-  s = launch_expert_ffn(L.x_perm, L.offsets, L.row_scale, A_max, a->d, a->f, a->N, cap,
-                        a->dtype, a->W_gate, a->W_up, a->W_down, L.y_perm, a->device_status,
-                        L.ffn_ws, stream);
+  if (fp8) {
+    // E4M3 gate/up: the dispatched rows are the quantised token rows
+    s = launch_copy_row_bytes(L.xq, (size_t)a->d, L.inv_pos, a->T, a->k, L.x_perm, stream);
+    if (s != MOE_OK) return s;
+    s = launch_ffn_tc_fp8(L.x_perm, L.xs, L.perm_token, L.offsets, L.row_scale, A_max, a->d,
+                          a->f, a->N, cap, a->Wq_gate, a->wscale_gate, a->Wq_up, a->wscale_up,
+                          a->W_down, L.ffn_ws, L.y_perm, a->device_status, stream);
+  } else {
+    s = launch_expert_ffn(L.x_perm, L.offsets, L.row_scale, A_max, a->d, a->f, a->N, cap,
+                          a->dtype, a->W_gate, a->W_up, a->W_down, L.y_perm, a->device_status,
+                          L.ffn_ws, stream);
+  }
   if (s != MOE_OK) return s;
   if (a->fs > 0) {
     set_shared_offsets<<<1, 1, 0, stream>>>(L.sh_offsets, a->T);

@@ -91,9 +91,26 @@ moe_status_t launch_permute(const int32_t *topk_idx, const float *topk_w, const 
                             bool neg_one_drops = false);
 
 // Copies each token's row of x to the positions inv_pos gives its slots
-// (-1: dropped), in token order; nothing when x_perm is null.
+// (-1: dropped), in token order; nothing when x_perm is null.  Rows of
+// row_bytes bytes (a multiple of 16).
 moe_status_t launch_copy_rows(const void *x, moe_dtype_t dtype, const int32_t *inv_pos, int T,
                               int d, int k, void *x_perm, cudaStream_t stream);
+moe_status_t launch_copy_row_bytes(const void *x, size_t row_bytes, const int32_t *inv_pos,
+                                   int T, int k, void *x_perm, cudaStream_t stream);
+
+// FP8 E4M3 with absmax scales: rows of x [R, C] bf16 -> codes [R, C] + [R]
+// scales; gate/up weights W [N, d, f] bf16 -> codes [N, f, d] + [N, f].
+moe_status_t launch_quantize_rows_e4m3(const void *x, int R, int C, uint8_t *q, float *scale,
+                                       cudaStream_t stream);
+moe_status_t launch_quantize_weights_e4m3(const void *W, int N, int d, int f, uint8_t *q,
+                                          float *scale, cudaStream_t stream);
+// Expert FFN with E4M3 gate/up (see ffn_tc.cu).
+moe_status_t launch_ffn_tc_fp8(const void *xq_perm, const float *x_scale,
+                               const int32_t *perm_token, const int32_t *offsets,
+                               const float *row_scale, int A_max, int d, int f, int N,
+                               int capacity, const void *Wq_gate, const float *sw_gate,
+                               const void *Wq_up, const float *sw_up, const void *W_down, void *h,
+                               void *y_perm, int32_t *device_status, cudaStream_t stream);
 
 size_t ffn_workspace_bytes(int A_max, int d, int f, int N, moe_dtype_t dtype);
 // capacity: rows per expert the dispatch kept at most (0 = unknown/none); a

@@ -320,8 +320,13 @@ moe_status_t launch_permute(const int32_t *topk_idx, const float *topk_w, const 
 
 moe_status_t launch_copy_rows(const void *x, moe_dtype_t dtype, const int32_t *inv_pos, int T,
                               int d, int k, void *x_perm, cudaStream_t stream) {
+  return launch_copy_row_bytes(x, (size_t)d * (dtype == MOE_BF16 ? 2 : 4), inv_pos, T, k, x_perm,
+                               stream);
+}
+
+moe_status_t launch_copy_row_bytes(const void *x, size_t row_bytes, const int32_t *inv_pos,
+                                   int T, int k, void *x_perm, cudaStream_t stream) {
   if (x_perm && T > 0) {
-    const size_t row_bytes = (size_t)d * (dtype == MOE_BF16 ? 2 : 4);
     const int vecs = (int)(row_bytes / 16);
     long grid = ((long)T + 7) / 8;
     if (grid > 148L * 16) grid = 148L * 16;

@@ -1,0 +1,123 @@
+// FP8 E4M3 expert weights and token rows, calibration-free absmax scales.
+//
+// Source: "大模型MoE混合专家架构原理与DeepSeek-V4工程实践解析", section
+// MoE模型推理部署与显存优化实战 (inference is bound by memory bandwidth; the
+// remedy named third is storing the weights in fewer bits, with FP8 used for
+// the cached activations); "MoE稀疏激活原理与工程实践", 4.3 (16-bit weights
+// compressed to fewer bits to shrink memory).
+//
+// Reading (the pages name the idea, not a format): OCP FP8 E4M3 (bias 7, 3
+// mantissa bits, largest finite 448, no infinities).  A vector v -- one token
+// row of x over d, or one output channel of a gate/up matrix over d -- is
+// stored as q = E4M3(v * (448 / amax|v|)) (round to nearest even, saturated)
+// and one fp32 scale amax / 448; both factors are formed in fp32 (an all-zero
+// vector takes scale 1).  Weights are written channel-major, [N, f, d], so
+// the FP8 GEMM reads both operands K-major.
+#include <cuda_fp8.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ uint8_t to_e4m3(float v) {
+  return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+}
+
+// One warp per row (grid-stride over rows); C % 8 == 0, 16-byte rows.
+__global__ void __launch_bounds__(256) quantize_rows_e4m3(const __nv_bfloat16 *__restrict__ x,
+                                                          int R, int C, uint8_t *__restrict__ q,
+                                                          float *__restrict__ scale) {
+  const int lane = threadIdx.x % 32;
+  const int warps = blockDim.x / 32;
+  const int nv = C / 8;
+  for (long r = (long)blockIdx.x * warps + threadIdx.x / 32; r < R; r += (long)gridDim.x * warps) {
+    const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)r * C);
+    float am = 0.f;
+    for (int v = lane; v < nv; v += 32) {
+      float f[8];
+      load8(reinterpret_cast<const __nv_bfloat16 *>(row + v), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    const float inv = am > 0.f ? 448.0f / am : 1.0f;
+    if (lane == 0) scale[r] = am > 0.f ? am / 448.0f : 1.0f;
+    uint2 *out = reinterpret_cast<uint2 *>(q + (size_t)r * C);
+    for (int v = lane; v < nv; v += 32) {
+      float f[8];
+      load8(reinterpret_cast<const __nv_bfloat16 *>(row + v), f);
+      uint32_t w[2] = {0u, 0u};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i / 4] |= (uint32_t)to_e4m3(f[i] * inv) << (8 * (i % 4));
+      out[v] = make_uint2(w[0], w[1]);
+    }
+  }
+}
+
+// Block (32 output channels, expert e): the channels' absmax over d, then the
+// codes in tiles of 128 d, transposed through shared memory so each channel's
+// 128 bytes leave as eight 16-byte stores.  d % 16 == 0.
+constexpr int kQCols = 32;
+constexpr int kQRows = 128;
+__global__ void __launch_bounds__(256) quantize_weights_e4m3(
+    const __nv_bfloat16 *__restrict__ W, int d, int f, uint8_t *__restrict__ q,
+    float *__restrict__ scale) {
+  __shared__ float red[8][kQCols];
+  __shared__ float inv_s[kQCols];
+  __shared__ __align__(16) uint8_t tile[kQCols][kQRows + 16];
+  const int e = blockIdx.y, f0 = blockIdx.x * kQCols;
+  const int c = threadIdx.x % kQCols, rg = threadIdx.x / kQCols;   // 8 row groups
+  const __nv_bfloat16 *We = W + (size_t)e * d * f;
+  const bool col_ok = f0 + c < f;
+  float am = 0.f;
+  if (col_ok)
+    for (int i = rg; i < d; i += 8) am = fmaxf(am, fabsf(__bfloat162float(We[(size_t)i * f + f0 + c])));
+  red[rg][c] = am;
+  __syncthreads();
+  if (rg == 0) {
+    float a = 0.f;
+    for (int g = 0; g < 8; ++g) a = fmaxf(a, red[g][c]);
+    inv_s[c] = a > 0.f ? 448.0f / a : 1.0f;
+    if (col_ok) scale[(size_t)e * f + f0 + c] = a > 0.f ? a / 448.0f : 1.0f;
+  }
+  __syncthreads();
+  const int wc = threadIdx.x / 8, wch = threadIdx.x % 8;   // writer: channel, 16-B chunk
+  for (int d0 = 0; d0 < d; d0 += kQRows) {
+    if (col_ok) {
+      const float inv = inv_s[c];
+      for (int j = rg; j < kQRows && d0 + j < d; j += 8)
+        tile[c][j] = to_e4m3(__bfloat162float(We[(size_t)(d0 + j) * f + f0 + c]) * inv);
+    }
+    __syncthreads();
+    if (f0 + wc < f && d0 + wch * 16 < d)
+      *reinterpret_cast<uint4 *>(q + ((size_t)e * f + f0 + wc) * d + d0 + wch * 16) =
+          *reinterpret_cast<const uint4 *>(&tile[wc][wch * 16]);
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+moe_status_t launch_quantize_rows_e4m3(const void *x, int R, int C, uint8_t *q, float *scale,
+                                       cudaStream_t stream) {
+  if (R == 0) return MOE_OK;
+  long grid = ((long)R + 7) / 8;
+  if (grid > 148L * 16) grid = 148L * 16;
+  quantize_rows_e4m3<<<(int)grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(x), R, C,
+                                                    q, scale);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+moe_status_t launch_quantize_weights_e4m3(const void *W, int N, int d, int f, uint8_t *q,
+                                          float *scale, cudaStream_t stream) {
+  dim3 grid((f + kQCols - 1) / kQCols, N);
+  quantize_weights_e4m3<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(W), d, f,
+                                                  q, scale);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+}  // namespace moe

@@ -14,8 +14,9 @@
 //     MN-major: rows of 64 MN-elements (128 B), one row per k, 8-k atoms of
 //               1024 B; LBO = distance between 64-element MN chunks,
 //               SBO = distance between 8-k groups.
-//   instruction descriptor (kind::f16, 32 bit):
-//     [4,6) D fmt (1 = f32)  [7,10) A fmt (1 = bf16)  [10,13) B fmt (1 = bf16)
+//   instruction descriptor (kind::f16 and kind::f8f6f4, 32 bit):
+//     [4,6) D fmt (1 = f32)  [7,10) A fmt (kind::f16: 1 = bf16; kind::f8f6f4:
+//     0 = E4M3)  [10,13) B fmt (the same codes)
 //     [15] A major (1 = MN)  [16] B major (1 = MN)  [17,23) N >> 3  [24,29) M >> 4
 #pragma once
 
@@ -260,6 +261,16 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
   asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
 }
+// A pair MMA with 8-bit operands (kind::f8f6f4; E4M3 x E4M3 -> f32 here, 32 K
+// per instruction), laid out as for mma_f16_pair below.
+__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // D (both CTAs' tensor memory, 128 rows each) (+)= A (both CTAs' smem, 128 rows
 // each) x B (N/2 rows in each CTA's smem).  Issued by one thread of the even CTA.
 __device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
@@ -302,6 +313,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// E4M3 x E4M3 -> f32 (kind::f8f6f4: A and B format field 0 = E4M3), both
+// operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 }  // namespace tc

@@ -48,13 +48,15 @@ MUTANTS = [
     ("reroute_weights_first_choice",
      "const int e = cand[(size_t)t * kr + final_cand[(size_t)t * k + j]];\n        final_w",
      "const int e = cand[(size_t)t * kr + j];\n        final_w"),
-    ("e4m3_ties_to_odd", "(c & 1) == 0 && (best & 1) == 1", "(c & 1) == 1 && (best & 1) == 0"),
+    ("e4m3_ties_to_odd", "else c = (lo & 1) == 0 ? lo : hi;", "else c = (lo & 1) == 0 ? hi : lo;"),
+    ("e4m3_round_down", "if (dlo < dhi) c = lo;", "if (dlo <= 2 * dhi) c = lo;"),
     ("e4m3_subnormal_exponent", "ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
     ("e4m3_bias_8", "ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
     ("fp8_scale_inverted", "*scale = amax > 0.0f ? amax / 448.0f : 1.0f;",
      "*scale = amax > 0.0f ? 448.0f / amax : 1.0f;"),
-    ("fp8_weights_input_axis", "quantize_vector(W, dtype, (size_t)e * d * f + j, (size_t)f, d,",
-     "quantize_vector(W, dtype, (size_t)e * d * f + (size_t)j * d, 1, d,"),
+    ("fp8_weights_input_axis",
+     "quantize_vector(c->W, c->dtype, (size_t)e * c->d * c->f + j, (size_t)c->f, c->d,",
+     "quantize_vector(c->W, c->dtype, (size_t)e * c->d * c->f + (size_t)j * c->d, 1, c->d,"),
 ]
 
 
