@@ -53,12 +53,16 @@ class Work:
     flop_ffn: float
 
 
-def layer_work(T, d, f, N, k, A, touched, fs=0, esize=2):
-    """Algorithmic work of one forward: A kept rows, `touched` experts with >=1 row."""
+def layer_work(T, d, f, N, k, A, touched, fs=0, esize=2, fp8_gate_up=False):
+    """Algorithmic work of one forward: A kept rows, `touched` experts with >=1 row.
+    fp8_gate_up: the routed gate/up weights are 1-byte E4M3 codes plus one fp32
+    scale per output channel (the down projection keeps `esize`)."""
     flop_router = 2.0 * T * d * N
     flop_ffn = 6.0 * d * f * A
     flop_shared = 6.0 * d * fs * T
-    wbytes = touched * expert_params(d, f) * esize + d * N * esize + expert_params(d, fs) * esize
+    per_expert = (2 * d * f * 1 + 2 * f * 4 + d * f * esize) if fp8_gate_up \
+        else expert_params(d, f) * esize
+    wbytes = touched * per_expert + d * N * esize + expert_params(d, fs) * esize
     # x read twice (router, gather), x_perm written+read, h written+read (gate/up -> down),
     # y_perm written+read, y written in fp32 (+ shared y written + read)
     act = (2 * T * d + 2 * A * d + 2 * A * f + 2 * A * d) * esize + T * d * 4
@@ -68,10 +72,16 @@ def layer_work(T, d, f, N, k, A, touched, fs=0, esize=2):
                 flop_ffn + flop_shared)
 
 
-def roofline_time_s(work: Work, pk=None, sustained=False):
+# Dense FP8 over dense bf16 tensor rate, nominal (4.5 vs 2.25 PFLOP/s).
+FP8_OVER_BF16 = 2.0
+
+
+def roofline_time_s(work: Work, pk=None, sustained=False, fp8_flop=0.0):
+    """fp8_flop: the part of work.flop that runs on FP8 tensor cores (at the
+    bf16 peak times the nominal FP8/bf16 ratio)."""
     pk = pk or peaks()
     tc = pk["bf16_tflops_sustained" if sustained else "bf16_tflops"] * 1e12
     bw = pk["hbm_gbs"] * 1e9
-    t_flop = work.flop / tc
+    t_flop = (work.flop - fp8_flop) / tc + fp8_flop / (tc * FP8_OVER_BF16)
     t_bytes = work.weight_bytes / bw
     return max(t_flop, t_bytes), ("tensor" if t_flop >= t_bytes else "hbm"), t_flop, t_bytes
