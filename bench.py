@@ -65,6 +65,8 @@ def parse():
     ap.add_argument("--fp8", action="store_true",
                     help="routed gate/up projections in FP8 E4M3 (per-channel weight and "
                          "per-token activation scales); the down projection stays bf16")
+    ap.add_argument("--fp8-down", action="store_true",
+                    help="with --fp8: the down projection in FP8 E4M3 too (h quantised per row)")
     ap.add_argument("--forward-only", action="store_true",
                     help="time moe_forward only (no stage, end-to-end or CPU legs)")
     return ap.parse_args()
@@ -282,7 +284,7 @@ def run_ours(args, ws, rank, local):
     layer = B.MoELayer(inp.W_g, inp.W_gate, inp.W_up, inp.W_down, cfg.k, bias=inp.bias,
                        Ws_gate=inp.Ws_gate, Ws_up=inp.Ws_up, Ws_down=inp.Ws_down,
                        capacity_factor=cfg.cf, y_dtype=y_dtype, reroute_rounds=args.reroute,
-                       fp8=args.fp8)
+                       fp8=args.fp8, fp8_down=args.fp8 and args.fp8_down)
     y = torch.empty((cfg.T, cfg.d), dtype=y_dtype, device=dev)
     outs = layer.outputs_for(cfg.T, dev)
     a = layer.args(inp.x, y, outs)
@@ -360,7 +362,8 @@ def run_ours(args, ws, rank, local):
     }
     if args.fp8:
         # the FP8 layer's FFN: E4M3 rows of the permuted tokens, E4M3 gate/up
-        qg, sg, qu, su = layer.fp8
+        qg, sg, qu, su = layer.fp8[:4]
+        qd, sd = layer.fp8[4:6] if len(layer.fp8) > 4 else (None, None)
         xq, sx = B.quantize_rows_e4m3(inp.x)
         A_kept = int(perm["offsets"][-1].item())          # rows past it hold no token
         xq_perm = torch.zeros((A_max, cfg.d), dtype=torch.uint8, device=dev)
@@ -368,7 +371,8 @@ def run_ours(args, ws, rank, local):
         stage_ms["quantize_rows"] = time_stage(lambda: B.quantize_rows_e4m3(inp.x), reps)
         stage_ms["expert_ffn_bf16"] = stage_ms["expert_ffn"]
         stage_ms["expert_ffn"] = time_stage(lambda: B.moe_expert_ffn_fp8(
-            xq_perm, sx, perm["perm_token"], perm["offsets"], qg, sg, qu, su, inp.W_down,
+            xq_perm, sx, perm["perm_token"], perm["offsets"], qg, sg, qu, su,
+            W_down=None if qd is not None else inp.W_down, Wq_down=qd, wscale_down=sd,
             row_scale=perm["row_scale"], y_perm=y_perm, A_max=A_max), reps)
     if args.reroute > 0:
         cand, cand_w = B.moe_router_topk(inp.x, inp.W_g, k + args.reroute, bias=inp.bias)
@@ -413,22 +417,24 @@ def run_ours(args, ws, rank, local):
     A = int(offsets[-1].item())
     touched = int((kept > 0).sum().item())
     esz = 2 if cfg.dtype == "bf16" else 4
+    fp8_down = args.fp8 and args.fp8_down
     work = RL.layer_work(cfg.T, cfg.d, cfg.f, N, k, A, touched, cfg.fs, esz,
-                         fp8_gate_up=args.fp8)
+                         fp8_gate_up=args.fp8, fp8_down=fp8_down)
     pk = RL.peaks()
-    t_roof, bound, t_flop, t_bytes = RL.roofline_time_s(
-        work, pk, fp8_flop=4.0 * cfg.d * cfg.f * A if args.fp8 else 0.0)
+    fp8_flop = (4.0 if args.fp8 else 0.0) * cfg.d * cfg.f * A + (2.0 if fp8_down else 0.0) * cfg.d * cfg.f * A
+    t_roof, bound, t_flop, t_bytes = RL.roofline_time_s(work, pk, fp8_flop=fp8_flop)
     value = whole_job_value(ws, cfg.T, ms_max)
 
     # dominant kernel: the grouped expert FFN (gate/up + SwiGLU, down + gate scale)
     ffn_ms = stage_ms["expert_ffn"]
     ffn_flop = 6.0 * cfg.d * cfg.f * A
     ffn_bytes = touched * (RL.expert_params(cfg.d, cfg.f) * esz if not args.fp8
-                           else 2 * cfg.d * cfg.f + 2 * cfg.f * 4 + cfg.d * cfg.f * esz)
+                           else 2 * cfg.d * cfg.f + 2 * cfg.f * 4 +
+                           (cfg.d * cfg.f + cfg.d * 4 if fp8_down else cfg.d * cfg.f * esz))
     # FP8 layers: 2/3 of the FFN FLOPs (gate/up) run at the FP8 rate, so the
     # FFN's peak is the bf16 peak scaled by FLOPs over bf16-equivalent FLOPs
-    peak_scale = (ffn_flop / (ffn_flop / 3 + (2 * ffn_flop / 3) / RL.FP8_OVER_BF16)
-                  if args.fp8 else 1.0)
+    fp8_share = (1.0 if fp8_down else 2 / 3) if args.fp8 else 0.0
+    peak_scale = 1.0 / ((1 - fp8_share) + fp8_share / RL.FP8_OVER_BF16)
     if bound == "tensor":
         achieved = ffn_flop / (ffn_ms / 1e3) / 1e12
         peak = round(pk["bf16_tflops"] * peak_scale, 1)
@@ -437,7 +443,8 @@ def run_ours(args, ws, rank, local):
         achieved = ffn_bytes / (ffn_ms / 1e3) / 1e9
         peak = pk["hbm_gbs"]
         unit = "GB/s"
-    traffic, tkernel = traffic_from_profiles(cfg.name + ("_fp8" if args.fp8 else ""))
+    traffic, tkernel = traffic_from_profiles(
+        cfg.name + ("_fp8_all" if fp8_down else "_fp8" if args.fp8 else ""))
     line = {
         "metric": "MoE-layer tokens/s on 1 B300 and % of roofline (active FLOPs vs expert bytes)",
         "value": round(value, 1),
@@ -449,14 +456,14 @@ def run_ours(args, ws, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": ("e4m3 gate/up + bf16" if args.fp8 else
+        "dtype": ("e4m3 experts + bf16" if fp8_down else "e4m3 gate/up + bf16" if args.fp8 else
                   "bf16" if cfg.dtype == "bf16" else "f32"),
         "data": "synthetic (seeded Gaussian x and N(0,1/fan_in) weights of the workload's shape)",
         "config": {"workload": cfg_desc(cfg) + (f", overflow re-routed in {args.reroute} rounds"
                                                  if args.reroute else "")
-                   + (", gate/up in FP8 E4M3 (per-channel / per-token absmax scales)"
-                      if args.fp8 else ""),
-                   "fp8_gate_up": bool(args.fp8),
+                   + (", gate/up" + (" and down" if fp8_down else "") +
+                      " in FP8 E4M3 (per-channel / per-row absmax scales)" if args.fp8 else ""),
+                   "fp8_gate_up": bool(args.fp8), "fp8_down": bool(fp8_down),
                    "reroute_rounds": args.reroute, "T": cfg.T, "d": cfg.d, "f": cfg.f, "N": N,
                    "k": k, "fs": cfg.fs, "capacity_factor": cfg.cf, "bias_std": cfg.bias_std,
                    "y_dtype": args.y_dtype, "parallelism": f"replicas x{ws} (no exchange)",

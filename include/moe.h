@@ -213,9 +213,10 @@ moe_status_t moe_expert_ffn(const void *x_perm, const int32_t *offsets,
  * E4M3(v * (448 / amax|v|)) (nearest even, saturating) and the fp32 scale
  * amax / 448 (an all-zero vector: scale 1).
  *
- * moe_quantize_weights_e4m3: gate or up weights W [N,d,f] bf16, one scale per
- *   output channel (a column over d): Wq [N,f,d] codes (channel-major, so the
- *   GEMM reads it K-major), scale [N,f].  d % 16 == 0.  An offline step.
+ * moe_quantize_weights_e4m3: weights W [N,d,f] bf16 read as [N, K=d, M=f]
+ *   (gate/up: K = model dim; W_down [N,f,d]: pass (d=f, f=d)), one scale per
+ *   output column m over K: Wq [N,f,d] codes (channel-major, so the GEMM
+ *   reads it K-major), scale [N,f].  d % 16 == 0.  An offline step.
  * moe_quantize_rows_e4m3: rows x [R,C] bf16, one scale per row: q [R,C],
  *   scale [R].  C % 16 == 0.
  * moe_expert_ffn_fp8: moe_expert_ffn with E4M3 gate/up: xq_perm [A_max,d]
@@ -223,8 +224,14 @@ moe_status_t moe_expert_ffn(const void *x_perm, const int32_t *offsets,
  *   row p's scale = x_scale[perm_token[p]] (x_scale [T] per token);
  *   g = (xq . Wq_gate[e][j]) * x_scale * wscale_gate[e][j], u likewise,
  *   h = SiLU(g) * u rounded to bf16, y_perm = row_scale * (h W_down) as in
- *   moe_expert_ffn.  Workspace: moe_expert_ffn_workspace_size(.., MOE_BF16).
+ *   moe_expert_ffn.  With Wq_down ([N,d,f] codes, wscale_down [N,d]; W_down
+ *   may be NULL) the down projection is E4M3 too: each kept row of h is
+ *   quantised like x (one scale per row, f % 16 == 0) and
+ *   y_perm[p][m] = row_scale[p] * (hq . Wq_down[e][m]) * h_scale[p] *
+ *   wscale_down[e][m].  Workspace: moe_expert_ffn_fp8_workspace_size.
  * ------------------------------------------------------------------------- */
+size_t moe_expert_ffn_fp8_workspace_size(int A_max, int d, int f, int N,
+                                         int fp8_down);
 moe_status_t moe_quantize_weights_e4m3(const void *W, int N, int d, int f,
                                        uint8_t *Wq, float *scale, void *stream);
 moe_status_t moe_quantize_rows_e4m3(const void *x, int R, int C, uint8_t *q,
@@ -235,7 +242,8 @@ moe_status_t moe_expert_ffn_fp8(const uint8_t *xq_perm, const float *x_scale,
                                 int A_max, int d, int f, int N,
                                 const uint8_t *Wq_gate, const float *wscale_gate,
                                 const uint8_t *Wq_up, const float *wscale_up,
-                                const void *W_down, void *y_perm,
+                                const void *W_down, const uint8_t *Wq_down,
+                                const float *wscale_down, void *y_perm,
                                 int32_t *device_status, void *workspace,
                                 size_t workspace_bytes, void *stream);
 
@@ -291,6 +299,10 @@ typedef struct moe_forward_args {
   const float *wscale_gate;   /* [N,f] channel scales                        */
   const uint8_t *Wq_up;       /* [N,f,d]                                     */
   const float *wscale_up;     /* [N,f]                                       */
+  const uint8_t *Wq_down;     /* optional with the above: E4M3 down projection
+                                 [N,d,f] (W_down may then be NULL); h is
+                                 quantised per row before it               */
+  const float *wscale_down;   /* [N,d]                                       */
 } moe_forward_args;
 
 size_t moe_forward_workspace_size(const moe_forward_args *args);

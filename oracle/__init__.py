@@ -42,6 +42,7 @@ def _load(path=None):
         lib.oracle_combine_rows.argtypes = [ci, ci, ci, i32p, f64p, f64p, f64p, f64p]
         lib.oracle_routing_stats.argtypes = [ci, ci, f64p, i32p, f64p, i32p, f64p, f64p]
         lib.oracle_reroute.argtypes = [ci, ci, ci, ci, ci, i32p, f64p, i32p, i32p, i32p, f64p]
+        lib.oracle_expert_hidden.argtypes = [ci, ci, ci, vp, vp, ci, vp, ci, f64p, ci]
         lib.oracle_e4m3_decode.argtypes = [ctypes.c_long, vp, f64p]
         lib.oracle_e4m3_decode.restype = None
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_long, f32p, vp]
@@ -398,22 +399,47 @@ def dequantize_e4m3(codes, scales):
     return e4m3_decode(codes) * np.asarray(scales, dtype=np.float64)[..., None]
 
 
-def expert_rows_fp8(qg_e, sg_e, qu_e, su_e, W_down_e, xq_rows, sx_rows, nthreads=None):
+def expert_hidden(W_gate_e, W_up_e, xrows, nthreads=None):
+    """h[R,f] (fp64) = SiLU(x W_gate_e) * (x W_up_e) for each row of xrows."""
+    lib = _load()
+    bg, bu, bx = _Buf(W_gate_e), _Buf(W_up_e), _Buf(xrows)
+    assert bg.dtype is not None and bg.dtype == bu.dtype
+    d, f = bg.keep.shape
+    R = bx.keep.shape[0]
+    h = np.empty((R, f), dtype=np.float64)
+    _check(lib.oracle_expert_hidden(d, f, bg.dtype, bg.ptr, bu.ptr, R, bx.ptr, bx.dtype,
+                                    h.ctypes.data, nthreads or default_threads()),
+           "oracle_expert_hidden")
+    return h
+
+
+def expert_rows_fp8(qg_e, sg_e, qu_e, su_e, W_down_e, xq_rows, sx_rows, qd_e=None, sd_e=None,
+                    nthreads=None):
     """SwiGLU expert with E4M3 gate/up weights (codes [f,d], scales [f]) on E4M3
-    token rows (codes [R,d], scales [R]); the down projection W_down_e [f,d]
-    as given.  Every value is the exact dequantised one; fp64 throughout."""
+    token rows (codes [R,d], scales [R]).  Down projection: W_down_e [f,d] as
+    given, or, with qd_e (codes [d,f]) and sd_e (scales [d]), E4M3 too: then h
+    is rounded to bf16 (as the layer stores it) and quantised per row like x
+    before it.  Every value is the exact dequantised one; fp64 throughout."""
     wg = np.ascontiguousarray(dequantize_e4m3(qg_e, sg_e).T)
     wu = np.ascontiguousarray(dequantize_e4m3(qu_e, su_e).T)
-    wd = W_down_e.detach().cpu().double().contiguous() if isinstance(W_down_e, torch.Tensor) \
-        else np.ascontiguousarray(W_down_e, dtype=np.float64)
     xr = dequantize_e4m3(xq_rows, sx_rows)
-    return expert_rows(wg, wu, wd, xr, nthreads)
+    if qd_e is None:
+        wd = W_down_e.detach().cpu().double().contiguous() \
+            if isinstance(W_down_e, torch.Tensor) \
+            else np.ascontiguousarray(W_down_e, dtype=np.float64)
+        return expert_rows(wg, wu, wd, xr, nthreads)
+    h = expert_hidden(wg, wu, xr, nthreads)
+    qh, sh = quantize_rows_e4m3(torch.from_numpy(h).to(torch.bfloat16))
+    hd = dequantize_e4m3(qh, sh)                          # [R, f]
+    wd = dequantize_e4m3(qd_e, sd_e)                      # [d, f]: row m = output column m
+    return hd @ wd.T                                      # o[r, m] = sum_j h[r, j] wd[m, j]
 
 
 def forward_rows_fp8(xq_rows, sx_rows, topk_idx_rows, topk_w_rows, inv_pos_rows,
                      fetch_expert_fp8, shared=None, x_rows=None, nthreads=None):
     """Layer output for a subset of tokens with E4M3 gate/up weights and token
-    rows: fetch_expert_fp8(e) -> (qg [f,d], sg [f], qu [f,d], su [f], W_down [f,d]).
+    rows: fetch_expert_fp8(e) -> (qg [f,d], sg [f], qu [f,d], su [f], W_down [f,d])
+    or the same plus (qd [d,f], sd [d]) for an E4M3 down projection.
     Experts one at a time (each dequantised expert is held in fp64).  The
     shared expert (Ws_gate, Ws_up, Ws_down), when given, runs in the layer's
     own precision on x_rows.  Returns y [R,d] fp64."""
@@ -424,9 +450,10 @@ def forward_rows_fp8(xq_rows, sx_rows, topk_idx_rows, topk_w_rows, inv_pos_rows,
     out = np.zeros((R, k, d), dtype=np.float64)
     for e in sorted(set(int(v) for v in idx[inv >= 0].ravel())):
         rows, slots = np.nonzero((idx == e) & (inv >= 0))
-        qg, sg, qu, su, wd = fetch_expert_fp8(e)
-        out[rows, slots] = expert_rows_fp8(qg, sg, qu, su, wd, xq_rows[rows], sx_rows[rows],
-                                           nthreads)
+        w = fetch_expert_fp8(e)          # qg, sg, qu, su, W_down (, qd, sd)
+        out[rows, slots] = expert_rows_fp8(*w[:5], xq_rows[rows], sx_rows[rows],
+                                           *(w[5:7] if len(w) > 5 else (None, None)),
+                                           nthreads=nthreads)
     sh = None
     if shared is not None:
         sh = expert_rows(shared[0], shared[1], shared[2], x_rows, nthreads)

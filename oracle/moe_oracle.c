@@ -281,6 +281,38 @@ static void ffn_rows(long lo, long hi, void *p) {
   free(g); free(u); free(xr);
 }
 
+/* The hidden activations alone: h[r, j] = SiLU(g) * u for row r (the first
+ * half of the expert above; used where h itself is quantised). */
+typedef struct {
+  int d, f, dtype, x_dtype;
+  const void *Wg, *Wu, *xrows;
+  double *h;
+} hid_ctx;
+
+static void hidden_rows(long lo, long hi, void *p) {
+  hid_ctx *c = (hid_ctx *)p;
+  for (long r = lo; r < hi; ++r) {
+    double *h = c->h + (size_t)r * c->f;
+    for (int j = 0; j < c->f; ++j) {
+      double g = 0.0, u = 0.0;
+      for (int i = 0; i < c->d; ++i) {
+        const double xi = elem(c->xrows, c->x_dtype, (size_t)r * c->d + i);
+        g += xi * elem(c->Wg, c->dtype, (size_t)i * c->f + j);
+        u += xi * elem(c->Wu, c->dtype, (size_t)i * c->f + j);
+      }
+      h[j] = g / (1.0 + exp(-g)) * u;
+    }
+  }
+}
+
+int oracle_expert_hidden(int d, int f, int dtype, const void *W_gate_e, const void *W_up_e,
+                         int R, const void *xrows, int x_dtype, double *h, int nthreads) {
+  if (d < 1 || f < 1 || R < 0 || !W_gate_e || !W_up_e || (R > 0 && (!xrows || !h))) return 1;
+  hid_ctx c = {d, f, dtype, x_dtype, W_gate_e, W_up_e, xrows, h};
+  parallel_for(R, nthreads, hidden_rows, &c);
+  return 0;
+}
+
 int oracle_expert_rows(int d, int f, int dtype, const void *W_gate_e,
                        const void *W_up_e, const void *W_down_e, int R,
                        const void *xrows, int x_dtype, double *out,

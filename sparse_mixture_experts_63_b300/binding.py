@@ -28,7 +28,8 @@ EXPORTS = ("moe_status_string", "moe_last_error", "moe_version", "moe_launch_cou
            "moe_forward_workspace_size", "moe_forward", "moe_forward_host_io",
            "moe_routing_stats_workspace_size", "moe_routing_stats",
            "moe_permute_reroute_workspace_size", "moe_permute_reroute",
-           "moe_quantize_weights_e4m3", "moe_quantize_rows_e4m3", "moe_expert_ffn_fp8")
+           "moe_quantize_weights_e4m3", "moe_quantize_rows_e4m3",
+           "moe_expert_ffn_fp8_workspace_size", "moe_expert_ffn_fp8")
 
 
 class MoEError(RuntimeError):
@@ -53,7 +54,8 @@ class moe_forward_args(ctypes.Structure):
                 ("device_status", ctypes.c_void_p), ("reroute_rounds", ctypes.c_int),
                 ("rerouted", ctypes.c_void_p), ("Wq_gate", ctypes.c_void_p),
                 ("wscale_gate", ctypes.c_void_p), ("Wq_up", ctypes.c_void_p),
-                ("wscale_up", ctypes.c_void_p)]
+                ("wscale_up", ctypes.c_void_p), ("Wq_down", ctypes.c_void_p),
+                ("wscale_down", ctypes.c_void_p)]
 
 
 _lib = None
@@ -100,8 +102,10 @@ def lib():
                                           [sz, vp])
         L.moe_quantize_weights_e4m3.argtypes = [vp, ci, ci, ci, vp, vp, vp]
         L.moe_quantize_rows_e4m3.argtypes = [vp, ci, ci, vp, vp, vp]
+        L.moe_expert_ffn_fp8_workspace_size.argtypes = [ci, ci, ci, ci, ci]
+        L.moe_expert_ffn_fp8_workspace_size.restype = sz
         L.moe_expert_ffn_fp8.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, vp, vp, vp, vp, vp,
-                                         vp, vp, vp, sz, vp]
+                                         vp, vp, vp, vp, vp, sz, vp]
         for n in ("moe_router_topk", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn",
                   "moe_quantize_weights_e4m3", "moe_quantize_rows_e4m3", "moe_expert_ffn_fp8",
                   "moe_combine", "moe_routing_stats", "moe_permute_reroute",
@@ -240,8 +244,9 @@ def moe_expert_ffn(x_perm, offsets, W_gate, W_up, W_down, row_scale=None, y_perm
 
 
 def quantize_weights_e4m3(W, stream=None):
-    """Gate or up weights W [N,d,f] bf16 -> (codes uint8 [N,f,d], scales fp32 [N,f]),
-    E4M3 with one absmax scale per output channel."""
+    """Weights W [N,K,M] bf16 (K the reduction dim: gate/up [N,d,f], down
+    [N,f,d]) -> (codes uint8 [N,M,K], scales fp32 [N,M]), E4M3 with one absmax
+    scale per output channel."""
     _cuda(W)
     N, d, f = W.shape
     q = torch.empty((N, f, d), dtype=torch.uint8, device=W.device)
@@ -263,23 +268,25 @@ def quantize_rows_e4m3(x, stream=None):
 
 
 def moe_expert_ffn_fp8(xq_perm, x_scale, perm_token, offsets, Wq_gate, wscale_gate, Wq_up,
-                       wscale_up, W_down, row_scale=None, y_perm=None, device_status=None,
-                       stream=None, A_max=None):
+                       wscale_up, W_down=None, Wq_down=None, wscale_down=None, row_scale=None,
+                       y_perm=None, device_status=None, stream=None, A_max=None):
     """moe_expert_ffn with E4M3 gate/up (codes [N,f,d] + channel scales [N,f]) on
-    E4M3 permuted token rows xq_perm [A_max,d] (row p's scale x_scale[perm_token[p]])."""
+    E4M3 permuted token rows xq_perm [A_max,d] (row p's scale x_scale[perm_token[p]]);
+    the down projection from W_down (bf16) or, given Wq_down [N,d,f] and
+    wscale_down [N,d], in E4M3 on h quantised per row."""
     _cuda(xq_perm, x_scale, perm_token, offsets, Wq_gate, wscale_gate, Wq_up, wscale_up, W_down,
-          row_scale, y_perm)
+          Wq_down, wscale_down, row_scale, y_perm)
     A = xq_perm.shape[0] if A_max is None else A_max
     d = xq_perm.shape[1]
     N, f, _ = Wq_gate.shape
     if y_perm is None:
-        y_perm = torch.empty((max(A, 1), d), dtype=W_down.dtype, device=xq_perm.device)
-    ws_bytes = lib().moe_expert_ffn_workspace_size(A, d, f, N, MOE_BF16)
+        y_perm = torch.empty((max(A, 1), d), dtype=torch.bfloat16, device=xq_perm.device)
+    ws_bytes = lib().moe_expert_ffn_fp8_workspace_size(A, d, f, N, int(Wq_down is not None))
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=xq_perm.device)
     _check("moe_expert_ffn_fp8", lib().moe_expert_ffn_fp8(
         _p(xq_perm), _p(x_scale), _p(perm_token), _p(offsets), _p(row_scale), A, d, f, N,
-        _p(Wq_gate), _p(wscale_gate), _p(Wq_up), _p(wscale_up), _p(W_down), _p(y_perm),
-        _p(device_status), _p(ws), ws_bytes, _stream(stream)))
+        _p(Wq_gate), _p(wscale_gate), _p(Wq_up), _p(wscale_up), _p(W_down), _p(Wq_down),
+        _p(wscale_down), _p(y_perm), _p(device_status), _p(ws), ws_bytes, _stream(stream)))
     return y_perm
 
 
@@ -388,9 +395,11 @@ def make_forward_args(x, W_g, W_gate, W_up, W_down, k, y, bias=None, Ws_gate=Non
     a.device_status = _p(device_status)
     a.reroute_rounds = int(reroute_rounds)
     a.rerouted = _p(o.get("rerouted"))
-    if fp8_gate_up is not None:   # (Wq_gate, wscale_gate, Wq_up, wscale_up)
+    if fp8_gate_up is not None:   # (Wq_gate, wscale_gate, Wq_up, wscale_up[, Wq_down, wscale_down])
         _cuda(*fp8_gate_up)
-        a.Wq_gate, a.wscale_gate, a.Wq_up, a.wscale_up = (_p(t) for t in fp8_gate_up)
+        a.Wq_gate, a.wscale_gate, a.Wq_up, a.wscale_up = (_p(t) for t in fp8_gate_up[:4])
+        if len(fp8_gate_up) > 4:
+            a.Wq_down, a.wscale_down = _p(fp8_gate_up[4]), _p(fp8_gate_up[5])
     return a
 
 
@@ -420,18 +429,22 @@ class MoELayer:
     ``layer(x)`` returns y [T,d] (fp32 by default) and keeps the routing
     outputs of the last call in ``layer.last``.  ``fp8=True`` quantises the
     routed experts' gate/up weights to E4M3 once (per-channel scales) and runs
-    those projections in FP8 (x quantised per token on the fly).
+    those projections in FP8 (x quantised per token on the fly);
+    ``fp8_down=True`` does the same for the down projection (h quantised per
+    row on the fly).
     """
 
     def __init__(self, W_g, W_gate, W_up, W_down, k, bias=None, Ws_gate=None, Ws_up=None,
                  Ws_down=None, capacity_factor=0.0, y_dtype=torch.float32, reroute_rounds=0,
-                 fp8=False):
+                 fp8=False, fp8_down=False):
         self.reroute_rounds = reroute_rounds
         self.fp8 = None
-        if fp8:
+        if fp8 or fp8_down:
             qg, sg = quantize_weights_e4m3(W_gate)
             qu, su = quantize_weights_e4m3(W_up)
             self.fp8 = (qg, sg, qu, su)
+            if fp8_down:   # W_down [N,f,d] read as [N, K=f, M=d]
+                self.fp8 += quantize_weights_e4m3(W_down)
         self.W_g, self.W_gate, self.W_up, self.W_down = W_g, W_gate, W_up, W_down
         self.k, self.bias, self.cf, self.y_dtype = k, bias, capacity_factor, y_dtype
         self.Ws_gate, self.Ws_up, self.Ws_down = Ws_gate, Ws_up, Ws_down

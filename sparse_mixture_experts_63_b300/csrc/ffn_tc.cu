@@ -115,12 +115,12 @@ struct TcParams {
   int wide;                // 1: tiles over 256 rows run as two sub-tiles
   int stages;              // pipeline stages (kStageRegion / stage_bytes)
   int stage_bytes;         // kABytes + token rows of a stage (both sub-tiles)
-  // FP8 gate/up (E4M3 weights and token rows, K-major): D is multiplied by
-  // the output channel's scale and the token's scale before SwiGLU
-  const float *wscale_g;   // [N, f] gate channel scales
-  const float *wscale_u;   // [N, f] up channel scales
-  const float *xscale;     // [T] token scales
-  const int32_t *perm_token;  // [A] token of each permuted row
+  // FP8 (E4M3 weights and rows, K-major): D is multiplied by the output
+  // channel's scale and the row's scale before the epilogue's math
+  const float *wscale_g;   // [N, M] channel scales (GEMM1: gate; GEMM2: down)
+  const float *wscale_u;   // [N, M] up channel scales (GEMM1)
+  const float *xscale;     // row scales: [T] by token (GEMM1) or [A] by permuted row (GEMM2)
+  const int32_t *perm_token;  // [A] token of each permuted row (GEMM1), else null
 };
 
 // Token sub-tiles of a tile: rows [row0, row0 + rows0) and, for a wide tile
@@ -312,20 +312,22 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams &p, const TileInfo
   }
 }
 
-// FP8 GEMM1: D of a 32-column chunk (permuted rows row0 .. row0 + 31, of
-// which `valid` hold rows) times this thread's channel scale and each
-// column's token scale.
+// FP8: D of a 32-column chunk (permuted rows row0 .. row0 + 31, of which
+// `valid` hold rows) times this thread's channel scale and each column's row
+// scale (GEMM1: the token's, through perm_token; GEMM2: h's own row scale).
 __device__ __forceinline__ void scale_chunk(const TcParams &p, int row0, int valid, int lane,
                                             float wsc, uint32_t (&r)[32]) {
-  const float sxl = lane < valid ? p.xscale[p.perm_token[row0 + lane]] : 0.f;
+  const float sxl =
+      lane < valid ? p.xscale[p.perm_token ? p.perm_token[row0 + lane] : row0 + lane] : 0.f;
 #pragma unroll
   for (int c = 0; c < 32; ++c)
     r[c] = __float_as_uint(__uint_as_float(r[c]) * (wsc * __shfl_sync(0xffffffffu, sxl, c)));
 }
 
-// FP8: GEMM1 with E4M3 weights [N, f, d] and token rows, both K-major, 128 K
-// per stage (the same 128-byte rows as 64 bf16), kind::f8f6f4 MMAs, and the
-// channel x token scales applied to D before SwiGLU.
+// FP8: E4M3 weights [N, M, K] and token (or h) rows, both K-major, 128 K per
+// stage (the same 128-byte rows as 64 bf16), kind::f8f6f4 MMAs, and the
+// channel x row scales applied to D before SwiGLU (GEMM1) or the gate-weight
+// scale (GEMM2).
 template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA0,
@@ -561,11 +563,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = cid; t < total_tiles && go_on; t += ncl) {
       const TileInfo ti = decode_tile(p, prefix, t);
       const int nsub = ti.rows1 > 0 ? 2 : 1;
-      float wsc = 1.f;   // FP8: this thread's output channel scale (gate or up)
+      float wsc = 1.f;   // FP8: this thread's output channel scale
       if (FP8) {
-        const int fch = ti.pair * 128 + (int)rank * 64 + (lane_grp & 1) * 32 + lane;
-        const float *ws = lane_grp < 2 ? p.wscale_g : p.wscale_u;
-        wsc = fch < p.M ? ws[(size_t)ti.e * p.M + fch] : 0.f;
+        // GEMM1: lanes 0-63 gate, 64-127 up of 64 hidden units; GEMM2: 128 columns of y
+        const int ch = p.gemm1 ? ti.pair * 128 + (int)rank * 64 + (lane_grp & 1) * 32 + lane
+                               : ti.pair * 256 + (int)rank * kBM + lane_grp * 32 + lane;
+        const float *ws = (!p.gemm1 || lane_grp < 2) ? p.wscale_g : p.wscale_u;
+        wsc = ch < p.M ? ws[(size_t)ti.e * p.M + ch] : 0.f;
       }
       for (int sub = 0; sub < nsub; ++sub) {
         const int srow0 = ti.row0 + (sub ? ti.rows0 : 0);   // first permuted row of the sub-tile
@@ -852,23 +856,43 @@ moe_status_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, const flo
                      stream);
 }
 
+size_t ffn_fp8_workspace_bytes(int A_max, int f, bool fp8_down) {
+  size_t b = align_up((size_t)A_max * f * 2, 256);                 // h, bf16
+  if (fp8_down)
+    b += align_up((size_t)A_max * f, 256) + align_up((size_t)A_max * 4, 256);  // hq, its scales
+  return b;
+}
+
 // The same with E4M3 gate/up: xq_perm [A_max, d] E4M3 token rows (scale of
 // permuted row p: x_scale[perm_token[p]]), Wq_gate / Wq_up [N, f, d] E4M3
-// with channel scales [N, f]; h and the down projection stay bf16.
+// with channel scales [N, f]; h is written in bf16.  The down projection is
+// bf16 from W_down, or, with Wq_down [N, d, f] and its channel scales [N, d],
+// E4M3 on h quantised per row (rows past offsets[N] left alone).
 moe_status_t launch_ffn_tc_fp8(const void *xq_perm, const float *x_scale,
                                const int32_t *perm_token, const int32_t *offsets,
                                const float *row_scale, int A_max, int d, int f, int N,
                                int capacity, const void *Wq_gate, const float *sw_gate,
-                               const void *Wq_up, const float *sw_up, const void *W_down, void *h,
+                               const void *Wq_up, const float *sw_up, const void *W_down,
+                               const void *Wq_down, const float *sw_down, void *workspace,
                                void *y_perm, int32_t *device_status, cudaStream_t stream) {
   if (A_max == 0) return MOE_OK;
   moe_status_t s = check_ffn_launch(N);
   if (s != MOE_OK) return s;
+  char *ws = static_cast<char *>(workspace);
+  void *h = ws;
+  uint8_t *hq = reinterpret_cast<uint8_t *>(ws + align_up((size_t)A_max * f * 2, 256));
+  float *hs = reinterpret_cast<float *>(reinterpret_cast<char *>(hq) +
+                                        align_up((size_t)A_max * f, 256));
   CUtensorMap wg, wu, bx[kNumBoxes];
   bool ok = make_weight_map_k8(&wg, Wq_gate, N, f, d) && make_weight_map_k8(&wu, Wq_up, N, f, d);
   const int box_rows[kNumBoxes] = {32, 64, 80, 128};
   for (int i = 0; i < kNumBoxes; ++i)
     ok = ok && make_rows_map_u8(&bx[i], xq_perm, A_max, d, box_rows[i]);
+  CUtensorMap wd, bh[kNumBoxes];
+  if (Wq_down) {
+    ok = ok && make_weight_map_k8(&wd, Wq_down, N, d, f);
+    for (int i = 0; i < kNumBoxes; ++i) ok = ok && make_rows_map_u8(&bh[i], hq, A_max, f, box_rows[i]);
+  }
   if (!ok) {
     set_error("tensor map encoding failed (alignment or size)");
     return MOE_ERR_INVALID_ARG;
@@ -879,8 +903,15 @@ moe_status_t launch_ffn_tc_fp8(const void *xq_perm, const float *x_scale,
               sw_gate, sw_up, x_scale, perm_token};
   s = launch_gemm<true>(wg, wu, bx, p1, stream);
   if (s != MOE_OK) return s;
-  return launch_down(offsets, row_scale, A_max, d, f, N, c, W_down, h, y_perm, device_status,
-                     stream);
+  if (!Wq_down)
+    return launch_down(offsets, row_scale, A_max, d, f, N, c, W_down, h, y_perm, device_status,
+                       stream);
+  s = launch_quantize_rows_e4m3(h, A_max, f, hq, hs, stream, offsets + N);
+  if (s != MOE_OK) return s;
+  TcParams p2{offsets, N, f, d, (d + 255) / 256, 0, static_cast<__nv_bfloat16 *>(y_perm), d,
+              row_scale, device_status, raster_group(f), c.tile_cap, c.wide, c.stages,
+              c.stage_bytes, sw_down, nullptr, hs, nullptr};
+  return launch_gemm<true>(wd, wd, bh, p2, stream);
 }
 
 }  // namespace moe

@@ -119,7 +119,8 @@ ForwardLayout layout_forward(const moe_forward_args *a, void *ws) {
     L.xs = c.take<float>(a->T);
   }
   L.y_perm = c.take_bytes((size_t)A_max * a->d * es);
-  L.ffn_ws = c.take_bytes(ffn_workspace_bytes((int)A_max, a->d, a->f, a->N, a->dtype));
+  L.ffn_ws = c.take_bytes(a->Wq_gate ? ffn_fp8_workspace_bytes((int)A_max, a->f, a->Wq_down != nullptr)
+                                     : ffn_workspace_bytes((int)A_max, a->d, a->f, a->N, a->dtype));
   L.perm_ws = c.take_bytes(permute_workspace_bytes(a->T, a->N, a->k));
   if (a->reroute_rounds > 0) {
     const size_t tkr = (size_t)a->T * (a->k + a->reroute_rounds);
@@ -310,24 +311,34 @@ moe_status_t moe_quantize_rows_e4m3(const void *x, int R, int C, uint8_t *q, flo
   return launch_quantize_rows_e4m3(x, R, C, q, scale, static_cast<cudaStream_t>(stream));
 }
 
+size_t moe_expert_ffn_fp8_workspace_size(int A_max, int d, int f, int N, int fp8_down) {
+  if (A_max < 0 || d < 1 || f < 1 || N < 1) return 0;
+  return ffn_fp8_workspace_bytes(A_max, f, fp8_down != 0);
+}
+
 moe_status_t moe_expert_ffn_fp8(const uint8_t *xq_perm, const float *x_scale,
                                 const int32_t *perm_token, const int32_t *offsets,
                                 const float *row_scale, int A_max, int d, int f, int N,
                                 const uint8_t *Wq_gate, const float *wscale_gate,
                                 const uint8_t *Wq_up, const float *wscale_up,
-                                const void *W_down, void *y_perm, int32_t *device_status,
-                                void *workspace, size_t workspace_bytes, void *stream) {
-  CHECK_ARG(A_max >= 0 && d >= 16 && f >= 8 && N >= 1, "bad sizes A_max=%d d=%d f=%d N=%d",
+                                const void *W_down, const uint8_t *Wq_down,
+                                const float *wscale_down, void *y_perm,
+                                int32_t *device_status, void *workspace,
+                                size_t workspace_bytes, void *stream) {
+  CHECK_ARG(A_max >= 0 && d >= 16 && f >= 16 && N >= 1, "bad sizes A_max=%d d=%d f=%d N=%d",
             A_max, d, f, N);
   CHECK_ARG(d % 16 == 0 && f % 8 == 0, "d=%d must be a multiple of 16 and f=%d of 8", d, f);
-  CHECK_ARG(offsets && Wq_gate && Wq_up && wscale_gate && wscale_up && W_down,
+  CHECK_ARG(!Wq_down || f % 16 == 0, "an E4M3 down projection needs f %% 16 == 0 (f=%d)", f);
+  CHECK_ARG(offsets && Wq_gate && Wq_up && wscale_gate && wscale_up,
             "required pointer is NULL");
+  CHECK_ARG(Wq_down ? wscale_down != nullptr : W_down != nullptr,
+            "the down projection needs W_down, or Wq_down with wscale_down");
   CHECK_ARG(A_max == 0 || (xq_perm && x_scale && perm_token && y_perm),
             "required pointer is NULL");
   CHECK_ARG(aligned16(xq_perm) && aligned16(y_perm) && aligned16(Wq_gate) && aligned16(Wq_up) &&
-                aligned16(W_down),
+                aligned16(W_down) && aligned16(Wq_down),
             "tensors must be 16-byte aligned");
-  size_t need = ffn_workspace_bytes(A_max, d, f, N, MOE_BF16);
+  size_t need = ffn_fp8_workspace_bytes(A_max, f, Wq_down != nullptr);
   if (need > 0 && (!workspace || workspace_bytes < need)) {
     set_error("moe_expert_ffn_fp8: workspace %zu bytes, needs %zu", workspace_bytes, need);
     return MOE_ERR_WORKSPACE;
@@ -335,8 +346,8 @@ moe_status_t moe_expert_ffn_fp8(const uint8_t *xq_perm, const float *x_scale,
   moe_status_t s = check_device();
   if (s != MOE_OK) return s;
   return launch_ffn_tc_fp8(xq_perm, x_scale, perm_token, offsets, row_scale, A_max, d, f, N, 0,
-                           Wq_gate, wscale_gate, Wq_up, wscale_up, W_down, workspace, y_perm,
-                           device_status, static_cast<cudaStream_t>(stream));
+                           Wq_gate, wscale_gate, Wq_up, wscale_up, W_down, Wq_down, wscale_down,
+                           workspace, y_perm, device_status, static_cast<cudaStream_t>(stream));
 }
 
 size_t moe_permute_reroute_workspace_size(int T, int N, int k, int R) {
@@ -426,8 +437,11 @@ static moe_status_t validate_forward(const moe_forward_args *a) {
   CHECK_ARG(a->d % 8 == 0 && a->f % 8 == 0, "d=%d and f=%d must be multiples of 8", a->d, a->f);
   CHECK_ARG(a->fs >= 0 && a->fs % 8 == 0, "fs=%d must be a non-negative multiple of 8", a->fs);
   const bool fp8 = a->Wq_gate || a->Wq_up || a->wscale_gate || a->wscale_up;
-  CHECK_ARG(a->x && a->W_g && (fp8 || (a->W_gate && a->W_up)) && a->W_down && a->y,
+  CHECK_ARG(a->x && a->W_g && (fp8 || (a->W_gate && a->W_up)) && (a->W_down || a->Wq_down) &&
+                a->y,
             "required pointer is NULL");
+  CHECK_ARG(!a->Wq_down || (fp8 && a->wscale_down && a->f % 16 == 0 && aligned16(a->Wq_down)),
+            "an E4M3 down projection needs the E4M3 gate/up, wscale_down and f %% 16 == 0");
   if (fp8) {
     CHECK_ARG(a->Wq_gate && a->Wq_up && a->wscale_gate && a->wscale_up,
               "FP8 gate/up needs Wq_gate, Wq_up, wscale_gate and wscale_up");
@@ -515,7 +529,8 @@ moe_status_t moe_forward(const moe_forward_args *a, void *workspace, size_t work
     if (s != MOE_OK) return s;
     s = launch_ffn_tc_fp8(L.x_perm, L.xs, L.perm_token, L.offsets, L.row_scale, A_max, a->d,
                           a->f, a->N, cap, a->Wq_gate, a->wscale_gate, a->Wq_up, a->wscale_up,
-                          a->W_down, L.ffn_ws, L.y_perm, a->device_status, stream);
+                          a->W_down, a->Wq_down, a->wscale_down, L.ffn_ws, L.y_perm,
+                          a->device_status, stream);
   } else {
     s = launch_expert_ffn(L.x_perm, L.offsets, L.row_scale, A_max, a->d, a->f, a->N, cap,
                           a->dtype, a->W_gate, a->W_up, a->W_down, L.y_perm, a->device_status,

@@ -101,15 +101,18 @@ moe_status_t launch_copy_row_bytes(const void *x, size_t row_bytes, const int32_
 // FP8 E4M3 with absmax scales: rows of x [R, C] bf16 -> codes [R, C] + [R]
 // scales; gate/up weights W [N, d, f] bf16 -> codes [N, f, d] + [N, f].
 moe_status_t launch_quantize_rows_e4m3(const void *x, int R, int C, uint8_t *q, float *scale,
-                                       cudaStream_t stream);
+                                       cudaStream_t stream, const int32_t *rows_valid = nullptr);
 moe_status_t launch_quantize_weights_e4m3(const void *W, int N, int d, int f, uint8_t *q,
                                           float *scale, cudaStream_t stream);
-// Expert FFN with E4M3 gate/up (see ffn_tc.cu).
+// Expert FFN with E4M3 gate/up and, when Wq_down is given, E4M3 down (see
+// ffn_tc.cu).  Workspace: ffn_fp8_workspace_bytes.
+size_t ffn_fp8_workspace_bytes(int A_max, int f, bool fp8_down);
 moe_status_t launch_ffn_tc_fp8(const void *xq_perm, const float *x_scale,
                                const int32_t *perm_token, const int32_t *offsets,
                                const float *row_scale, int A_max, int d, int f, int N,
                                int capacity, const void *Wq_gate, const float *sw_gate,
-                               const void *Wq_up, const float *sw_up, const void *W_down, void *h,
+                               const void *Wq_up, const float *sw_up, const void *W_down,
+                               const void *Wq_down, const float *sw_down, void *workspace,
                                void *y_perm, int32_t *device_status, cudaStream_t stream);
 
 size_t ffn_workspace_bytes(int A_max, int d, int f, int N, moe_dtype_t dtype);

@@ -7,12 +7,14 @@
 // compressed to fewer bits to shrink memory).
 //
 // Reading (the pages name the idea, not a format): OCP FP8 E4M3 (bias 7, 3
-// mantissa bits, largest finite 448, no infinities).  A vector v -- one token
-// row of x over d, or one output channel of a gate/up matrix over d -- is
+// mantissa bits, largest finite 448, no infinities).  A vector v -- one row
+// of x (or of h) over its length, or one output channel of a weight matrix
+// over its reduction dim -- is
 // stored as q = E4M3(v * (448 / amax|v|)) (round to nearest even, saturated)
 // and one fp32 scale amax / 448; both factors are formed in fp32 (an all-zero
-// vector takes scale 1).  Weights are written channel-major, [N, f, d], so
-// the FP8 GEMM reads both operands K-major.
+// vector takes scale 1).  Weights W [N, K, M] (K the reduction dim) are
+// written channel-major, [N, M, K], so the FP8 GEMM reads both operands
+// K-major: gate/up [N, d, f] -> [N, f, d], down [N, f, d] -> [N, d, f].
 #include <cuda_fp8.h>
 
 #include "moe_internal.cuh"
@@ -24,41 +26,63 @@ __device__ __forceinline__ uint8_t to_e4m3(float v) {
   return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
 }
 
-// One warp per row (grid-stride over rows); C % 8 == 0, 16-byte rows.
+// G threads per row (G a power of two, 32..256; 256 / G rows per CTA,
+// grid-stride over row batches); C % 8 == 0, 16-byte rows.  With rows_valid,
+// rows from *rows_valid on are left alone.
 __global__ void __launch_bounds__(256) quantize_rows_e4m3(const __nv_bfloat16 *__restrict__ x,
-                                                          int R, int C, uint8_t *__restrict__ q,
-                                                          float *__restrict__ scale) {
-  const int lane = threadIdx.x % 32;
-  const int warps = blockDim.x / 32;
+                                                          int R, int C, int G,
+                                                          uint8_t *__restrict__ q,
+                                                          float *__restrict__ scale,
+                                                          const int32_t *__restrict__ rows_valid) {
+  __shared__ float red[8];                     // one per warp
+  const int lg = threadIdx.x % G;              // thread within the row's group
+  const int grp = threadIdx.x / G;
+  const int rpc = blockDim.x / G;              // rows per CTA
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nv = C / 8;
-  for (long r = (long)blockIdx.x * warps + threadIdx.x / 32; r < R; r += (long)gridDim.x * warps) {
-    const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)r * C);
+  if (rows_valid) R = min(R, *rows_valid);
+  for (long b = blockIdx.x; b * rpc < R; b += gridDim.x) {
+    const long r = b * rpc + grp;
+    const bool active = r < R;
+    const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)(active ? r : 0) * C);
     float am = 0.f;
-    for (int v = lane; v < nv; v += 32) {
-      float f[8];
-      load8(reinterpret_cast<const __nv_bfloat16 *>(row + v), f);
+    if (active)
+      for (int v = lg; v < nv; v += G) {
+        float f[8];
+        load8(reinterpret_cast<const __nv_bfloat16 *>(row + v), f);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
-    }
+        for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
+      }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    if (G > 32) {                              // combine the group's warps
+      if (lane == 0) red[warp] = am;
+      __syncthreads();
+      const int w0 = (grp * G) / 32;
+      am = 0.f;
+      for (int w = 0; w < G / 32; ++w) am = fmaxf(am, red[w0 + w]);
+      __syncthreads();
+    }
     const float inv = am > 0.f ? 448.0f / am : 1.0f;
-    if (lane == 0) scale[r] = am > 0.f ? am / 448.0f : 1.0f;
-    uint2 *out = reinterpret_cast<uint2 *>(q + (size_t)r * C);
-    for (int v = lane; v < nv; v += 32) {
-      float f[8];
-      load8(reinterpret_cast<const __nv_bfloat16 *>(row + v), f);
-      uint32_t w[2] = {0u, 0u};
+    if (active && lg == 0) scale[r] = am > 0.f ? am / 448.0f : 1.0f;
+    if (active) {
+      uint2 *out = reinterpret_cast<uint2 *>(q + (size_t)r * C);
+      for (int v = lg; v < nv; v += G) {
+        float f[8];
+        load8(reinterpret_cast<const __nv_bfloat16 *>(row + v), f);
+        uint32_t w[2] = {0u, 0u};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) w[i / 4] |= (uint32_t)to_e4m3(f[i] * inv) << (8 * (i % 4));
-      out[v] = make_uint2(w[0], w[1]);
+        for (int i = 0; i < 8; ++i) w[i / 4] |= (uint32_t)to_e4m3(f[i] * inv) << (8 * (i % 4));
+        out[v] = make_uint2(w[0], w[1]);
+      }
     }
   }
 }
 
-// Block (32 output channels, expert e): the channels' absmax over d, then the
-// codes in tiles of 128 d, transposed through shared memory so each channel's
-// 128 bytes leave as eight 16-byte stores.  d % 16 == 0.
+// W [N, d, f] viewed as [N, K = d, M = f].  Block (32 output channels, expert
+// e): the channels' absmax over d, then the codes in tiles of 128 d,
+// transposed through shared memory so each channel's 128 bytes leave as eight
+// 16-byte stores.  d % 16 == 0.
 constexpr int kQCols = 32;
 constexpr int kQRows = 128;
 __global__ void __launch_bounds__(256) quantize_weights_e4m3(
@@ -101,12 +125,17 @@ __global__ void __launch_bounds__(256) quantize_weights_e4m3(
 }  // namespace
 
 moe_status_t launch_quantize_rows_e4m3(const void *x, int R, int C, uint8_t *q, float *scale,
-                                       cudaStream_t stream) {
+                                       cudaStream_t stream, const int32_t *rows_valid) {
   if (R == 0) return MOE_OK;
-  long grid = ((long)R + 7) / 8;
-  if (grid > 148L * 16) grid = 148L * 16;
+  // threads per row: enough for a few 16-byte vectors each, 32..256
+  const int nv = C / 8;
+  int G = 32;
+  while (G < 256 && G * 4 < nv) G *= 2;
+  const long rpc = 256 / G;
+  long grid = ((long)R + rpc - 1) / rpc;
+  if (grid > 148L * 8) grid = 148L * 8;
   quantize_rows_e4m3<<<(int)grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(x), R, C,
-                                                    q, scale);
+                                                    G, q, scale, rows_valid);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

@@ -53,15 +53,15 @@ class Work:
     flop_ffn: float
 
 
-def layer_work(T, d, f, N, k, A, touched, fs=0, esize=2, fp8_gate_up=False):
+def layer_work(T, d, f, N, k, A, touched, fs=0, esize=2, fp8_gate_up=False, fp8_down=False):
     """Algorithmic work of one forward: A kept rows, `touched` experts with >=1 row.
-    fp8_gate_up: the routed gate/up weights are 1-byte E4M3 codes plus one fp32
-    scale per output channel (the down projection keeps `esize`)."""
+    fp8_gate_up / fp8_down: those routed weights are 1-byte E4M3 codes plus one
+    fp32 scale per output channel (the others keep `esize`)."""
     flop_router = 2.0 * T * d * N
     flop_ffn = 6.0 * d * f * A
     flop_shared = 6.0 * d * fs * T
-    per_expert = (2 * d * f * 1 + 2 * f * 4 + d * f * esize) if fp8_gate_up \
-        else expert_params(d, f) * esize
+    per_expert = ((2 * d * f + 2 * f * 4) if fp8_gate_up else 2 * d * f * esize) + \
+        ((d * f + d * 4) if fp8_down else d * f * esize)
     wbytes = touched * per_expert + d * N * esize + expert_params(d, fs) * esize
     # x read twice (router, gather), x_perm written+read, h written+read (gate/up -> down),
     # y_perm written+read, y written in fp32 (+ shared y written + read)

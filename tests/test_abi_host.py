@@ -107,10 +107,17 @@ def test_stage_entry_points_reject_bad_arguments(lib):
     assert lib.moe_quantize_rows_e4m3(4096, 4, 40, 4096, 4096, None) == 1
     assert lib.moe_quantize_rows_e4m3(4096, 4, 64, 4096, None, None) == 1
     p = 4096
-    assert lib.moe_expert_ffn_fp8(p, p, p, p, None, 8, 64, 64, 2, p, None, p, p, p, p, None, p,
-                                  1 << 30, None) == 1
-    assert lib.moe_expert_ffn_fp8(p, p, p, p, None, 8, 64, 64, 2, p, p, p, p, p, p, None, p,
-                                  16, None) == 3
+    assert lib.moe_expert_ffn_fp8(p, p, p, p, None, 8, 64, 64, 2, p, None, p, p, p, None, None,
+                                  p, None, p, 1 << 30, None) == 1
+    assert lib.moe_expert_ffn_fp8(p, p, p, p, None, 8, 64, 64, 2, p, p, p, p, p, None, None, p,
+                                  None, p, 16, None) == 3
+    # E4M3 down projection: scales missing; f not a multiple of 16
+    assert lib.moe_expert_ffn_fp8(p, p, p, p, None, 8, 64, 64, 2, p, p, p, p, None, p, None, p,
+                                  None, p, 1 << 30, None) == 1
+    assert lib.moe_expert_ffn_fp8(p, p, p, p, None, 8, 64, 72, 2, p, p, p, p, None, p, p, p,
+                                  None, p, 1 << 30, None) == 1
+    assert (lib.moe_expert_ffn_fp8_workspace_size(100, 64, 64, 4, 1) >
+            lib.moe_expert_ffn_fp8_workspace_size(100, 64, 64, 4, 0))
     # combine: d not a multiple of 8
     assert lib.moe_combine(4096, 1, 4096, 4, 2, 60, None, 4096, 0, None) == 1
     assert "d=60" in B.lib().moe_last_error().decode()

@@ -59,19 +59,22 @@ def test_quantize_weights_bit_exact(N, d, f):
 
 
 def _fp8_fetch(inp, qw):
-    (qg, sg), (qu, su) = qw
+    (qg, sg), (qu, su) = qw[:2]
+    qd = qw[2] if len(qw) > 2 else None
 
     def fetch(e):
-        return qg[e], sg[e], qu[e], su[e], inp.W_down[e].cpu()
+        w = (qg[e], sg[e], qu[e], su[e], inp.W_down[e].cpu())
+        return w if qd is None else w + (qd[0][e], qd[1][e])
     return fetch
 
 
+@pytest.mark.parametrize("down", [False, True], ids=["bf16_down", "fp8_down"])
 @pytest.mark.parametrize("counts", [
     [0, 1, 256, 257, 288, 320, 321, 600, 641, 100, 0, 960],
     [0, 1, 160, 161, 255, 256, 257, 288, 320, 321, 600, 641, 100, 0, 960, 200],
     [3, 17, 64, 0, 31],
 ])
-def test_expert_ffn_fp8_crafted_counts(counts):
+def test_expert_ffn_fp8_crafted_counts(counts, down):
     """FP8 gate/up on expert sizes at every tiling edge (empty, one row, one
     and two sub-tiles, experts split into several tiles), tokens repeated in
     any order, against the oracle's fp64 expert on the same E4M3 values."""
@@ -89,33 +92,36 @@ def test_expert_ffn_fp8_crafted_counts(counts):
     qx, sx = oracle.quantize_rows_e4m3(x)
     (qg, sg), (qu, su) = oracle.quantize_weights_e4m3(Wg), oracle.quantize_weights_e4m3(Wu)
     ptn = pt.numpy()
-    y = B.moe_expert_ffn_fp8(torch.from_numpy(qx[ptn]).cuda(), torch.from_numpy(sx).cuda(),
-                             pt.cuda(), torch.from_numpy(off).cuda(), torch.from_numpy(qg).cuda(),
-                             torch.from_numpy(sg).cuda(), torch.from_numpy(qu).cuda(),
-                             torch.from_numpy(su).cuda(), Wd.cuda(), row_scale=rs.cuda(),
-                             A_max=A)
+    qd, sd = oracle.quantize_weights_e4m3(Wd) if down else (None, None)
+    gpu = lambda a: None if a is None else torch.from_numpy(a).cuda()
+    y = B.moe_expert_ffn_fp8(gpu(qx[ptn]), gpu(sx), pt.cuda(), gpu(off), gpu(qg), gpu(sg),
+                             gpu(qu), gpu(su), W_down=None if down else Wd.cuda(),
+                             Wq_down=gpu(qd), wscale_down=gpu(sd), row_scale=rs.cuda(), A_max=A)
     torch.cuda.synchronize()
     ref = np.zeros((A, d))
     for e in range(N):
         if counts[e]:
             rows = ptn[off[e]:off[e + 1]]
-            ref[off[e]:off[e + 1]] = oracle.expert_rows_fp8(qg[e], sg[e], qu[e], su[e], Wd[e],
-                                                            qx[rows], sx[rows])
+            ref[off[e]:off[e + 1]] = oracle.expert_rows_fp8(
+                qg[e], sg[e], qu[e], su[e], Wd[e], qx[rows], sx[rows],
+                None if qd is None else qd[e], None if sd is None else sd[e])
     ref *= rs.double().numpy()[:, None]
     parity.assert_y_close(y[:A].float().cpu().numpy(), ref, "bf16")
 
 
-def _check_fp8_layer(cfg, inp, rows=None):
+def _check_fp8_layer(cfg, inp, rows=None, down=False):
     layer = B.MoELayer(inp.W_g, inp.W_gate, inp.W_up, inp.W_down, cfg.k, bias=inp.bias,
                        Ws_gate=inp.Ws_gate, Ws_up=inp.Ws_up, Ws_down=inp.Ws_down,
-                       capacity_factor=cfg.cf, fp8=True)
+                       capacity_factor=cfg.cf, fp8=True, fp8_down=down)
     y = layer(inp.x)
     torch.cuda.synchronize()
     out = layer.last
     assert int(out["device_status"].item()) == 0
     # the layer's quantised weights are the oracle's, byte for byte
     qw = [oracle.quantize_weights_e4m3(inp.W_gate.cpu()), oracle.quantize_weights_e4m3(inp.W_up.cpu())]
-    for (qo, so), i in zip(qw, (0, 2)):
+    if down:
+        qw.append(oracle.quantize_weights_e4m3(inp.W_down.cpu()))
+    for (qo, so), i in zip(qw, (0, 2, 4)):
         np.testing.assert_array_equal(layer.fp8[i].cpu().numpy(), qo)
         np.testing.assert_array_equal(layer.fp8[i + 1].cpu().numpy(), so)
     x_c = inp.x.cpu()
@@ -145,25 +151,29 @@ def _check_fp8_layer(cfg, inp, rows=None):
     y_b = oracle.forward_rows(x_c[torch.as_tensor(sel)], idx_o[sel], w_o[sel],
                               g_o["inv_pos"][sel], parity.fetcher(inp), shared=shared)
     q_err = float(np.linalg.norm(y_g - y_b) / max(np.linalg.norm(y_b), 1e-30))
-    assert q_err < 0.1, f"FP8 layer {q_err:.3f} (rel-fro) away from the bf16 layer"
+    assert q_err < (0.15 if down else 0.1), f"FP8 layer {q_err:.3f} (rel-fro) away from the bf16 layer"
     return dict(max_abs=max_abs, rel_fro=fro, fp8_vs_bf16_rel_fro=q_err, rows=len(sel))
 
 
+@pytest.mark.parametrize("down", [False, True], ids=["bf16_down", "fp8_down"])
 @pytest.mark.parametrize("name", list(SMALL))
-def test_layer_fp8_reduced(name):
+def test_layer_fp8_reduced(name, down):
     cfg = SMALL[name]
+    if down and cfg.f % 16:
+        pytest.skip("an E4M3 down projection needs f % 16 == 0")
     inp = make_inputs(cfg, device=torch.device("cuda"))
-    print(name, _check_fp8_layer(cfg, inp))
+    print(name, down, _check_fp8_layer(cfg, inp, down=down))
 
 
+@pytest.mark.parametrize("down", [False, True], ids=["bf16_down", "fp8_down"])
 @pytest.mark.parametrize("name,rows", [("mixtral_decode", None), ("capacity", 256)])
-def test_layer_fp8_full_size(name, rows):
+def test_layer_fp8_full_size(name, rows, down):
     cfg = CONFIGS[name]
     inp = make_inputs(cfg, device=torch.device("cuda"))
     sel = None
     if rows is not None:
         sel = np.sort(np.random.default_rng(cfg.seed).choice(cfg.T, size=rows, replace=False))
-    print(name, _check_fp8_layer(cfg, inp, sel))
+    print(name, down, _check_fp8_layer(cfg, inp, sel, down=down))
     del inp
     torch.cuda.empty_cache()
 

@@ -661,3 +661,49 @@ def test_fp8_expert_equals_bf16_expert_on_representable_values():
     qw = [oracle.quantize_weights_e4m3(W[None]) for W in Ws]
     got = oracle.expert_rows_fp8(qw[0][0][0], qw[0][1][0], qw[1][0][0], qw[1][1][0], Wd, qx, sxq)
     np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_expert_hidden_is_the_first_half_of_the_expert():
+    """h = SiLU(x W_gate) * (x W_up) from the hidden-activation function, times
+    W_down, is the whole expert (pinned above by its closed forms)."""
+    g = torch.Generator().manual_seed(9)
+    d, f, R = 24, 40, 7
+    Wg, Wu = torch.randn(d, f, generator=g), torch.randn(d, f, generator=g)
+    Wd = torch.randn(f, d, generator=g)
+    x = torch.randn(R, d, generator=g)
+    h = oracle.expert_hidden(Wg, Wu, x)
+    np.testing.assert_allclose(h @ Wd.double().numpy(), oracle.expert_rows(Wg, Wu, Wd, x),
+                               rtol=1e-12, atol=1e-12)
+    # closed form on one element: x = e_0, so g = Wg[0], u = Wu[0]
+    e0 = torch.zeros(1, d)
+    e0[0, 0] = 1
+    gv, uv = Wg[0].double().numpy(), Wu[0].double().numpy()
+    np.testing.assert_allclose(oracle.expert_hidden(Wg, Wu, e0)[0], gv / (1 + np.exp(-gv)) * uv,
+                               rtol=1e-14)
+
+
+def test_fp8_down_projection_uses_channel_and_row_scales():
+    """An E4M3 down projection with exactly representable W_down equals the
+    down projection of the quantised h (bf16-rounded, per-row E4M3) with W_down
+    itself; scales on the wrong axis would not."""
+    rng = np.random.default_rng(23)
+    R, d, f = 6, 32, 48
+    x = torch.from_numpy(rng.normal(size=(R, d))).to(torch.bfloat16)
+    Wg = torch.from_numpy(rng.normal(size=(d, f)) / d ** 0.5).to(torch.bfloat16)
+    Wu = torch.from_numpy(rng.normal(size=(d, f)) / d ** 0.5).to(torch.bfloat16)
+    cd = rng.integers(0, 0x7E, size=(d, f)).astype(np.uint8) | \
+        (rng.integers(0, 2, size=(d, f)).astype(np.uint8) << 7)
+    cd[:, 1] = 0x7E
+    sd = 2.0 ** rng.integers(-12, -8, size=d)
+    Wd = torch.from_numpy((oracle.e4m3_decode(cd) * sd[:, None]).T.copy()).to(torch.bfloat16)
+    qx, sx = oracle.quantize_rows_e4m3(x)
+    (qg, sg), (qu, su) = oracle.quantize_weights_e4m3(Wg[None]), oracle.quantize_weights_e4m3(Wu[None])
+    (qd, sdq) = oracle.quantize_weights_e4m3(Wd[None])
+    np.testing.assert_array_equal(qd[0], cd)
+    got = oracle.expert_rows_fp8(qg[0], sg[0], qu[0], su[0], Wd, qx, sx, qd[0], sdq[0])
+    h = oracle.expert_hidden(np.ascontiguousarray(oracle.dequantize_e4m3(qg[0], sg[0]).T),
+                             np.ascontiguousarray(oracle.dequantize_e4m3(qu[0], su[0]).T),
+                             oracle.dequantize_e4m3(qx, sx))
+    qh, sh = oracle.quantize_rows_e4m3(torch.from_numpy(h).to(torch.bfloat16))
+    ref = oracle.dequantize_e4m3(qh, sh) @ Wd.double().numpy()
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)

@@ -50,6 +50,7 @@ MUTANTS = [
      "const int e = cand[(size_t)t * kr + j];\n        final_w"),
     ("e4m3_ties_to_odd", "else c = (lo & 1) == 0 ? lo : hi;", "else c = (lo & 1) == 0 ? hi : lo;"),
     ("e4m3_round_down", "if (dlo < dhi) c = lo;", "if (dlo <= 2 * dhi) c = lo;"),
+    ("hidden_silu_sign", "h[j] = g / (1.0 + exp(-g)) * u;", "h[j] = g / (1.0 + exp(g)) * u;"),
     ("e4m3_subnormal_exponent", "ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
     ("e4m3_bias_8", "ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
     ("fp8_scale_inverted", "*scale = amax > 0.0f ? amax / 448.0f : 1.0f;",
