@@ -1,8 +1,8 @@
 """Seeded sweep of random layer shapes through moe_forward against the oracle.
 
 Each case draws d, f (multiples of 8), N, k, T, a router bias, and with some
-probability a shared expert, a capacity factor, overflow re-routing and a
-bf16 output, so that tile tails, narrow and wide token tiles, the one-chunk
+probability a shared expert, a capacity factor, overflow re-routing, a
+bf16 output and FP8 E4M3 expert weights (gate/up, or all three), so that tile tails, narrow and wide token tiles, the one-chunk
 dispatch, capacity drops and re-routing rounds meet in combinations the
 fixed configurations do not.  Every expected value comes from the oracle on
 the case's own inputs."""
@@ -34,19 +34,22 @@ def _case(i):
     R = int(rng.integers(1, 3)) if cf > 0 and rng.random() < 0.5 and k + 2 <= N else 0
     bias = float(rng.choice([0.0, 0.5, 1.0]))
     y_bf16 = bool(rng.random() < 0.25)
+    fp8 = bool(d % 16 == 0 and rng.random() < 0.35)
+    fp8_down = bool(fp8 and f % 16 == 0 and rng.random() < 0.5)
     cfg = MoEConfig(f"sweep{i}", T=T, d=d, f=f, N=N, k=k, fs=fs, cf=cf, bias_std=bias,
                     seed=2000 + i)
-    return cfg, R, y_bf16
+    return cfg, R, y_bf16, fp8, fp8_down
 
 
 @pytest.mark.parametrize("i", range(CASES))
 def test_random_layer(i):
-    cfg, R, y_bf16 = _case(i)
+    cfg, R, y_bf16, fp8, fp8_down = _case(i)
     inp = make_inputs(cfg, device="cuda")
     y_dtype = torch.bfloat16 if y_bf16 else torch.float32
     layer = B.MoELayer(inp.W_g, inp.W_gate, inp.W_up, inp.W_down, cfg.k, bias=inp.bias,
                        Ws_gate=inp.Ws_gate, Ws_up=inp.Ws_up, Ws_down=inp.Ws_down,
-                       capacity_factor=cfg.cf, y_dtype=y_dtype, reroute_rounds=R)
+                       capacity_factor=cfg.cf, y_dtype=y_dtype, reroute_rounds=R,
+                       fp8=fp8, fp8_down=fp8_down)
     y = layer(inp.x)
     torch.cuda.synchronize()
     out = layer.last
@@ -88,7 +91,21 @@ def test_random_layer(i):
     if cfg.fs:
         shared = (inp.Ws_gate.cpu(), inp.Ws_up.cpu(), inp.Ws_down.cpu())
     idx_safe = np.where(idx_f >= 0, idx_f, 0)
-    y_o = oracle.forward_rows(x_c, idx_safe, w_f, g["inv_pos"], parity.fetcher(inp), shared=shared)
+    if fp8:
+        # the oracle's own E4M3 codes of x and of the expert weights
+        qx, sx = oracle.quantize_rows_e4m3(x_c)
+        qg, sg = oracle.quantize_weights_e4m3(inp.W_gate.cpu())
+        qu, su = oracle.quantize_weights_e4m3(inp.W_up.cpu())
+        qd, sd = oracle.quantize_weights_e4m3(inp.W_down.cpu()) if fp8_down else (None, None)
+
+        def fetch(e):
+            w = (qg[e], sg[e], qu[e], su[e], inp.W_down[e].cpu())
+            return w if qd is None else w + (qd[e], sd[e])
+        y_o = oracle.forward_rows_fp8(qx, sx, idx_safe, w_f, g["inv_pos"], fetch, shared=shared,
+                                      x_rows=x_c)
+    else:
+        y_o = oracle.forward_rows(x_c, idx_safe, w_f, g["inv_pos"], parity.fetcher(inp),
+                                  shared=shared)
     y_g = y.float().cpu().numpy().astype(np.float64)
     if y_bf16:
         # a bf16 store adds up to half an ulp (2^-8 relative) on top of the
