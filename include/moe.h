@@ -319,6 +319,27 @@ moe_status_t moe_forward_host_io(const moe_forward_args *args,
                                  void *workspace, size_t workspace_bytes,
                                  void *stream);
 
+/* The host-buffer call with the copies overlapped with the layer: the T
+ * tokens run as `chunks` consecutive batches on `stream`; every chunk's x
+ * rows go host->device on h2d_stream (all issued at once, each batch waits
+ * for its own), and each batch's y rows go back on d2h_stream as soon as it
+ * is done; `stream` then waits for the last copy.  Each token's output row
+ * depends on that token alone, so y equals moe_forward_host_io's -- except
+ * under a capacity limit or re-routing, whose drops depend on the whole
+ * batch: there chunks is taken as 1.  chunks <= 0: moe_forward_overlap_chunks
+ * (as many as keep each batch's tensor work at least twice the time to
+ * stream its weights again, at most one per 2048 tokens, 16 in all).  The
+ * call returns y only: the routing outputs of args must be NULL.  Three
+ * distinct streams; workspace: moe_forward_workspace_size(args).  Pinned
+ * host memory makes the copies asynchronous. */
+int moe_forward_overlap_chunks(const moe_forward_args *args);
+moe_status_t moe_forward_host_io_overlapped(const moe_forward_args *args,
+                                            const void *x_host, void *y_host,
+                                            void *workspace,
+                                            size_t workspace_bytes, int chunks,
+                                            void *stream, void *h2d_stream,
+                                            void *d2h_stream);
+
 /* ---------------------------------------------------------------------------
  * Routing diagnostics (forward only): how evenly the router spreads the load.
  * Source: "MoE稀疏激活原理与工程实践", 4.2 路由质量诊断 (selection frequency of

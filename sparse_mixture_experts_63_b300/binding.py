@@ -26,6 +26,7 @@ EXPORTS = ("moe_status_string", "moe_last_error", "moe_version", "moe_launch_cou
            "moe_permute_noalloc",
            "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
            "moe_forward_workspace_size", "moe_forward", "moe_forward_host_io",
+           "moe_forward_overlap_chunks", "moe_forward_host_io_overlapped",
            "moe_routing_stats_workspace_size", "moe_routing_stats",
            "moe_permute_reroute_workspace_size", "moe_permute_reroute",
            "moe_quantize_weights_e4m3", "moe_quantize_rows_e4m3",
@@ -93,6 +94,10 @@ def lib():
         L.moe_forward_workspace_size.restype = sz
         L.moe_forward.argtypes = [ctypes.POINTER(moe_forward_args), vp, sz, vp]
         L.moe_forward_host_io.argtypes = [ctypes.POINTER(moe_forward_args), vp, vp, vp, sz, vp]
+        L.moe_forward_overlap_chunks.argtypes = [ctypes.POINTER(moe_forward_args)]
+        L.moe_forward_overlap_chunks.restype = ci
+        L.moe_forward_host_io_overlapped.argtypes = [ctypes.POINTER(moe_forward_args), vp, vp,
+                                                     vp, sz, ci, vp, vp, vp]
         L.moe_routing_stats_workspace_size.argtypes = [ci, ci]
         L.moe_routing_stats_workspace_size.restype = sz
         L.moe_routing_stats.argtypes = [vp, vp, ci, ci, vp, vp, vp, vp, sz, vp]
@@ -109,7 +114,7 @@ def lib():
         for n in ("moe_router_topk", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn",
                   "moe_quantize_weights_e4m3", "moe_quantize_rows_e4m3", "moe_expert_ffn_fp8",
                   "moe_combine", "moe_routing_stats", "moe_permute_reroute",
-                  "moe_forward", "moe_forward_host_io"):
+                  "moe_forward", "moe_forward_host_io", "moe_forward_host_io_overlapped"):
             getattr(L, n).restype = ci
         _lib = L
     return _lib
@@ -421,6 +426,28 @@ def moe_forward_host_io(args, x_host, y_host, workspace, stream=None):
     _check("moe_forward_host_io", lib().moe_forward_host_io(
         ctypes.byref(args), _p(x_host), _p(y_host), _p(workspace), workspace.numel(),
         _stream(stream)))
+
+
+_copy_streams = {}
+
+
+def moe_forward_host_io_overlapped(args, x_host, y_host, workspace, chunks=0, stream=None):
+    """moe_forward_host_io with the copies overlapped with the layer (token
+    chunks; see include/moe.h).  The two copy streams are the binding's own,
+    one pair per device."""
+    if x_host.is_cuda or y_host.is_cuda:
+        raise ValueError("x_host / y_host must be host tensors")
+    dev = torch.cuda.current_device()
+    if dev not in _copy_streams:
+        _copy_streams[dev] = (torch.cuda.Stream(), torch.cuda.Stream())
+    h2d, d2h = _copy_streams[dev]
+    _check("moe_forward_host_io_overlapped", lib().moe_forward_host_io_overlapped(
+        ctypes.byref(args), _p(x_host), _p(y_host), _p(workspace), workspace.numel(), int(chunks),
+        _stream(stream), _stream(h2d), _stream(d2h)))
+
+
+def moe_forward_overlap_chunks(args) -> int:
+    return int(lib().moe_forward_overlap_chunks(ctypes.byref(args)))
 
 
 class MoELayer:

@@ -167,6 +167,45 @@ moe_status_t validate_ffn(const void *x_perm, const int32_t *offsets, int A_max,
   return MOE_OK;
 }
 
+constexpr int kMaxChunks = 16;
+
+// Chunks for the overlapped host-buffer call: as many as keep each chunk's
+// tensor work at least twice its weight streaming (every chunk reads every
+// touched expert's weights again), at most one per 2048 tokens and 16 in all;
+// estimated with 274 FLOP per byte (dense bf16 rate over copy bandwidth).
+int auto_chunks(const moe_forward_args *a) {
+  const double kFlopPerByte = 274.0;
+  const double rows = (double)a->T * a->k;
+  const double flop = 6.0 * rows * a->d * a->f + 6.0 * (double)a->T * a->d * a->fs;
+  const double touched = rows < a->N ? rows : a->N;
+  const double bytes = esize(a->dtype) * (3.0 * a->d * a->f * touched + 3.0 * (double)a->d * a->fs);
+  int n = (int)(flop / (2.0 * bytes * kFlopPerByte));
+  const int by_tokens = a->T / 2048;
+  if (n > by_tokens) n = by_tokens;
+  if (n > kMaxChunks) n = kMaxChunks;
+  return n < 1 ? 1 : n;
+}
+
+// Events of the overlapped call (2 per chunk + 2), made once per thread and
+// device.
+moe_status_t chunk_events(cudaEvent_t **out) {
+  constexpr int kEv = 2 * kMaxChunks + 2;
+  thread_local cudaEvent_t ev[kMaxDevicesCached][kEv];
+  thread_local bool made[kMaxDevicesCached];
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevicesCached) {
+    set_error("device index %d above %d", dev, kMaxDevicesCached);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (!made[dev]) {
+    for (int i = 0; i < kEv; ++i)
+      MOE_CUDA_TRY(cudaEventCreateWithFlags(&ev[dev][i], cudaEventDisableTiming));
+    made[dev] = true;
+  }
+  *out = ev[dev];
+  return MOE_OK;
+}
+
 }  // namespace
 
 size_t ffn_workspace_bytes(int A_max, int d, int f, int N, moe_dtype_t dtype) {
@@ -562,6 +601,75 @@ moe_status_t moe_forward_host_io(const moe_forward_args *a, const void *x_host, 
   s = moe_forward(a, workspace, workspace_bytes, stream_);
   if (s != MOE_OK) return s;
   MOE_CUDA_TRY(cudaMemcpyAsync(y_host, a->y, yb, cudaMemcpyDeviceToHost, stream));
+  return MOE_OK;
+}
+
+int moe_forward_overlap_chunks(const moe_forward_args *a) {
+  if (validate_forward(a) != MOE_OK) return 0;
+  return auto_chunks(a);
+}
+
+moe_status_t moe_forward_host_io_overlapped(const moe_forward_args *a, const void *x_host,
+                                            void *y_host, void *workspace,
+                                            size_t workspace_bytes, int chunks, void *stream_,
+                                            void *h2d_stream_, void *d2h_stream_) {
+  moe_status_t s = validate_forward(a);
+  if (s != MOE_OK) return s;
+  CHECK_ARG(x_host && y_host, "host buffers are NULL");
+  CHECK_ARG(h2d_stream_ && d2h_stream_ && h2d_stream_ != stream_ && d2h_stream_ != stream_ &&
+                h2d_stream_ != d2h_stream_,
+            "three distinct streams are needed");
+  CHECK_ARG(!a->logits && !a->topk_idx && !a->topk_w && !a->counts && !a->offsets &&
+                !a->inv_pos && !a->dropped && !a->rerouted,
+            "the overlapped call returns y only: routing outputs must be NULL");
+  ForwardLayout need = layout_forward(a, nullptr);
+  if (!workspace || workspace_bytes < need.bytes) {
+    set_error("moe_forward_host_io_overlapped: workspace %zu bytes, needs %zu",
+              workspace_bytes, need.bytes);
+    return MOE_ERR_WORKSPACE;
+  }
+  if ((s = check_device()) != MOE_OK) return s;
+  int n = chunks > 0 ? chunks : auto_chunks(a);
+  if (a->capacity_factor > 0 || a->reroute_rounds > 0) n = 1;   // drops depend on the batch
+  if (n > kMaxChunks) n = kMaxChunks;
+  if (n > a->T) n = a->T;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  cudaStream_t h2d = static_cast<cudaStream_t>(h2d_stream_);
+  cudaStream_t d2h = static_cast<cudaStream_t>(d2h_stream_);
+  cudaEvent_t *ev = nullptr;
+  if ((s = chunk_events(&ev)) != MOE_OK) return s;   // [0] start, [1..n] h2d, [n+1..2n] layer
+  const size_t xr = (size_t)a->d * esize(a->dtype), yr = (size_t)a->d * esize(a->y_dtype);
+  const int Tc = (a->T + n - 1) / n;
+  n = (a->T + Tc - 1) / Tc;                    // no empty last chunk
+  // the copies start after the caller's earlier work on `stream`
+  MOE_CUDA_TRY(cudaEventRecord(ev[0], stream));
+  MOE_CUDA_TRY(cudaStreamWaitEvent(h2d, ev[0], 0));
+  MOE_CUDA_TRY(cudaStreamWaitEvent(d2h, ev[0], 0));
+  for (int c = 0; c < n; ++c) {
+    const size_t t0 = (size_t)c * Tc, tc = (size_t)(a->T - (int)t0 < Tc ? a->T - (int)t0 : Tc);
+    MOE_CUDA_TRY(cudaMemcpyAsync(static_cast<char *>(const_cast<void *>(a->x)) + t0 * xr,
+                                 static_cast<const char *>(x_host) + t0 * xr, tc * xr,
+                                 cudaMemcpyHostToDevice, h2d));
+    MOE_CUDA_TRY(cudaEventRecord(ev[1 + c], h2d));
+  }
+  for (int c = 0; c < n; ++c) {
+    const size_t t0 = (size_t)c * Tc, tc = (size_t)(a->T - (int)t0 < Tc ? a->T - (int)t0 : Tc);
+    moe_forward_args ac = *a;
+    ac.T = (int)tc;
+    ac.x = static_cast<const char *>(a->x) + t0 * xr;
+    ac.y = static_cast<char *>(a->y) + t0 * yr;
+    MOE_CUDA_TRY(cudaStreamWaitEvent(stream, ev[1 + c], 0));
+    s = moe_forward(&ac, workspace, workspace_bytes, stream_);
+    if (s != MOE_OK) return s;
+    MOE_CUDA_TRY(cudaEventRecord(ev[1 + n + c], stream));
+    MOE_CUDA_TRY(cudaStreamWaitEvent(d2h, ev[1 + n + c], 0));
+    MOE_CUDA_TRY(cudaMemcpyAsync(static_cast<char *>(y_host) + t0 * yr,
+                                 static_cast<const char *>(ac.y), tc * yr, cudaMemcpyDeviceToHost,
+                                 d2h));
+  }
+  // `stream` covers the whole call: it waits for the last copy back
+  MOE_CUDA_TRY(cudaEventRecord(ev[2 * n + 1], d2h));
+  MOE_CUDA_TRY(cudaStreamWaitEvent(stream, ev[2 * n + 1], 0));
   return MOE_OK;
 }
 

@@ -157,3 +157,33 @@ def test_forward_reroute_needs_capacity(lib):
     assert lib.moe_forward_workspace_size(ctypes.byref(a)) > 0
     a.reroute_rounds = 7                                             # k + R > N
     assert lib.moe_forward_workspace_size(ctypes.byref(a)) == 0
+
+
+def test_overlapped_host_io_rejects_bad_arguments(lib):
+    a = _args()
+    h = ctypes.c_void_p(4096)
+    # routing outputs set (the call returns y only); a stream used twice; no host buffer
+    b = _args(topk_idx=4096)
+    assert lib.moe_forward_host_io_overlapped(ctypes.byref(b), h, h, h, 1 << 40, 2, 8, 16,
+                                              24) == 1
+    assert lib.moe_forward_host_io_overlapped(ctypes.byref(a), h, h, h, 1 << 40, 2, 8, 8,
+                                              24) == 1
+    assert lib.moe_forward_host_io_overlapped(ctypes.byref(a), None, h, h, 1 << 40, 2, 8, 16,
+                                              24) == 1
+    need = lib.moe_forward_workspace_size(ctypes.byref(a))
+    assert lib.moe_forward_host_io_overlapped(ctypes.byref(a), h, h, h, need - 1, 2, 8, 16,
+                                              24) == 3
+
+
+def test_overlap_chunks_rule(lib):
+    """Chunks keep each batch's tensor work at least twice its weight
+    streaming, at most one per 2048 tokens: a prefill-shaped layer (16384
+    tokens, 8 experts of 4096 x 14336) gets 7; a DeepSeek-shaped one (weights
+    near the ridge) and a 32-token decode batch get 1."""
+    pre = _args(T=16384, d=4096, f=14336, N=8, k=2)
+    ds = _args(T=8192, d=7168, f=2048, N=256, k=8, fs=2048, Ws_gate=4096, Ws_up=4096,
+               Ws_down=4096)
+    dec = _args(T=32, d=4096, f=14336, N=8, k=2)
+    assert lib.moe_forward_overlap_chunks(ctypes.byref(pre)) == 7
+    assert lib.moe_forward_overlap_chunks(ctypes.byref(ds)) == 1
+    assert lib.moe_forward_overlap_chunks(ctypes.byref(dec)) == 1

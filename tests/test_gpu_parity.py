@@ -496,3 +496,28 @@ def test_forward_captures_into_a_cuda_graph(name, R):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(y, y_direct)
+
+
+@pytest.mark.parametrize("name,chunks", [("mixtral_small", 3), ("deepseek_small", 2),
+                                         ("mixtral_small", 0), ("capacity_small", 4)])
+def test_overlapped_host_io_equals_forward(name, chunks):
+    """Host buffers in and out with the copies overlapped with token chunks of
+    the layer: y equals the single device call bit for bit (each token's row
+    depends on that token alone; with a capacity the call runs one chunk)."""
+    cfg = REDUCED[name]
+    inp = make_inputs(cfg, device=_cuda())
+    layer = B.MoELayer(inp.W_g, inp.W_gate, inp.W_up, inp.W_down, cfg.k, bias=inp.bias,
+                       Ws_gate=inp.Ws_gate, Ws_up=inp.Ws_up, Ws_down=inp.Ws_down,
+                       capacity_factor=cfg.cf)
+    y_dev = layer(inp.x)
+    x_stage = torch.empty_like(inp.x)
+    y = torch.empty_like(y_dev)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a = layer.args(x_stage, y, {"device_status": st})
+    ws = layer.workspace(a, y.device)
+    x_host = inp.x.cpu().pin_memory()
+    y_host = torch.full(tuple(y.shape), float("nan"), dtype=y.dtype).pin_memory()
+    B.moe_forward_host_io_overlapped(a, x_host, y_host, ws, chunks)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(y_host, y_dev.cpu())
