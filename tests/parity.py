@@ -229,3 +229,63 @@ def check_layer(inp, rows=None, y_dtype=torch.float32, report=None):
     if report is not None:
         report.append((cfg.name, res))
     return res
+
+
+def _fp8_fetch(inp, qw):
+    (qg, sg), (qu, su) = qw[:2]
+    qd = qw[2] if len(qw) > 2 else None
+
+    def fetch(e):
+        w = (qg[e], sg[e], qu[e], su[e], inp.W_down[e].cpu())
+        return w if qd is None else w + (qd[0][e], qd[1][e])
+    return fetch
+
+
+def check_layer_fp8(cfg, inp, rows=None, down=False):
+    """moe_forward with E4M3 gate/up (and down, with `down`) against the
+    oracle's fp64 layer on its own E4M3 codes of x and of the weights; the
+    layer's codes must equal the oracle's byte for byte.  Routing as in
+    check_layer (near-tie rows left out).  Returns the measured errors."""
+    layer = B.MoELayer(inp.W_g, inp.W_gate, inp.W_up, inp.W_down, cfg.k, bias=inp.bias,
+                       Ws_gate=inp.Ws_gate, Ws_up=inp.Ws_up, Ws_down=inp.Ws_down,
+                       capacity_factor=cfg.cf, fp8=True, fp8_down=down)
+    y = layer(inp.x)
+    torch.cuda.synchronize()
+    out = layer.last
+    assert int(out["device_status"].item()) == 0
+    # the layer's quantised weights are the oracle's, byte for byte
+    qw = [oracle.quantize_weights_e4m3(inp.W_gate.cpu()), oracle.quantize_weights_e4m3(inp.W_up.cpu())]
+    if down:
+        qw.append(oracle.quantize_weights_e4m3(inp.W_down.cpu()))
+    for (qo, so), i in zip(qw, (0, 2, 4)):
+        np.testing.assert_array_equal(layer.fp8[i].cpu().numpy(), qo)
+        np.testing.assert_array_equal(layer.fp8[i + 1].cpu().numpy(), so)
+    x_c = inp.x.cpu()
+    lo = oracle.router_logits(x_c, inp.W_g.cpu(), None if inp.bias is None else inp.bias.cpu())
+    idx_o, w_o = oracle.topk_softmax(lo, cfg.k)
+    idx_g = out["topk_idx"].cpu().numpy()
+    flipped = np.unique(np.nonzero(np.sort(idx_g, 1) != np.sort(idx_o, 1))[0])
+    C = oracle.capacity(cfg.cf, cfg.T, cfg.k, cfg.N)
+    g_o = oracle.group(idx_o, cfg.N, C)
+    sel = np.arange(cfg.T) if rows is None else np.asarray(rows)
+    skip = np.zeros(cfg.T, dtype=bool)
+    skip[flipped] = True
+    if C > 0 and flipped.size:
+        ex = np.unique(np.concatenate([idx_g[flipped].ravel(), idx_o[flipped].ravel()]))
+        skip |= np.isin(idx_o, ex).any(1)
+    assert int(skip[sel].sum()) <= max(2, len(sel) // 100)
+    sel = sel[~skip[sel]]
+    qx, sx = oracle.quantize_rows_e4m3(x_c)
+    shared = None if not cfg.fs else (inp.Ws_gate.cpu(), inp.Ws_up.cpu(), inp.Ws_down.cpu())
+    y_o = oracle.forward_rows_fp8(qx[sel], sx[sel], idx_o[sel], w_o[sel], g_o["inv_pos"][sel],
+                                  _fp8_fetch(inp, qw), shared=shared,
+                                  x_rows=x_c[torch.as_tensor(sel)])
+    y_g = y[torch.as_tensor(sel, device=y.device)].float().cpu().numpy()
+    max_abs, fro = assert_y_close(y_g, y_o, "bf16")
+    # how far E4M3 moves the layer from its bf16 definition (reported; a
+    # loose bound catches a lost or misplaced scale)
+    y_b = oracle.forward_rows(x_c[torch.as_tensor(sel)], idx_o[sel], w_o[sel],
+                              g_o["inv_pos"][sel], fetcher(inp), shared=shared)
+    q_err = float(np.linalg.norm(y_g - y_b) / max(np.linalg.norm(y_b), 1e-30))
+    assert q_err < (0.15 if down else 0.1), f"FP8 layer {q_err:.3f} (rel-fro) away from the bf16 layer"
+    return dict(max_abs=max_abs, rel_fro=fro, fp8_vs_bf16_rel_fro=q_err, rows=len(sel))

@@ -58,16 +58,6 @@ def test_quantize_weights_bit_exact(N, d, f):
     np.testing.assert_array_equal(s.cpu().numpy(), so)
 
 
-def _fp8_fetch(inp, qw):
-    (qg, sg), (qu, su) = qw[:2]
-    qd = qw[2] if len(qw) > 2 else None
-
-    def fetch(e):
-        w = (qg[e], sg[e], qu[e], su[e], inp.W_down[e].cpu())
-        return w if qd is None else w + (qd[0][e], qd[1][e])
-    return fetch
-
-
 @pytest.mark.parametrize("down", [False, True], ids=["bf16_down", "fp8_down"])
 @pytest.mark.parametrize("counts", [
     [0, 1, 256, 257, 288, 320, 321, 600, 641, 100, 0, 960],
@@ -109,52 +99,6 @@ def test_expert_ffn_fp8_crafted_counts(counts, down):
     parity.assert_y_close(y[:A].float().cpu().numpy(), ref, "bf16")
 
 
-def _check_fp8_layer(cfg, inp, rows=None, down=False):
-    layer = B.MoELayer(inp.W_g, inp.W_gate, inp.W_up, inp.W_down, cfg.k, bias=inp.bias,
-                       Ws_gate=inp.Ws_gate, Ws_up=inp.Ws_up, Ws_down=inp.Ws_down,
-                       capacity_factor=cfg.cf, fp8=True, fp8_down=down)
-    y = layer(inp.x)
-    torch.cuda.synchronize()
-    out = layer.last
-    assert int(out["device_status"].item()) == 0
-    # the layer's quantised weights are the oracle's, byte for byte
-    qw = [oracle.quantize_weights_e4m3(inp.W_gate.cpu()), oracle.quantize_weights_e4m3(inp.W_up.cpu())]
-    if down:
-        qw.append(oracle.quantize_weights_e4m3(inp.W_down.cpu()))
-    for (qo, so), i in zip(qw, (0, 2, 4)):
-        np.testing.assert_array_equal(layer.fp8[i].cpu().numpy(), qo)
-        np.testing.assert_array_equal(layer.fp8[i + 1].cpu().numpy(), so)
-    x_c = inp.x.cpu()
-    lo = oracle.router_logits(x_c, inp.W_g.cpu(), None if inp.bias is None else inp.bias.cpu())
-    idx_o, w_o = oracle.topk_softmax(lo, cfg.k)
-    idx_g = out["topk_idx"].cpu().numpy()
-    flipped = np.unique(np.nonzero(np.sort(idx_g, 1) != np.sort(idx_o, 1))[0])
-    C = oracle.capacity(cfg.cf, cfg.T, cfg.k, cfg.N)
-    g_o = oracle.group(idx_o, cfg.N, C)
-    sel = np.arange(cfg.T) if rows is None else np.asarray(rows)
-    skip = np.zeros(cfg.T, dtype=bool)
-    skip[flipped] = True
-    if C > 0 and flipped.size:
-        ex = np.unique(np.concatenate([idx_g[flipped].ravel(), idx_o[flipped].ravel()]))
-        skip |= np.isin(idx_o, ex).any(1)
-    assert int(skip[sel].sum()) <= max(2, len(sel) // 100)
-    sel = sel[~skip[sel]]
-    qx, sx = oracle.quantize_rows_e4m3(x_c)
-    shared = None if not cfg.fs else (inp.Ws_gate.cpu(), inp.Ws_up.cpu(), inp.Ws_down.cpu())
-    y_o = oracle.forward_rows_fp8(qx[sel], sx[sel], idx_o[sel], w_o[sel], g_o["inv_pos"][sel],
-                                  _fp8_fetch(inp, qw), shared=shared,
-                                  x_rows=x_c[torch.as_tensor(sel)])
-    y_g = y[torch.as_tensor(sel, device=y.device)].float().cpu().numpy()
-    max_abs, fro = parity.assert_y_close(y_g, y_o, "bf16")
-    # how far E4M3 moves the layer from its bf16 definition (reported; a
-    # loose bound catches a lost or misplaced scale)
-    y_b = oracle.forward_rows(x_c[torch.as_tensor(sel)], idx_o[sel], w_o[sel],
-                              g_o["inv_pos"][sel], parity.fetcher(inp), shared=shared)
-    q_err = float(np.linalg.norm(y_g - y_b) / max(np.linalg.norm(y_b), 1e-30))
-    assert q_err < (0.15 if down else 0.1), f"FP8 layer {q_err:.3f} (rel-fro) away from the bf16 layer"
-    return dict(max_abs=max_abs, rel_fro=fro, fp8_vs_bf16_rel_fro=q_err, rows=len(sel))
-
-
 @pytest.mark.parametrize("down", [False, True], ids=["bf16_down", "fp8_down"])
 @pytest.mark.parametrize("name", list(SMALL))
 def test_layer_fp8_reduced(name, down):
@@ -162,7 +106,7 @@ def test_layer_fp8_reduced(name, down):
     if down and cfg.f % 16:
         pytest.skip("an E4M3 down projection needs f % 16 == 0")
     inp = make_inputs(cfg, device=torch.device("cuda"))
-    print(name, down, _check_fp8_layer(cfg, inp, down=down))
+    print(name, down, parity.check_layer_fp8(cfg, inp, down=down))
 
 
 @pytest.mark.parametrize("down", [False, True], ids=["bf16_down", "fp8_down"])
@@ -173,7 +117,7 @@ def test_layer_fp8_full_size(name, rows, down):
     sel = None
     if rows is not None:
         sel = np.sort(np.random.default_rng(cfg.seed).choice(cfg.T, size=rows, replace=False))
-    print(name, down, _check_fp8_layer(cfg, inp, sel, down=down))
+    print(name, down, parity.check_layer_fp8(cfg, inp, sel, down=down))
     del inp
     torch.cuda.empty_cache()
 
