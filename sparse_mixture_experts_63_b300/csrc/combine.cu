@@ -19,6 +19,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const TI *__restrict__ y_p
                                                       const int32_t *__restrict__ inv_pos, int T,
                                                       int k, int d, const TI *__restrict__ shared,
                                                       TO *__restrict__ y) {
+  pdl_begin();
   const int groups = d / 8;
   const long total = (long)T * groups;
   for (long g = (long)blockIdx.x * blockDim.x + threadIdx.x; g < total;
@@ -63,9 +64,9 @@ moe_status_t launch_typed(const void *y_perm, const int32_t *inv_pos, int T, int
   if (total == 0) return MOE_OK;
   long grid = (total + 255) / 256;
   if (grid > 148L * 32) grid = 148L * 32;
-  combine_kernel<TI, TO><<<(int)grid, 256, 0, stream>>>(
+  MOE_CUDA_TRY(launch_pdl(combine_kernel<TI, TO>, dim3((int)grid), dim3(256), 0, stream,
       static_cast<const TI *>(y_perm), inv_pos, T, k, d, static_cast<const TI *>(shared_y),
-      static_cast<TO *>(y));
+      static_cast<TO *>(y)));
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

@@ -336,6 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmB1,
                     const __grid_constant__ CUtensorMap tmB2,
                     const __grid_constant__ CUtensorMap tmB3, const TcParams p) {
+  // the next kernel may start launching; this one's set-up (barriers, tensor
+  // memory, descriptor prefetch) overlaps the previous kernel's tail
+  pdl_trigger();
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -378,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tmem_alloc_pair(tmem_slot, kTmemCols);
     tc::tmem_relinquish_pair();
   }
+  pdl_wait();   // the offsets and rows come from the previous kernels
   build_tile_prefix(p, prefix);
   tc::tc_fence_before();
   __syncthreads();
@@ -755,17 +759,19 @@ moe_status_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUt
     if (dev < kMaxDevicesCached) attr_set[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_begin
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(2 * max_pairs());
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   MOE_CUDA_TRY(
       cudaLaunchKernelEx(&cfg, grouped_gemm_tc<FP8>, a0, a1, b[0], b[1], b[2], b[3], p));
   MOE_LAUNCH_CHECK();

@@ -76,6 +76,7 @@ struct Carve {
 };
 
 __global__ void set_shared_offsets(int32_t *off, int T) {
+  pdl_begin();
   off[0] = 0;
   off[1] = T;
 }
@@ -577,7 +578,7 @@ moe_status_t moe_forward(const moe_forward_args *a, void *workspace, size_t work
   }
   if (s != MOE_OK) return s;
   if (a->fs > 0) {
-    set_shared_offsets<<<1, 1, 0, stream>>>(L.sh_offsets, a->T);
+    MOE_CUDA_TRY(launch_pdl(set_shared_offsets, dim3(1), dim3(1), 0, stream, L.sh_offsets, a->T));
     MOE_LAUNCH_CHECK();
     s = launch_expert_ffn(a->x, L.sh_offsets, nullptr, a->T, a->d, a->fs, 1, 0, a->dtype,
                           a->Ws_gate, a->Ws_up, a->Ws_down, L.ys, a->device_status,

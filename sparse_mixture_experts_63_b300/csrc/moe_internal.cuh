@@ -62,8 +62,41 @@ __device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may start
+// while the previous kernel on its stream is still running; pdl_begin() lets
+// the next kernel start launching (it waits in its own pdl_begin) and then
+// waits until the previous kernel has finished and its writes are visible.
+// Every kernel of the layer calls it before touching global memory (without
+// the launch attribute both are no-ops), so kernel i finishing implies every
+// earlier kernel has finished.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_begin() {
+  pdl_trigger();
+  pdl_wait();
+}
+
 __device__ __forceinline__ void report(int32_t *status, int32_t bits) {
   if (status) atomicOr(status, bits);
+}
+
+// Launches `kernel` with programmatic stream serialisation (see pdl_begin).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 // ---- launchers (each returns MOE_OK or an error; never synchronises) --------

@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(kThreads) permute_hist(const int32_t *__restri
                                                          int T, int N, int k,
                                                          int32_t *__restrict__ hist,
                                                          int32_t *status, int neg_one_drops) {
+  pdl_begin();
   extern __shared__ int32_t sh_hist[];  // [N]
   for (int e = threadIdx.x; e < N; e += blockDim.x) sh_hist[e] = 0;
   __syncthreads();
@@ -57,6 +58,7 @@ __global__ void __launch_bounds__(kMaxN) permute_scan(int32_t *__restrict__ hist
                                                       int32_t *__restrict__ counts,
                                                       int32_t *__restrict__ offsets,
                                                       int32_t *__restrict__ dropped) {
+  pdl_begin();
   __shared__ int32_t warp_sums[kMaxN / 32];
   const int e = threadIdx.x;
   int32_t total = 0;
@@ -103,6 +105,7 @@ __global__ void __launch_bounds__(kThreads) permute_scatter(
     const int32_t *__restrict__ topk_idx, const float *__restrict__ topk_w, int T, int N, int k,
     int capacity, const int32_t *__restrict__ chunk_base, const int32_t *__restrict__ offsets,
     int32_t *__restrict__ perm_token, float *__restrict__ row_scale, int32_t *__restrict__ inv_pos) {
+  pdl_begin();
   extern __shared__ int32_t sm[];
   int32_t *running = sm;                  // [N] rows of each expert seen in earlier rounds
   int32_t *warp_cnt = sm + N;             // [8][N] per-warp counts of this round
@@ -162,6 +165,7 @@ __global__ void __launch_bounds__(kSmallThreads) permute_small(
     int32_t *__restrict__ perm_token, float *__restrict__ row_scale,
     int32_t *__restrict__ inv_pos, int32_t *__restrict__ dropped, int32_t *status,
     int neg_one_drops) {
+  pdl_begin();
   constexpr int kWarps = kSmallThreads / 32;
   __shared__ int32_t hist[kSmallMaxN];
   __shared__ int32_t off_s[kSmallMaxN + 1];
@@ -243,6 +247,7 @@ __global__ void __launch_bounds__(256) permute_copy_rows(const VecT *__restrict_
                                                          const int32_t *__restrict__ inv_pos,
                                                          int T, int k, int vecs_per_row,
                                                          VecT *__restrict__ x_perm) {
+  pdl_begin();
   constexpr int kUnroll = 4;
   const int lane = threadIdx.x % 32;
   const int warps = blockDim.x / 32;
@@ -294,24 +299,23 @@ moe_status_t launch_permute(const int32_t *topk_idx, const float *topk_w, const 
   int32_t *hist = static_cast<int32_t *>(workspace);
   const int nchunks = (T + kChunkTokens - 1) / kChunkTokens;
   if (nchunks == 1 && N <= kSmallMaxN) {
-    permute_small<<<1, kSmallThreads, 0, stream>>>(topk_idx, topk_w, T, N, k, capacity, counts,
-                                                   offsets, perm_token, row_scale, inv_pos,
-                                                   dropped, device_status, neg_one_drops ? 1 : 0);
+    MOE_CUDA_TRY(launch_pdl(permute_small, dim3(1), dim3(kSmallThreads), 0, stream, topk_idx,
+        topk_w, T, N, k, capacity, counts, offsets, perm_token, row_scale, inv_pos, dropped,
+        device_status, neg_one_drops ? 1 : 0));
     MOE_LAUNCH_CHECK();
   } else {
   if (nchunks > 0) {
-    permute_hist<<<nchunks, kThreads, N * sizeof(int32_t), stream>>>(
-        topk_idx, T, N, k, hist, device_status, neg_one_drops ? 1 : 0);
+    MOE_CUDA_TRY(launch_pdl(permute_hist, dim3(nchunks), dim3(kThreads), N * sizeof(int32_t),
+        stream, topk_idx, T, N, k, hist, device_status, neg_one_drops ? 1 : 0));
     MOE_LAUNCH_CHECK();
   }
-  permute_scan<<<1, kMaxN, 0, stream>>>(hist, nchunks, T, N, k, capacity, counts, offsets,
-                                        dropped);
+  MOE_CUDA_TRY(launch_pdl(permute_scan, dim3(1), dim3(kMaxN), 0, stream, hist, nchunks, T, N, k,
+      capacity, counts, offsets, dropped));
   MOE_LAUNCH_CHECK();
   if (nchunks > 0) {
     size_t smem = (size_t)N * (1 + kThreads / 32) * sizeof(int32_t);
-    permute_scatter<<<nchunks, kThreads, smem, stream>>>(topk_idx, topk_w, T, N, k, capacity,
-                                                         hist, offsets, perm_token, row_scale,
-                                                         inv_pos);
+    MOE_CUDA_TRY(launch_pdl(permute_scatter, dim3(nchunks), dim3(kThreads), smem, stream, topk_idx,
+        topk_w, T, N, k, capacity, hist, offsets, perm_token, row_scale, inv_pos));
     MOE_LAUNCH_CHECK();
   }
   }
@@ -330,8 +334,8 @@ moe_status_t launch_copy_row_bytes(const void *x, size_t row_bytes, const int32_
     const int vecs = (int)(row_bytes / 16);
     long grid = ((long)T + 7) / 8;
     if (grid > 148L * 16) grid = 148L * 16;
-    permute_copy_rows<uint4><<<(int)grid, 256, 0, stream>>>(
-        static_cast<const uint4 *>(x), inv_pos, T, k, vecs, static_cast<uint4 *>(x_perm));
+    MOE_CUDA_TRY(launch_pdl(permute_copy_rows<uint4>, dim3((int)grid), dim3(256), 0, stream,
+        static_cast<const uint4 *>(x), inv_pos, T, k, vecs, static_cast<uint4 *>(x_perm)));
     MOE_LAUNCH_CHECK();
   }
   return MOE_OK;

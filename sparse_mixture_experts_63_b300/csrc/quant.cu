@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(256) quantize_rows_e4m3(const __nv_bfloat16 *_
                                                           uint8_t *__restrict__ q,
                                                           float *__restrict__ scale,
                                                           const int32_t *__restrict__ rows_valid) {
+  pdl_begin();
   __shared__ float red[8];                     // one per warp
   const int lg = threadIdx.x % G;              // thread within the row's group
   const int grp = threadIdx.x / G;
@@ -134,8 +135,8 @@ moe_status_t launch_quantize_rows_e4m3(const void *x, int R, int C, uint8_t *q, 
   const long rpc = 256 / G;
   long grid = ((long)R + rpc - 1) / rpc;
   if (grid > 148L * 8) grid = 148L * 8;
-  quantize_rows_e4m3<<<(int)grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(x), R, C,
-                                                    G, q, scale, rows_valid);
+  MOE_CUDA_TRY(launch_pdl(quantize_rows_e4m3, dim3((int)grid), dim3(256), 0, stream,
+      static_cast<const __nv_bfloat16 *>(x), R, C, G, q, scale, rows_valid));
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(256) router_small_n(const T *__restrict__ x,
                                                       int d, int N, int k, float *logits,
                                                       int32_t *topk_idx, float *topk_w,
                                                       int32_t *status) {
+  pdl_begin();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   T *ws = reinterpret_cast<T *>(smem_raw);  // [d][NP], zero-padded experts
   if (N == NP && (reinterpret_cast<uintptr_t>(Wg) & 15) == 0) {
@@ -180,6 +181,7 @@ template <typename T, int NP>
 __global__ void __launch_bounds__(kDecWarps * 32) router_decode(
     const T *__restrict__ x, const T *__restrict__ Wg, const float *__restrict__ bias, int Tn,
     int d, int N, int k, float *logits, int32_t *topk_idx, float *topk_w, int32_t *status) {
+  pdl_begin();
   __shared__ float part[kDecWarps][NP];
   const int t = blockIdx.x;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -249,6 +251,7 @@ __global__ void __launch_bounds__(256) router_tiled(const T *__restrict__ x,
                                                     int N, int k, float *logits,
                                                     int32_t *topk_idx, float *topk_w,
                                                     int32_t *status) {
+  pdl_begin();
   constexpr int EJ = NP / kWarp;  // experts per thread
   __shared__ float xs[kTM][kKC + 1];
   __shared__ __align__(16) float wsm[kKC * NP];  // [kKC][NP]; reused as logits [kTM][NP]
@@ -336,14 +339,14 @@ moe_status_t launch_typed(const void *x, const void *W_g, const float *bias, int
   if (T_ == 0) return MOE_OK;
   if (T_ <= 512 && N <= 32 && d % 8 == 0) {
     if (N <= 8)
-      router_decode<T, 8><<<T_, kDecWarps * 32, 0, stream>>>(xp, wp, bias, T_, d, N, k, logits,
-                                                             topk_idx, topk_w, status);
+      MOE_CUDA_TRY(launch_pdl(router_decode<T, 8>, dim3(T_), dim3(kDecWarps * 32), 0, stream, xp,
+          wp, bias, T_, d, N, k, logits, topk_idx, topk_w, status));
     else if (N <= 16)
-      router_decode<T, 16><<<T_, kDecWarps * 32, 0, stream>>>(xp, wp, bias, T_, d, N, k, logits,
-                                                              topk_idx, topk_w, status);
+      MOE_CUDA_TRY(launch_pdl(router_decode<T, 16>, dim3(T_), dim3(kDecWarps * 32), 0, stream, xp,
+          wp, bias, T_, d, N, k, logits, topk_idx, topk_w, status));
     else
-      router_decode<T, 32><<<T_, kDecWarps * 32, 0, stream>>>(xp, wp, bias, T_, d, N, k, logits,
-                                                              topk_idx, topk_w, status);
+      MOE_CUDA_TRY(launch_pdl(router_decode<T, 32>, dim3(T_), dim3(kDecWarps * 32), 0, stream, xp,
+          wp, bias, T_, d, N, k, logits, topk_idx, topk_w, status));
     MOE_LAUNCH_CHECK();
     return MOE_OK;
   }
@@ -365,24 +368,24 @@ moe_status_t launch_typed(const void *x, const void *W_g, const float *bias, int
                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
           if (done) done[0] = true;
         }
-        router_small_n<T, 8><<<grid, 256, smem, stream>>>(xp, wp, bias, T_, d, N, k, logits,
-                                                          topk_idx, topk_w, status);
+        MOE_CUDA_TRY(launch_pdl(router_small_n<T, 8>, dim3(grid), dim3(256), smem, stream, xp, wp,
+            bias, T_, d, N, k, logits, topk_idx, topk_w, status));
       } else if (NP == 16) {
         if (!done || !done[1]) {
           MOE_CUDA_TRY(cudaFuncSetAttribute(router_small_n<T, 16>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
           if (done) done[1] = true;
         }
-        router_small_n<T, 16><<<grid, 256, smem, stream>>>(xp, wp, bias, T_, d, N, k, logits,
-                                                           topk_idx, topk_w, status);
+        MOE_CUDA_TRY(launch_pdl(router_small_n<T, 16>, dim3(grid), dim3(256), smem, stream, xp, wp,
+            bias, T_, d, N, k, logits, topk_idx, topk_w, status));
       } else {
         if (!done || !done[2]) {
           MOE_CUDA_TRY(cudaFuncSetAttribute(router_small_n<T, 32>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
           if (done) done[2] = true;
         }
-        router_small_n<T, 32><<<grid, 256, smem, stream>>>(xp, wp, bias, T_, d, N, k, logits,
-                                                           topk_idx, topk_w, status);
+        MOE_CUDA_TRY(launch_pdl(router_small_n<T, 32>, dim3(grid), dim3(256), smem, stream, xp, wp,
+            bias, T_, d, N, k, logits, topk_idx, topk_w, status));
       }
       MOE_LAUNCH_CHECK();
       return MOE_OK;
@@ -390,17 +393,17 @@ moe_status_t launch_typed(const void *x, const void *W_g, const float *bias, int
   }
   int grid = (T_ + kTM - 1) / kTM;
   if (N <= 32)
-    router_tiled<T, 32><<<grid, 256, 0, stream>>>(xp, wp, bias, T_, d, N, k, logits, topk_idx,
-                                                  topk_w, status);
+    MOE_CUDA_TRY(launch_pdl(router_tiled<T, 32>, dim3(grid), dim3(256), 0, stream, xp, wp, bias, T_,
+        d, N, k, logits, topk_idx, topk_w, status));
   else if (N <= 64)
-    router_tiled<T, 64><<<grid, 256, 0, stream>>>(xp, wp, bias, T_, d, N, k, logits, topk_idx,
-                                                  topk_w, status);
+    MOE_CUDA_TRY(launch_pdl(router_tiled<T, 64>, dim3(grid), dim3(256), 0, stream, xp, wp, bias, T_,
+        d, N, k, logits, topk_idx, topk_w, status));
   else if (N <= 128)
-    router_tiled<T, 128><<<grid, 256, 0, stream>>>(xp, wp, bias, T_, d, N, k, logits,
-                                                   topk_idx, topk_w, status);
+    MOE_CUDA_TRY(launch_pdl(router_tiled<T, 128>, dim3(grid), dim3(256), 0, stream, xp, wp, bias,
+        T_, d, N, k, logits, topk_idx, topk_w, status));
   else
-    router_tiled<T, 256><<<grid, 256, 0, stream>>>(xp, wp, bias, T_, d, N, k, logits,
-                                                   topk_idx, topk_w, status);
+    MOE_CUDA_TRY(launch_pdl(router_tiled<T, 256>, dim3(grid), dim3(256), 0, stream, xp, wp, bias,
+        T_, d, N, k, logits, topk_idx, topk_w, status));
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

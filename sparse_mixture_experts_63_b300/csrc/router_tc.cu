@@ -109,6 +109,7 @@ template <int KMAX>
 __global__ void __launch_bounds__(kThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmW, const RParams p) {
+  pdl_begin();
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -356,17 +357,19 @@ moe_status_t launch_k(const CUtensorMap &tx, const CUtensorMap &tw, const RParam
     if (dev < kMaxDevicesCached) attr[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attrs[1];
-  attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = p.group_ctas;
-  attrs[0].val.clusterDim.y = 1;
-  attrs[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_begin
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  attrs[1].id = cudaLaunchAttributeClusterDimension;
+  attrs[1].val.clusterDim.x = p.group_ctas;
+  attrs[1].val.clusterDim.y = 1;
+  attrs[1].val.clusterDim.z = 1;
   cfg.gridDim = dim3(tiles * p.group_ctas);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attrs;
-  cfg.numAttrs = p.group_ctas > 1 ? 1 : 0;
+  cfg.numAttrs = p.group_ctas > 1 ? 2 : 1;
   MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, router_tc_kernel<KMAX>, tx, tw, p));
   MOE_LAUNCH_CHECK();
   return MOE_OK;
