@@ -91,8 +91,7 @@ struct ForwardLayout {
   int32_t *topk_idx, *counts, *offsets, *inv_pos, *perm_token, *dropped, *sh_offsets;
   float *topk_w, *row_scale;
   void *x_perm, *y_perm, *ffn_ws, *perm_ws, *ys, *sh_ffn_ws;
-  uint8_t *xq;       // [T, d] E4M3 token rows (FP8 gate/up only)
-  float *xs;         // [T] their scales
+  float *xs;         // [T] token scales (FP8 gate/up only)
   int32_t *cand;     // [T, k+R] router candidates (re-routing only)
   float *cand_w;     // [T, k+R]
   void *rr_ws;       // re-routing workspace
@@ -116,7 +115,6 @@ ForwardLayout layout_forward(const moe_forward_args *a, void *ws) {
   L.row_scale = c.take<float>(tk);
   L.x_perm = c.take_bytes((size_t)A_max * a->d * es);   // E4M3 rows use the first half
   if (a->Wq_gate) {
-    L.xq = static_cast<uint8_t *>(c.take_bytes((size_t)a->T * a->d));
     L.xs = c.take<float>(a->T);
   }
   L.y_perm = c.take_bytes((size_t)A_max * a->d * es);
@@ -536,11 +534,7 @@ moe_status_t moe_forward(const moe_forward_args *a, void *workspace, size_t work
   const int cap = moe_capacity(a->capacity_factor, a->T, a->k, a->N);
   const int A_max = (int)routed_rows_max(a->T, a->N, a->k, cap);
   const bool fp8 = a->Wq_gate != nullptr;
-  void *x_perm = fp8 ? nullptr : L.x_perm;   // FP8: the quantised rows are copied later
-  if (fp8) {
-    s = launch_quantize_rows_e4m3(a->x, a->T, a->d, L.xq, L.xs, stream);
-    if (s != MOE_OK) return s;
-  }
+  void *x_perm = fp8 ? nullptr : L.x_perm;   // FP8: the rows are quantised as they are copied
 
   if (a->reroute_rounds > 0) {
     // the router ranks k+R candidates; the dispatch re-routes overflow to them
@@ -565,7 +559,8 @@ moe_status_t moe_forward(const moe_forward_args *a, void *workspace, size_t work
   }
   if (fp8) {
     // E4M3 gate/up: the dispatched rows are the quantised token rows
-    s = launch_copy_row_bytes(L.xq, (size_t)a->d, L.inv_pos, a->T, a->k, L.x_perm, stream);
+    s = launch_copy_rows_e4m3(a->x, L.inv_pos, a->T, a->d, a->k,
+                              static_cast<uint8_t *>(L.x_perm), L.xs, stream);
     if (s != MOE_OK) return s;
     s = launch_ffn_tc_fp8(L.x_perm, L.xs, L.perm_token, L.offsets, L.row_scale, A_max, a->d,
                           a->f, a->N, cap, a->Wq_gate, a->wscale_gate, a->Wq_up, a->wscale_up,

@@ -137,6 +137,10 @@ moe_status_t launch_quantize_rows_e4m3(const void *x, int R, int C, uint8_t *q, 
                                        cudaStream_t stream, const int32_t *rows_valid = nullptr);
 moe_status_t launch_quantize_weights_e4m3(const void *W, int N, int d, int f, uint8_t *q,
                                           float *scale, cudaStream_t stream);
+// The dispatch row copy with the rows quantised on the way (codes of token t
+// to every kept slot's permuted row; scale[t] as quantize_rows).
+moe_status_t launch_copy_rows_e4m3(const void *x, const int32_t *inv_pos, int T, int d, int k,
+                                   uint8_t *x_perm, float *scale, cudaStream_t stream);
 // Expert FFN with E4M3 gate/up and, when Wq_down is given, E4M3 down (see
 // ffn_tc.cu).  Workspace: ffn_fp8_workspace_bytes.
 size_t ffn_fp8_workspace_bytes(int A_max, int f, bool fp8_down);

@@ -80,6 +80,51 @@ __global__ void __launch_bounds__(256) quantize_rows_e4m3(const __nv_bfloat16 *_
   }
 }
 
+// The dispatch row copy of an FP8 layer: one warp per token (grid-stride)
+// quantises the token's row as quantize_rows_e4m3 does (scale to scale[t]) and
+// writes its codes to the permuted row of each kept slot (inv_pos; -1 =
+// dropped).  The row is read twice (absmax, then codes; the second read hits
+// L1/L2).  d % 16 == 0.
+__global__ void __launch_bounds__(256) copy_rows_e4m3(const __nv_bfloat16 *__restrict__ x,
+                                                      const int32_t *__restrict__ inv_pos, int T,
+                                                      int d, int k, uint8_t *__restrict__ x_perm,
+                                                      float *__restrict__ scale) {
+  pdl_begin();
+  const int lane = threadIdx.x % 32;
+  const int warps = blockDim.x / 32;
+  const int nv = d / 8;
+  for (int t = blockIdx.x * warps + threadIdx.x / 32; t < T; t += gridDim.x * warps) {
+    const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)t * d);
+    float am = 0.f;
+    for (int v = lane; v < nv; v += 32) {
+      float f[8];
+      load8(reinterpret_cast<const __nv_bfloat16 *>(row + v), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    const float inv = am > 0.f ? 448.0f / am : 1.0f;
+    if (lane == 0) scale[t] = am > 0.f ? am / 448.0f : 1.0f;
+    for (int j0 = 0; j0 < k; j0 += 32) {
+      const int nj = min(32, k - j0);
+      const int my = lane < nj ? inv_pos[(size_t)t * k + j0 + lane] : -1;
+      for (int v = lane; v < nv; v += 32) {
+        float f[8];
+        load8(reinterpret_cast<const __nv_bfloat16 *>(row + v), f);
+        uint32_t w[2] = {0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i / 4] |= (uint32_t)to_e4m3(f[i] * inv) << (8 * (i % 4));
+        const uint2 code = make_uint2(w[0], w[1]);
+        for (int j = 0; j < nj; ++j) {
+          const int pos = __shfl_sync(0xffffffffu, my, j);
+          if (pos >= 0) reinterpret_cast<uint2 *>(x_perm + (size_t)pos * d)[v] = code;
+        }
+      }
+    }
+  }
+}
+
 // W [N, d, f] viewed as [N, K = d, M = f].  Block (32 output channels, expert
 // e): the channels' absmax over d, then the codes in tiles of 128 d,
 // transposed through shared memory so each channel's 128 bytes leave as eight
@@ -137,6 +182,18 @@ moe_status_t launch_quantize_rows_e4m3(const void *x, int R, int C, uint8_t *q, 
   if (grid > 148L * 8) grid = 148L * 8;
   MOE_CUDA_TRY(launch_pdl(quantize_rows_e4m3, dim3((int)grid), dim3(256), 0, stream,
       static_cast<const __nv_bfloat16 *>(x), R, C, G, q, scale, rows_valid));
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+moe_status_t launch_copy_rows_e4m3(const void *x, const int32_t *inv_pos, int T, int d, int k,
+                                   uint8_t *x_perm, float *scale, cudaStream_t stream) {
+  if (T == 0) return MOE_OK;
+  long grid = ((long)T + 7) / 8;
+  if (grid > 148L * 16) grid = 148L * 16;
+  MOE_CUDA_TRY(launch_pdl(copy_rows_e4m3, dim3((int)grid), dim3(256), 0, stream,
+                          static_cast<const __nv_bfloat16 *>(x), inv_pos, T, d, k, x_perm,
+                          scale));
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
