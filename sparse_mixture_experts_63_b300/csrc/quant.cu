@@ -80,48 +80,60 @@ __global__ void __launch_bounds__(256) quantize_rows_e4m3(const __nv_bfloat16 *_
   }
 }
 
-// The dispatch row copy of an FP8 layer: one warp per token (grid-stride)
-// quantises the token's row as quantize_rows_e4m3 does (scale to scale[t]) and
-// writes its codes to the permuted row of each kept slot (inv_pos; -1 =
-// dropped).  The row is read twice (absmax, then codes; the second read hits
-// L1/L2).  d % 16 == 0.
+// The dispatch row copy of an FP8 layer: G threads per token (as in
+// quantize_rows_e4m3: 256 / G tokens per CTA, grid-stride) quantise the
+// token's row as quantize_rows_e4m3 does (scale to scale[t]) and write its
+// codes to the permuted row of each kept slot (inv_pos; -1 = dropped).  The
+// row is read twice (absmax, then codes; the second read hits L1/L2).
+// d % 16 == 0, k <= 32.
 __global__ void __launch_bounds__(256) copy_rows_e4m3(const __nv_bfloat16 *__restrict__ x,
                                                       const int32_t *__restrict__ inv_pos, int T,
-                                                      int d, int k, uint8_t *__restrict__ x_perm,
+                                                      int d, int k, int G,
+                                                      uint8_t *__restrict__ x_perm,
                                                       float *__restrict__ scale) {
   pdl_begin();
-  const int lane = threadIdx.x % 32;
-  const int warps = blockDim.x / 32;
+  __shared__ float red[8];                     // one per warp
+  __shared__ int32_t pos_s[8][32];             // kept positions of each token of the CTA
+  const int lg = threadIdx.x % G;
+  const int grp = threadIdx.x / G;
+  const int rpc = blockDim.x / G;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nv = d / 8;
-  for (int t = blockIdx.x * warps + threadIdx.x / 32; t < T; t += gridDim.x * warps) {
-    const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)t * d);
+  for (long b = blockIdx.x; b * rpc < T; b += gridDim.x) {
+    const long t = b * rpc + grp;
+    const bool active = t < T;
+    const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)(active ? t : 0) * d);
+    if (active && lg < k) pos_s[grp][lg] = inv_pos[(size_t)t * k + lg];
     float am = 0.f;
-    for (int v = lane; v < nv; v += 32) {
-      float f[8];
-      load8(reinterpret_cast<const __nv_bfloat16 *>(row + v), f);
+    if (active)
+      for (int v = lg; v < nv; v += G) {
+        float f[8];
+        load8(reinterpret_cast<const __nv_bfloat16 *>(row + v), f);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
-    }
+        for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
+      }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    if (lane == 0) red[warp] = am;
+    __syncthreads();
+    am = 0.f;
+    for (int w = 0; w < (G + 31) / 32; ++w) am = fmaxf(am, red[(grp * G) / 32 + w]);
     const float inv = am > 0.f ? 448.0f / am : 1.0f;
-    if (lane == 0) scale[t] = am > 0.f ? am / 448.0f : 1.0f;
-    for (int j0 = 0; j0 < k; j0 += 32) {
-      const int nj = min(32, k - j0);
-      const int my = lane < nj ? inv_pos[(size_t)t * k + j0 + lane] : -1;
-      for (int v = lane; v < nv; v += 32) {
+    if (active && lg == 0) scale[t] = am > 0.f ? am / 448.0f : 1.0f;
+    if (active)
+      for (int v = lg; v < nv; v += G) {
         float f[8];
         load8(reinterpret_cast<const __nv_bfloat16 *>(row + v), f);
         uint32_t w[2] = {0u, 0u};
 #pragma unroll
         for (int i = 0; i < 8; ++i) w[i / 4] |= (uint32_t)to_e4m3(f[i] * inv) << (8 * (i % 4));
         const uint2 code = make_uint2(w[0], w[1]);
-        for (int j = 0; j < nj; ++j) {
-          const int pos = __shfl_sync(0xffffffffu, my, j);
+        for (int j = 0; j < k; ++j) {
+          const int pos = pos_s[grp][j];
           if (pos >= 0) reinterpret_cast<uint2 *>(x_perm + (size_t)pos * d)[v] = code;
         }
       }
-    }
+    __syncthreads();   // red and pos_s are rewritten by the next batch
   }
 }
 
@@ -189,10 +201,14 @@ moe_status_t launch_quantize_rows_e4m3(const void *x, int R, int C, uint8_t *q, 
 moe_status_t launch_copy_rows_e4m3(const void *x, const int32_t *inv_pos, int T, int d, int k,
                                    uint8_t *x_perm, float *scale, cudaStream_t stream) {
   if (T == 0) return MOE_OK;
-  long grid = ((long)T + 7) / 8;
-  if (grid > 148L * 16) grid = 148L * 16;
+  const int nv = d / 8;                         // threads per token as in the row quantiser
+  int G = 32;
+  while (G < 256 && G * 4 < nv) G *= 2;
+  const long rpc = 256 / G;
+  long grid = ((long)T + rpc - 1) / rpc;
+  if (grid > 148L * 8) grid = 148L * 8;
   MOE_CUDA_TRY(launch_pdl(copy_rows_e4m3, dim3((int)grid), dim3(256), 0, stream,
-                          static_cast<const __nv_bfloat16 *>(x), inv_pos, T, d, k, x_perm,
+                          static_cast<const __nv_bfloat16 *>(x), inv_pos, T, d, k, G, x_perm,
                           scale));
   MOE_LAUNCH_CHECK();
   return MOE_OK;
