@@ -2,7 +2,7 @@
 """MoE-layer forward benchmark on B300: tokens/s and fraction of the roofline.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
-                    [--impl ours|reference]
+                    [--impl ours|reference] [--reroute R] [--fp8 [--fp8-down]]
 
 One step = one moe_forward (router, top-k/softmax, dispatch, grouped SwiGLU
 experts, combine) over one batch of the workload's T tokens, inputs resident
@@ -17,6 +17,13 @@ weak and value = all ranks' tokens / the slowest rank's time.
 
 --impl reference times the fp64 CPU oracle (the only reference there is) on
 the host cores, on a bounded sample of the same workload per step.
+
+--reroute R re-routes capacity overflow in R rounds (layers with a capacity);
+--fp8 runs the routed gate/up projections with E4M3 weights and token rows
+(--fp8-down the down projection too) and reports them against their own
+roofline (E4M3 bytes, FP8 FLOPs at twice the measured bf16 rate).  `e2e` is
+the same layer through the host-buffer call with pinned x in and y out, the
+copies overlapped with token chunks of the layer where that cannot change y.
 """
 import argparse
 import json
