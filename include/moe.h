@@ -220,7 +220,9 @@ moe_status_t moe_expert_ffn(const void *x_perm, const int32_t *offsets,
  * moe_quantize_rows_e4m3: rows x [R,C] bf16, one scale per row: q [R,C],
  *   scale [R].  C % 16 == 0.
  * moe_expert_ffn_fp8: moe_expert_ffn with E4M3 gate/up: xq_perm [A_max,d]
- *   codes of the permuted token rows (moe_permute on the quantised rows),
+ *   codes of the permuted token rows (row p = the codes of token
+ *   perm_token[p] from moe_quantize_rows_e4m3; moe_forward writes them while
+ *   it dispatches),
  *   row p's scale = x_scale[perm_token[p]] (x_scale [T] per token);
  *   g = (xq . Wq_gate[e][j]) * x_scale * wscale_gate[e][j], u likewise,
  *   h = SiLU(g) * u rounded to bf16, y_perm = row_scale * (h W_down) as in
