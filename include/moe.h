@@ -333,7 +333,9 @@ moe_status_t moe_forward_host_io(const moe_forward_args *args,
  * stream its weights again, at most one per 2048 tokens, 16 in all).  The
  * call returns y only: the routing outputs of args must be NULL.  Three
  * distinct streams; workspace: moe_forward_workspace_size(args).  Pinned
- * host memory makes the copies asynchronous. */
+ * host memory makes the copies asynchronous.  The first call on a host thread
+ * and device creates the CUDA events it orders the streams with and keeps
+ * them for later calls (make that first call outside any stream capture). */
 int moe_forward_overlap_chunks(const moe_forward_args *args);
 moe_status_t moe_forward_host_io_overlapped(const moe_forward_args *args,
                                             const void *x_host, void *y_host,
