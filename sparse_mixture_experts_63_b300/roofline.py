@@ -11,6 +11,10 @@ weights actually read are those of the distinct experts the batch touches):
   bytes = sum over experts with >= 1 kept row of 3*d*f*esize
         + d*N*esize (W_g) + 3*d*fs*esize (shared)
 
+With FP8 E4M3 expert weights a matrix counts one byte per weight plus one
+fp32 scale per output channel, and its FLOPs run at twice the bf16 rate (the
+nominal FP8/bf16 ratio of the dense tensor peaks).
+
 A = kept (token, expert) rows.  Activations are left out of the roofline
 bytes and reported separately.  Roofline time = max(FLOP / tensor peak,
 bytes / HBM bandwidth); the fraction reported is roofline time / measured time.
