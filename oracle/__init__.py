@@ -5,8 +5,9 @@ Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 shares no code with it.
 
 This module is argument marshalling around ``moe_oracle.c`` (ctypes); all the
-arithmetic is in that C file, written as the plain definition in double
-precision.  Inputs are torch CPU tensors (float32 or bfloat16) or numpy
+arithmetic of the layer is in that C file, written as the plain definition in
+double precision (``dequantize_e4m3``, the decoded codes times their scales,
+is a convenience for the tests).  Inputs are torch CPU tensors (float32 or bfloat16) or numpy
 arrays; outputs are numpy arrays (float64 for values, int32 for indices).
 """
 import ctypes
@@ -49,12 +50,16 @@ def _load(path=None):
         lib.oracle_e4m3_encode.restype = None
         lib.oracle_quantize_rows_e4m3.argtypes = [ci, ci, ci, vp, vp, f32p]
         lib.oracle_quantize_weights_e4m3.argtypes = [ci, ci, ci, ci, vp, vp, f32p, ci]
+        lib.oracle_down_rows_e4m3.argtypes = [ci, ci, ci, f64p, vp, f32p, f64p, ci]
+        lib.oracle_expert_rows_e4m3.argtypes = [ci, ci, vp, f32p, vp, f32p, ci, vp, f32p, ci,
+                                                vp, vp, f32p, f64p, ci]
         lib.oracle_moe_forward.argtypes = (
             [ci] * 6 + [vp, vp, f32p, vp, vp, vp, ci, vp, vp, vp, cd, f64p, f64p,
                         i32p, f64p, i32p, i32p, i32p, i32p, ci])
         for name in ("oracle_router_logits", "oracle_topk_softmax", "oracle_capacity",
                      "oracle_group", "oracle_expert_rows", "oracle_combine_rows",
-                     "oracle_moe_forward", "oracle_routing_stats", "oracle_reroute"):
+                     "oracle_moe_forward", "oracle_routing_stats", "oracle_reroute",
+                     "oracle_down_rows_e4m3", "oracle_expert_rows_e4m3"):
             getattr(lib, name).restype = ci
         _lib = lib
     return _lib
@@ -413,26 +418,62 @@ def expert_hidden(W_gate_e, W_up_e, xrows, nthreads=None):
     return h
 
 
+def _u8(a):
+    return np.ascontiguousarray(np.asarray(a), dtype=np.uint8)
+
+
+def _f32(a):
+    if isinstance(a, torch.Tensor):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def down_rows_e4m3(h, qd_e, sd_e, nthreads=None):
+    """E4M3 down projection of hidden rows h [R,f] (fp64): each row quantised
+    per row from its exact values (narrowed to fp32, as the quantiser takes
+    them), times W_down's E4M3 channels (codes [d,f], scales [d]).  Returns
+    out [R,d] fp64 (see moe_oracle.c)."""
+    hh = np.ascontiguousarray(h, dtype=np.float64)
+    R, f = hh.shape
+    qd, sd = _u8(qd_e), _f32(sd_e)
+    d = qd.shape[0]
+    assert qd.shape == (d, f) and sd.shape == (d,)
+    out = np.empty((R, d), dtype=np.float64)
+    _check(_load().oracle_down_rows_e4m3(R, f, d, hh.ctypes.data, qd.ctypes.data,
+                                         sd.ctypes.data, out.ctypes.data,
+                                         nthreads or default_threads()), "oracle_down_rows_e4m3")
+    return out
+
+
 def expert_rows_fp8(qg_e, sg_e, qu_e, su_e, W_down_e, xq_rows, sx_rows, qd_e=None, sd_e=None,
                     nthreads=None):
     """SwiGLU expert with E4M3 gate/up weights (codes [f,d], scales [f]) on E4M3
     token rows (codes [R,d], scales [R]).  Down projection: W_down_e [f,d] as
-    given, or, with qd_e (codes [d,f]) and sd_e (scales [d]), E4M3 too: then h
-    is rounded to bf16 (as the layer stores it) and quantised per row like x
-    before it.  Every value is the exact dequantised one; fp64 throughout."""
-    wg = np.ascontiguousarray(dequantize_e4m3(qg_e, sg_e).T)
-    wu = np.ascontiguousarray(dequantize_e4m3(qu_e, su_e).T)
-    xr = dequantize_e4m3(xq_rows, sx_rows)
+    given, or, with qd_e (codes [d,f]) and sd_e (scales [d]), E4M3 too: the
+    exact hidden row h is quantised per row like a token row before it.
+    Every operand is its exact dequantised value; fp64 throughout, in
+    moe_oracle.c."""
+    qg, qu, qx = _u8(qg_e), _u8(qu_e), _u8(xq_rows)
+    sg, su, sx = _f32(sg_e), _f32(su_e), _f32(sx_rows)
+    f, d = qg.shape
+    R = qx.shape[0]
+    assert qu.shape == (f, d) and qx.shape[1] == d and sx.shape == (R,)
+    out = np.empty((R, d), dtype=np.float64)
+    wd = qd = sd = None
+    wd_dtype, wd_ptr = F32, None
     if qd_e is None:
-        wd = W_down_e.detach().cpu().double().contiguous() \
-            if isinstance(W_down_e, torch.Tensor) \
-            else np.ascontiguousarray(W_down_e, dtype=np.float64)
-        return expert_rows(wg, wu, wd, xr, nthreads)
-    h = expert_hidden(wg, wu, xr, nthreads)
-    qh, sh = quantize_rows_e4m3(torch.from_numpy(h).to(torch.bfloat16))
-    hd = dequantize_e4m3(qh, sh)                          # [R, f]
-    wd = dequantize_e4m3(qd_e, sd_e)                      # [d, f]: row m = output column m
-    return hd @ wd.T                                      # o[r, m] = sum_j h[r, j] wd[m, j]
+        wd = _Buf(W_down_e)
+        assert wd.keep.shape == (f, d)
+        wd_dtype, wd_ptr = wd.dtype, wd.ptr
+    else:
+        qd, sd = _u8(qd_e), _f32(sd_e)
+        assert qd.shape == (d, f) and sd.shape == (d,)
+    _check(_load().oracle_expert_rows_e4m3(
+        d, f, qg.ctypes.data, sg.ctypes.data, qu.ctypes.data, su.ctypes.data, R,
+        qx.ctypes.data, sx.ctypes.data, wd_dtype, wd_ptr,
+        None if qd is None else qd.ctypes.data, None if sd is None else sd.ctypes.data,
+        out.ctypes.data, nthreads or default_threads()), "oracle_expert_rows_e4m3")
+    return out
 
 
 def forward_rows_fp8(xq_rows, sx_rows, topk_idx_rows, topk_w_rows, inv_pos_rows,

@@ -634,10 +634,20 @@ static double e4m3_value(uint8_t c) {
   return s ? -v : v;
 }
 
+/* The 256 code values, filled once from e4m3_value (a lookup, so the loops
+ * below need not recompute the definition for every element). */
+static double e4m3_tab[256];
+static pthread_once_t e4m3_tab_once = PTHREAD_ONCE_INIT;
+static void e4m3_tab_fill(void) {
+  for (int c = 0; c < 256; ++c) e4m3_tab[c] = e4m3_value((uint8_t)c);
+}
+static void e4m3_tab_init(void) { pthread_once(&e4m3_tab_once, e4m3_tab_fill); }
+
 /* Nearest finite E4M3 code to v (|v| > 448 -> +-448), ties to the code with
  * an even mantissa.  The finite non-negative codes 0x00..0x7E have increasing
  * values, so a bisection finds the last code whose value is <= |v|; the
- * answer is that code or the next one, whichever is nearer. */
+ * answer is that code or the next one, whichever is nearer.  Callers run
+ * e4m3_tab_init() first. */
 static uint8_t e4m3_encode(float vf) {
   const double v = (double)vf;
   const uint8_t sign = (v < 0.0 || (v == 0.0 && signbit(v))) ? 0x80 : 0;
@@ -647,9 +657,9 @@ static uint8_t e4m3_encode(float vf) {
   int lo = 0, hi = 0x7E;                       /* value(lo) <= a < value(hi) */
   while (hi - lo > 1) {
     const int mid = (lo + hi) / 2;
-    if (e4m3_value((uint8_t)mid) <= a) lo = mid; else hi = mid;
+    if (e4m3_tab[mid] <= a) lo = mid; else hi = mid;
   }
-  const double dlo = a - e4m3_value((uint8_t)lo), dhi = e4m3_value((uint8_t)hi) - a;
+  const double dlo = a - e4m3_tab[lo], dhi = e4m3_tab[hi] - a;
   int c;
   if (dlo < dhi) c = lo;
   else if (dhi < dlo) c = hi;
@@ -662,6 +672,7 @@ void oracle_e4m3_decode(long n, const uint8_t *codes, double *out) {
 }
 
 void oracle_e4m3_encode(long n, const float *v, uint8_t *codes) {
+  e4m3_tab_init();
   for (long i = 0; i < n; ++i) codes[i] = e4m3_encode(v[i]);
 }
 
@@ -686,6 +697,7 @@ static void quantize_vector(const void *p, int dtype, size_t base, size_t stride
 int oracle_quantize_rows_e4m3(int R, int C, int dtype, const void *x, uint8_t *q,
                               float *scale) {
   if (R < 0 || C < 1 || (R > 0 && (!x || !q || !scale))) return 1;
+  e4m3_tab_init();
   for (int r = 0; r < R; ++r)
     quantize_vector(x, dtype, (size_t)r * C, 1, C, q + (size_t)r * C, 1, scale + r);
   return 0;
@@ -713,7 +725,122 @@ static void quantize_channels(long lo, long hi, void *p) {
 int oracle_quantize_weights_e4m3(int N, int d, int f, int dtype, const void *W, uint8_t *q,
                                  float *scale, int nthreads) {
   if (N < 1 || d < 1 || f < 1 || !W || !q || !scale) return 1;
+  e4m3_tab_init();
   qw_ctx c = {d, f, dtype, W, q, scale};
   parallel_for((long)N * f, nthreads, quantize_channels, &c);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* The SwiGLU expert with E4M3 operands (same sources and reading as above).  */
+/* Every operand is its exact dequantised value, decode(code) * scale, and    */
+/* the arithmetic is the expert of step 6 in double precision:                */
+/*   x_r[i]   = decode(qx[r, i]) * sx[r]            (token row, per-row scale)  */
+/*   g[j]     = sum_i x_r[i] * decode(qg[j, i]) * sg[j]   (gate channel j)      */
+/*   u[j]     = sum_i x_r[i] * decode(qu[j, i]) * su[j]   (up channel j)        */
+/*   h[j]     = g[j] / (1 + exp(-g[j])) * u[j]                                 */
+/* and the down projection either from W_down [f, d] as given,                */
+/*   out[m]   = sum_j h[j] * W_down[j, m],                                     */
+/* or in E4M3 too: the row h (its exact values, narrowed to fp32 as the       */
+/* quantiser's definition takes them) is quantised like a token row, codes    */
+/* hq[j] and one scale hs, and with W_down's channel m stored as codes        */
+/* qd[m, j] (channel-major [d, f]) and scale sd[m]:                            */
+/*   out[m]   = sum_j decode(hq[j]) * hs * decode(qd[m, j]) * sd[m].           */
+/* ------------------------------------------------------------------------- */
+
+/* E4M3 down projection of R rows h [R, f] (double): out [R, d]. */
+typedef struct {
+  int f, d;
+  const double *h;
+  const uint8_t *qd;
+  const float *sd;
+  double *out;
+} down8_ctx;
+
+static void down8_row(const down8_ctx *c, long r, uint8_t *hq) {
+  float hs;
+  quantize_vector(c->h, ORACLE_F64, (size_t)r * c->f, 1, c->f, hq, 1, &hs);
+  double *o = c->out + (size_t)r * c->d;
+  for (int m = 0; m < c->d; ++m) {
+    const uint8_t *wq = c->qd + (size_t)m * c->f;
+    double acc = 0.0;
+    for (int j = 0; j < c->f; ++j)
+      acc += (e4m3_tab[hq[j]] * (double)hs) * (e4m3_tab[wq[j]] * (double)c->sd[m]);
+    o[m] = acc;
+  }
+}
+
+static void down8_rows(long lo, long hi, void *p) {
+  down8_ctx *c = (down8_ctx *)p;
+  uint8_t *hq = (uint8_t *)malloc((size_t)c->f);
+  if (!hq) return;
+  for (long r = lo; r < hi; ++r) down8_row(c, r, hq);
+  free(hq);
+}
+
+int oracle_down_rows_e4m3(int R, int f, int d, const double *h, const uint8_t *qd,
+                          const float *sd, double *out, int nthreads) {
+  if (R < 0 || f < 1 || d < 1 || !qd || !sd || (R > 0 && (!h || !out))) return 1;
+  e4m3_tab_init();
+  down8_ctx c = {f, d, h, qd, sd, out};
+  parallel_for(R, nthreads, down8_rows, &c);
+  return 0;
+}
+
+/* The whole E4M3 expert on R token rows.  Down projection: Wd [f, d] in
+ * wd_dtype when qd is NULL, else the E4M3 form (qd [d, f], sd [d]). */
+typedef struct {
+  int d, f, wd_dtype;
+  const uint8_t *qg, *qu, *qx, *qd;
+  const float *sg, *su, *sx, *sd;
+  const void *Wd;
+  double *out;
+} exp8_ctx;
+
+static void exp8_rows(long lo, long hi, void *p) {
+  exp8_ctx *c = (exp8_ctx *)p;
+  double *xr = (double *)malloc(sizeof(double) * (size_t)c->d);
+  double *h = (double *)malloc(sizeof(double) * (size_t)c->f);
+  uint8_t *hq = (uint8_t *)malloc((size_t)c->f);
+  if (!xr || !h || !hq) {
+    free(xr); free(h); free(hq);
+    return;
+  }
+  for (long r = lo; r < hi; ++r) {
+    for (int i = 0; i < c->d; ++i)
+      xr[i] = e4m3_tab[c->qx[(size_t)r * c->d + i]] * (double)c->sx[r];
+    for (int j = 0; j < c->f; ++j) {
+      const uint8_t *wg = c->qg + (size_t)j * c->d, *wu = c->qu + (size_t)j * c->d;
+      double g = 0.0, u = 0.0;
+      for (int i = 0; i < c->d; ++i) {
+        g += xr[i] * (e4m3_tab[wg[i]] * (double)c->sg[j]);
+        u += xr[i] * (e4m3_tab[wu[i]] * (double)c->su[j]);
+      }
+      h[j] = g / (1.0 + exp(-g)) * u;
+    }
+    double *o = c->out + (size_t)r * c->d;
+    if (c->qd) {
+      down8_ctx dc = {c->f, c->d, h, c->qd, c->sd, o};
+      down8_row(&dc, 0, hq);
+    } else {
+      for (int m = 0; m < c->d; ++m) o[m] = 0.0;
+      for (int j = 0; j < c->f; ++j)
+        for (int m = 0; m < c->d; ++m)
+          o[m] += h[j] * elem(c->Wd, c->wd_dtype, (size_t)j * c->d + m);
+    }
+  }
+  free(xr); free(h); free(hq);
+}
+
+int oracle_expert_rows_e4m3(int d, int f, const uint8_t *qg, const float *sg,
+                            const uint8_t *qu, const float *su, int R, const uint8_t *qx,
+                            const float *sx, int wd_dtype, const void *Wd, const uint8_t *qd,
+                            const float *sd, double *out, int nthreads) {
+  if (d < 1 || f < 1 || R < 0 || !qg || !sg || !qu || !su || (!Wd && !qd) ||
+      (qd && !sd) || (R > 0 && (!qx || !sx || !out)))
+    return 1;
+  e4m3_tab_init();
+  exp8_ctx c = {d, f, wd_dtype, qg, qu, qx, qd, sg, su, sx, sd, Wd, out};
+  parallel_for(R, nthreads, exp8_rows, &c);
   return 0;
 }

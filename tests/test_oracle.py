@@ -682,28 +682,76 @@ def test_expert_hidden_is_the_first_half_of_the_expert():
                                rtol=1e-14)
 
 
-def test_fp8_down_projection_uses_channel_and_row_scales():
-    """An E4M3 down projection with exactly representable W_down equals the
-    down projection of the quantised h (bf16-rounded, per-row E4M3) with W_down
-    itself; scales on the wrong axis would not."""
+def _codes(rng, shape, absmax_col=None):
+    """Random finite E4M3 codes with random signs; column absmax_col (if given)
+    holds +-448 so that every row's absmax is exactly 448."""
+    c = rng.integers(0, 0x7E, size=shape).astype(np.uint8) | \
+        (rng.integers(0, 2, size=shape).astype(np.uint8) << 7)
+    if absmax_col is not None:
+        c[..., absmax_col] = (c[..., absmax_col] & 0x80) | 0x7E
+    return c
+
+
+def test_fp8_down_rows_exact_on_representable_h():
+    """Rows of h that are E4M3 codes times a per-row power of two (each row's
+    absmax maps to 448) quantise exactly, and W_down channels that are codes
+    times a per-channel power of two too: the E4M3 down projection is then the
+    exact product h W_down.  Rows and channels get different scales and f != d,
+    so a scale on the wrong axis or row, a dropped scale or a transposed W_down
+    gives another result."""
+    rng = np.random.default_rng(29)
+    R, f, d = 7, 40, 24
+    ch = _codes(rng, (R, f), absmax_col=3)
+    hs = 2.0 ** rng.integers(-6, 6, size=R)
+    h = oracle.e4m3_decode(ch) * hs[:, None]
+    cd = _codes(rng, (d, f), absmax_col=11)
+    sd = (2.0 ** rng.integers(-12, -4, size=d)).astype(np.float32)
+    Wd = (oracle.e4m3_decode(cd) * sd[:, None]).T        # [f, d]: the matrix itself
+    got = oracle.down_rows_e4m3(h, cd, sd)
+    np.testing.assert_allclose(got, h @ Wd, rtol=1e-13, atol=1e-300)
+    # one-hot rows (values 448 times a power of two: exact scales) read out
+    # W_down's rows, scaled by the row's value
+    eye = np.zeros((3, f))
+    eye[0, 0], eye[1, 5], eye[2, f - 1] = 448.0, -448.0 * 2.0 ** -3, 448.0 * 2.0 ** -9
+    np.testing.assert_allclose(oracle.down_rows_e4m3(eye, cd, sd),
+                               eye[:, [0, 5, f - 1]].sum(1)[:, None] * Wd[[0, 5, f - 1]],
+                               rtol=1e-14)
+
+
+def test_fp8_down_quantises_the_unrounded_h():
+    """h is quantised from its own values, not from a bf16-rounded copy:
+    1.0625 + 2^-12 (above the tie between 1.0 and 1.125) becomes 1.125, while
+    its bf16 rounding (1.0625, exactly the tie) would become 1.0 (ties to even)."""
+    f, d = 16, 2
+    h = np.zeros((1, f))
+    h[0, 0], h[0, 1] = 1.0625 + 2.0 ** -12, 448.0            # absmax 448: scale 1
+    cd = np.zeros((d, f), dtype=np.uint8)
+    cd[0, 0] = 0x38                                          # W_down[0, 0] = 1.0
+    cd[1, 1] = 0x38                                          # W_down[1, 1] = 1.0
+    out = oracle.down_rows_e4m3(h, cd, np.ones(d, dtype=np.float32))
+    assert out.tolist() == [[1.125, 448.0]]
+
+
+def test_fp8_expert_down_is_hidden_then_down():
+    """The E4M3 expert with an E4M3 down projection is its hidden activation
+    (pinned through the bf16 expert above) followed by the E4M3 down
+    projection (pinned above), row by row."""
     rng = np.random.default_rng(23)
     R, d, f = 6, 32, 48
     x = torch.from_numpy(rng.normal(size=(R, d))).to(torch.bfloat16)
     Wg = torch.from_numpy(rng.normal(size=(d, f)) / d ** 0.5).to(torch.bfloat16)
     Wu = torch.from_numpy(rng.normal(size=(d, f)) / d ** 0.5).to(torch.bfloat16)
-    cd = rng.integers(0, 0x7E, size=(d, f)).astype(np.uint8) | \
-        (rng.integers(0, 2, size=(d, f)).astype(np.uint8) << 7)
-    cd[:, 1] = 0x7E
-    sd = 2.0 ** rng.integers(-12, -8, size=d)
-    Wd = torch.from_numpy((oracle.e4m3_decode(cd) * sd[:, None]).T.copy()).to(torch.bfloat16)
+    Wd = torch.from_numpy(rng.normal(size=(f, d)) / f ** 0.5).to(torch.bfloat16)
     qx, sx = oracle.quantize_rows_e4m3(x)
     (qg, sg), (qu, su) = oracle.quantize_weights_e4m3(Wg[None]), oracle.quantize_weights_e4m3(Wu[None])
     (qd, sdq) = oracle.quantize_weights_e4m3(Wd[None])
-    np.testing.assert_array_equal(qd[0], cd)
-    got = oracle.expert_rows_fp8(qg[0], sg[0], qu[0], su[0], Wd, qx, sx, qd[0], sdq[0])
+    got = oracle.expert_rows_fp8(qg[0], sg[0], qu[0], su[0], None, qx, sx, qd[0], sdq[0])
     h = oracle.expert_hidden(np.ascontiguousarray(oracle.dequantize_e4m3(qg[0], sg[0]).T),
                              np.ascontiguousarray(oracle.dequantize_e4m3(qu[0], su[0]).T),
                              oracle.dequantize_e4m3(qx, sx))
-    qh, sh = oracle.quantize_rows_e4m3(torch.from_numpy(h).to(torch.bfloat16))
-    ref = oracle.dequantize_e4m3(qh, sh) @ Wd.double().numpy()
-    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(got, oracle.down_rows_e4m3(h, qd[0], sdq[0]), rtol=1e-12,
+                               atol=1e-14)
+    # and the E4M3 down projection stays close to the exact one (a loose bound
+    # that a lost or misplaced scale breaks)
+    exact = h @ Wd.double().numpy()
+    assert np.linalg.norm(got - exact) / np.linalg.norm(exact) < 0.1

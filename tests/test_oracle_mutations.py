@@ -58,6 +58,28 @@ MUTANTS = [
     ("fp8_weights_input_axis",
      "quantize_vector(c->W, c->dtype, (size_t)e * c->d * c->f + j, (size_t)c->f, c->d,",
      "quantize_vector(c->W, c->dtype, (size_t)e * c->d * c->f + (size_t)j * c->d, 1, c->d,"),
+    # the E4M3 down projection of the hidden rows
+    ("fp8_h_row_scale_dropped", "(e4m3_tab[hq[j]] * (double)hs)", "(e4m3_tab[hq[j]])"),
+    ("fp8_down_channel_scale_dropped", "(e4m3_tab[wq[j]] * (double)c->sd[m])",
+     "(e4m3_tab[wq[j]])"),
+    ("fp8_h_scale_of_row0",
+     "quantize_vector(c->h, ORACLE_F64, (size_t)r * c->f, 1, c->f, hq, 1, &hs);",
+     "quantize_vector(c->h, ORACLE_F64, 0, 1, c->f, hq, 1, &hs);"),
+    ("fp8_down_transposed", "(e4m3_tab[wq[j]] * (double)c->sd[m])",
+     "(e4m3_tab[c->qd[(size_t)j * c->d + m]] * (double)c->sd[m])"),
+    ("fp8_h_rounded_to_bf16",
+     "quantize_vector(c->h, ORACLE_F64, (size_t)r * c->f, 1, c->f, hq, 1, &hs);",
+     "double *hb = (double *)malloc(sizeof(double) * (size_t)c->f);\n"
+     "  for (int j = 0; j < c->f; ++j) {\n"
+     "    float v = (float)c->h[(size_t)r * c->f + j];\n"
+     "    uint32_t b;\n"
+     "    memcpy(&b, &v, 4);\n"
+     "    b = (b + 0x7FFFu + ((b >> 16) & 1u)) & 0xFFFF0000u;\n"
+     "    memcpy(&v, &b, 4);\n"
+     "    hb[j] = v;\n"
+     "  }\n"
+     "  quantize_vector(hb, ORACLE_F64, 0, 1, c->f, hq, 1, &hs);\n"
+     "  free(hb);"),
 ]
 
 
