@@ -121,6 +121,7 @@ struct TcParams {
   const float *wscale_u;   // [N, M] up channel scales (GEMM1)
   const float *xscale;     // row scales: [T] by token (GEMM1) or [A] by permuted row (GEMM2)
   const int32_t *perm_token;  // [A] token of each permuted row (GEMM1), else null
+  int out_f32;             // GEMM1: h written in fp32 (out holds floats), else bf16
 };
 
 // Token sub-tiles of a tile: rows [row0, row0 + rows0) and, for a wide tile
@@ -257,7 +258,9 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams &p, const TileInfo
     tc::named_bar(1, kEpiThreads);
     const float4 *other4 =
         reinterpret_cast<const float4 *>(xbuf + (gate_side ? 0 : kXHalf) + hr * kXPitch);
+    // h of token column c (this side's 16) and hidden unit hr at [c * 64 + hr]
     __nv_bfloat16 *ob = obuf + (gate_side ? 0 : 16 * 64);
+    float *obf = reinterpret_cast<float *>(obuf) + (gate_side ? 0 : 16 * 64);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const float4 o4 = other4[q];
@@ -268,21 +271,38 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams &p, const TileInfo
         const float g = gate_side ? __uint_as_float(r[c]) : o[i];
         const float u = gate_side ? o[i] : __uint_as_float(r[16 + c]);
         const float h = __fdividef(g, 1.f + __expf(-g)) * u;
-        ob[c * 64 + hr] = __float2bfloat16_rn(h);
+        if (p.out_f32)
+          obf[c * 64 + hr] = h;
+        else
+          ob[c * 64 + hr] = __float2bfloat16_rn(h);
       }
     }
     tc::named_bar(1, kEpiThreads);
-    // copy out: ncols token rows x 64 hidden units (128 B) each.  The next
-    // chunk writes obuf only after its exchange barrier, which every thread
-    // reaches after finishing this copy.
+    // copy out: ncols token rows x 64 hidden units (128 B in bf16, 256 B in
+    // fp32) each.  The next chunk writes obuf only after its exchange barrier,
+    // which every thread reaches after finishing this copy.
     const int m0 = ti.pair * 128 + rank * 64;
-    const int vec_valid = max(0, min(8, (p.M - m0) / 8));
-    for (int q = etid; q < ncols * 8; q += kEpiThreads) {
-      const int c = q / 8, v = q % 8;
-      if (v < vec_valid) {
-        const uint4 val = *reinterpret_cast<const uint4 *>(obuf + c * 64 + v * 8);
-        *reinterpret_cast<uint4 *>(p.out + (size_t)(srow0 + cc * 32 + c) * p.out_ld + m0 +
-                                   v * 8) = val;
+    if (p.out_f32) {
+      const float *src = reinterpret_cast<const float *>(obuf);
+      float *dst = reinterpret_cast<float *>(p.out);
+      const int vec_valid = max(0, min(16, (p.M - m0) / 4));
+      for (int q = etid; q < ncols * 16; q += kEpiThreads) {
+        const int c = q / 16, v = q % 16;
+        if (v < vec_valid) {
+          const uint4 val = *reinterpret_cast<const uint4 *>(src + c * 64 + v * 4);
+          *reinterpret_cast<uint4 *>(dst + (size_t)(srow0 + cc * 32 + c) * p.out_ld + m0 +
+                                     v * 4) = val;
+        }
+      }
+    } else {
+      const int vec_valid = max(0, min(8, (p.M - m0) / 8));
+      for (int q = etid; q < ncols * 8; q += kEpiThreads) {
+        const int c = q / 8, v = q % 8;
+        if (v < vec_valid) {
+          const uint4 val = *reinterpret_cast<const uint4 *>(obuf + c * 64 + v * 8);
+          *reinterpret_cast<uint4 *>(p.out + (size_t)(srow0 + cc * 32 + c) * p.out_ld + m0 +
+                                     v * 8) = val;
+        }
       }
     }
   } else {
@@ -862,8 +882,10 @@ moe_status_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, const flo
                      stream);
 }
 
+// h in bf16 (bf16 down projection), or in fp32 followed by its E4M3 codes
+// and row scales (E4M3 down projection: the row quantiser sees h unrounded).
 size_t ffn_fp8_workspace_bytes(int A_max, int f, bool fp8_down) {
-  size_t b = align_up((size_t)A_max * f * 2, 256);                 // h, bf16
+  size_t b = align_up((size_t)A_max * f * (fp8_down ? 4 : 2), 256);
   if (fp8_down)
     b += align_up((size_t)A_max * f, 256) + align_up((size_t)A_max * 4, 256);  // hq, its scales
   return b;
@@ -871,9 +893,10 @@ size_t ffn_fp8_workspace_bytes(int A_max, int f, bool fp8_down) {
 
 // The same with E4M3 gate/up: xq_perm [A_max, d] E4M3 token rows (scale of
 // permuted row p: x_scale[perm_token[p]]), Wq_gate / Wq_up [N, f, d] E4M3
-// with channel scales [N, f]; h is written in bf16.  The down projection is
-// bf16 from W_down, or, with Wq_down [N, d, f] and its channel scales [N, d],
-// E4M3 on h quantised per row (rows past offsets[N] left alone).
+// with channel scales [N, f].  The down projection is bf16 from W_down on h
+// written in bf16, or, with Wq_down [N, d, f] and its channel scales [N, d],
+// E4M3 on h written in fp32 and quantised per row from those values (rows
+// past offsets[N] left alone).
 moe_status_t launch_ffn_tc_fp8(const void *xq_perm, const float *x_scale,
                                const int32_t *perm_token, const int32_t *offsets,
                                const float *row_scale, int A_max, int d, int f, int N,
@@ -886,7 +909,9 @@ moe_status_t launch_ffn_tc_fp8(const void *xq_perm, const float *x_scale,
   if (s != MOE_OK) return s;
   char *ws = static_cast<char *>(workspace);
   void *h = ws;
-  uint8_t *hq = reinterpret_cast<uint8_t *>(ws + align_up((size_t)A_max * f * 2, 256));
+  const bool h_f32 = Wq_down != nullptr;
+  uint8_t *hq = reinterpret_cast<uint8_t *>(ws + align_up((size_t)A_max * f * (h_f32 ? 4 : 2),
+                                                          256));
   float *hs = reinterpret_cast<float *>(reinterpret_cast<char *>(hq) +
                                         align_up((size_t)A_max * f, 256));
   CUtensorMap wg, wu, bx[kNumBoxes];
@@ -906,13 +931,13 @@ moe_status_t launch_ffn_tc_fp8(const void *xq_perm, const float *x_scale,
   const TileCfg c = tile_config(A_max, N, capacity);
   TcParams p1{offsets, N, d, f, (f + 127) / 128, 1, static_cast<__nv_bfloat16 *>(h), f, nullptr,
               device_status, raster_group(d), c.tile_cap, c.wide, c.stages, c.stage_bytes,
-              sw_gate, sw_up, x_scale, perm_token};
+              sw_gate, sw_up, x_scale, perm_token, h_f32 ? 1 : 0};
   s = launch_gemm<true>(wg, wu, bx, p1, stream);
   if (s != MOE_OK) return s;
   if (!Wq_down)
     return launch_down(offsets, row_scale, A_max, d, f, N, c, W_down, h, y_perm, device_status,
                        stream);
-  s = launch_quantize_rows_e4m3(h, A_max, f, hq, hs, stream, offsets + N);
+  s = launch_quantize_rows_e4m3(h, A_max, f, hq, hs, stream, offsets + N, /*f32_in=*/true);
   if (s != MOE_OK) return s;
   TcParams p2{offsets, N, f, d, (d + 255) / 256, 0, static_cast<__nv_bfloat16 *>(y_perm), d,
               row_scale, device_status, raster_group(f), c.tile_cap, c.wide, c.stages,

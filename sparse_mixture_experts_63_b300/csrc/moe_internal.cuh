@@ -131,10 +131,12 @@ moe_status_t launch_copy_rows(const void *x, moe_dtype_t dtype, const int32_t *i
 moe_status_t launch_copy_row_bytes(const void *x, size_t row_bytes, const int32_t *inv_pos,
                                    int T, int k, void *x_perm, cudaStream_t stream);
 
-// FP8 E4M3 with absmax scales: rows of x [R, C] bf16 -> codes [R, C] + [R]
-// scales; gate/up weights W [N, d, f] bf16 -> codes [N, f, d] + [N, f].
+// FP8 E4M3 with absmax scales: rows of x [R, C] bf16 (fp32 with f32_in) ->
+// codes [R, C] + [R] scales; gate/up weights W [N, d, f] bf16 -> codes
+// [N, f, d] + [N, f].
 moe_status_t launch_quantize_rows_e4m3(const void *x, int R, int C, uint8_t *q, float *scale,
-                                       cudaStream_t stream, const int32_t *rows_valid = nullptr);
+                                       cudaStream_t stream, const int32_t *rows_valid = nullptr,
+                                       bool f32_in = false);
 moe_status_t launch_quantize_weights_e4m3(const void *W, int N, int d, int f, uint8_t *q,
                                           float *scale, cudaStream_t stream);
 // The dispatch row copy with the rows quantised on the way (codes of token t

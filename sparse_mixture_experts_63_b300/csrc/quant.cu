@@ -27,9 +27,10 @@ __device__ __forceinline__ uint8_t to_e4m3(float v) {
 }
 
 // G threads per row (G a power of two, 32..256; 256 / G rows per CTA,
-// grid-stride over row batches); C % 8 == 0, 16-byte rows.  With rows_valid,
-// rows from *rows_valid on are left alone.
-__global__ void __launch_bounds__(256) quantize_rows_e4m3(const __nv_bfloat16 *__restrict__ x,
+// grid-stride over row batches); C % 8 == 0, 16-byte rows of bf16 or fp32
+// values.  With rows_valid, rows from *rows_valid on are left alone.
+template <typename TIn>
+__global__ void __launch_bounds__(256) quantize_rows_e4m3(const TIn *__restrict__ x,
                                                           int R, int C, int G,
                                                           uint8_t *__restrict__ q,
                                                           float *__restrict__ scale,
@@ -45,12 +46,12 @@ __global__ void __launch_bounds__(256) quantize_rows_e4m3(const __nv_bfloat16 *_
   for (long b = blockIdx.x; b * rpc < R; b += gridDim.x) {
     const long r = b * rpc + grp;
     const bool active = r < R;
-    const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)(active ? r : 0) * C);
+    const TIn *row = x + (size_t)(active ? r : 0) * C;
     float am = 0.f;
     if (active)
       for (int v = lg; v < nv; v += G) {
         float f[8];
-        load8(reinterpret_cast<const __nv_bfloat16 *>(row + v), f);
+        load8(row + 8 * v, f);
 #pragma unroll
         for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
       }
@@ -70,7 +71,7 @@ __global__ void __launch_bounds__(256) quantize_rows_e4m3(const __nv_bfloat16 *_
       uint2 *out = reinterpret_cast<uint2 *>(q + (size_t)r * C);
       for (int v = lg; v < nv; v += G) {
         float f[8];
-        load8(reinterpret_cast<const __nv_bfloat16 *>(row + v), f);
+        load8(row + 8 * v, f);
         uint32_t w[2] = {0u, 0u};
 #pragma unroll
         for (int i = 0; i < 8; ++i) w[i / 4] |= (uint32_t)to_e4m3(f[i] * inv) << (8 * (i % 4));
@@ -183,7 +184,8 @@ __global__ void __launch_bounds__(256) quantize_weights_e4m3(
 }  // namespace
 
 moe_status_t launch_quantize_rows_e4m3(const void *x, int R, int C, uint8_t *q, float *scale,
-                                       cudaStream_t stream, const int32_t *rows_valid) {
+                                       cudaStream_t stream, const int32_t *rows_valid,
+                                       bool f32_in) {
   if (R == 0) return MOE_OK;
   // threads per row: enough for a few 16-byte vectors each, 32..256
   const int nv = C / 8;
@@ -192,8 +194,13 @@ moe_status_t launch_quantize_rows_e4m3(const void *x, int R, int C, uint8_t *q, 
   const long rpc = 256 / G;
   long grid = ((long)R + rpc - 1) / rpc;
   if (grid > 148L * 8) grid = 148L * 8;
-  MOE_CUDA_TRY(launch_pdl(quantize_rows_e4m3, dim3((int)grid), dim3(256), 0, stream,
-      static_cast<const __nv_bfloat16 *>(x), R, C, G, q, scale, rows_valid));
+  if (f32_in)
+    MOE_CUDA_TRY(launch_pdl(quantize_rows_e4m3<float>, dim3((int)grid), dim3(256), 0, stream,
+                            static_cast<const float *>(x), R, C, G, q, scale, rows_valid));
+  else
+    MOE_CUDA_TRY(launch_pdl(quantize_rows_e4m3<__nv_bfloat16>, dim3((int)grid), dim3(256), 0,
+                            stream, static_cast<const __nv_bfloat16 *>(x), R, C, G, q, scale,
+                            rows_valid));
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
