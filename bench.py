@@ -45,6 +45,7 @@ from sparse_mixture_experts_63_b300.configs import CONFIGS  # noqa: E402
 from sparse_mixture_experts_63_b300.inputs import make_inputs, make_x  # noqa: E402
 
 L2_FLUSH_BYTES = 256 << 20   # > 126 MB L2
+METRIC = "MoE-layer tokens/s on 1 B300 and % of roofline (active FLOPs vs expert bytes)"
 BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 
 
@@ -76,60 +77,135 @@ def parse():
                     help="with --fp8: the down projection in FP8 E4M3 too (h quantised per row)")
     ap.add_argument("--forward-only", action="store_true",
                     help="time moe_forward only (no stage, end-to-end or CPU legs)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the forward-only timing of the other bf16 workloads that the "
+                         "default (prefill) run appends as `workloads`")
     return ap.parse_args()
 
 
 # ---------------------------------------------------------------- clocks ----
 class ClockSampler:
+    """SM clock and clock-event reasons of one GPU, read (never set) through
+    NVML every 10 ms on a background thread while the benchmark runs; the
+    summary covers the samples taken inside the timed window only.  Falls
+    back to `nvidia-smi -lms 100` when NVML cannot be loaded."""
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = os.path.join(tempfile.gettempdir(),
-                                 f"moe_bench_clocks_gpu{gpu_index}_{os.getpid()}.csv")
+    def __init__(self, torch_index, period_s=0.01):
+        self.torch_index = torch_index
+        self.period = period_s
+        self.samples = []          # (host time, sm MHz, max sm MHz, reason bits)
+        self.window = None
+        self._stop = None
+        self._thread = None
+        self._proc = None
+        self.source = "unsampled"
+
+    def _nvml_handle(self):
+        import pynvml
+        pynvml.nvmlInit()
+        uuid = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.torch_index).uuid)
+        except Exception:
+            pass
+        if uuid:
+            u = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            try:
+                return pynvml, pynvml.nvmlDeviceGetHandleByUUID(u)
+            except Exception:
+                pass
+        return pynvml, pynvml.nvmlDeviceGetHandleByIndex(self.torch_index)
 
     def start(self):
+        import threading
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            nv, h = self._nvml_handle()
+            smax = float(nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM))
+            get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons",
+                                  None) or nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        except Exception:
+            return self._start_smi()
+        self.source = f"nvml every {self.period * 1e3:.0f} ms"
+        self._stop = threading.Event()
+
+        def run():
+            while not self._stop.is_set():
+                try:
+                    self.samples.append((time.perf_counter(),
+                                         float(nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)),
+                                         smax, int(get_reasons(h))))
+                except Exception:
+                    pass
+                self._stop.wait(self.period)
+        self._thread = threading.Thread(target=run, daemon=True)
+        self._thread.start()
+
+    def _start_smi(self):
+        self.path = os.path.join(tempfile.gettempdir(),
+                                 f"moe_bench_clocks_{os.getpid()}_{self.torch_index}.csv")
+        try:
             self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.torch_index), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
+            self.source = "nvidia-smi every 100 ms"
         except (OSError, FileNotFoundError):
-            self.proc = None
+            self._proc = None
+
+    def mark(self, t0, t1):
+        """The timed window, in time.perf_counter() seconds."""
+        self.window = (t0, t1)
 
     def stop(self):
-        if self.proc is None:
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=2)
+            rows = list(self.samples)
+        elif self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._proc.kill()
+            self.fh.close()
+            rows = []
+            with open(self.path) as fh:   # no host timestamps: the whole run counts
+                for line in fh:
+                    p = [q.strip() for q in line.split(",")]
+                    try:
+                        bits = sum(self.BITS[n] for n, v in zip(
+                            ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                             "sw_power_cap"), p[5:9]) if v.lower() == "active")
+                        rows.append((None, float(p[1]), float(p[2]), bits))
+                    except (ValueError, IndexError):
+                        continue
+        else:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.fh.close()
-        sm, smax, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        with open(self.path) as fh:
-            for line in fh:
-                p = [q.strip() for q in line.split(",")]
-                if len(p) < 9:
-                    continue
-                try:
-                    sm.append(float(p[1]))
-                    smax.append(float(p[2]))
-                except ValueError:
-                    continue
-                for n, v in zip(names, p[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "samples": len(sm), "reasons": sorted(reasons)}
+        if self.window is not None and rows and rows[0][0] is not None:
+            t0, t1 = self.window
+            inside = [r for r in rows if t0 <= r[0] <= t1]
+        else:
+            inside = rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"],
+                    "source": self.source}
+        counts = {n: sum(1 for r in inside if r[3] & b) for n, b in self.BITS.items()}
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside),
+                "sm_min_mhz": min(r[1] for r in inside),
+                "samples": len(inside), "reasons": sorted(n for n, c in counts.items() if c),
+                "reason_samples": {n: c for n, c in counts.items() if c},
+                "source": self.source + ", timed window only"}
+
+
+def clocks_rejected(clocks):
+    return any(r in clocks.get("reasons", []) for r in BAD_REASONS)
 
 
 # --------------------------------------------------------------- helpers ----
@@ -274,7 +350,10 @@ def cpu_baseline(cfg, dev_inp, seconds):
 
 
 # ------------------------------------------------------------ our arm -------
-def run_ours(args, ws, rank, local):
+WORKLOADS_ALSO = ("deepseek", "mixtral_decode", "capacity")
+
+
+def resolve_cfg(args):
     cfg = CONFIGS[args.config]
     if args.tokens:
         cfg = cfg.scaled(T=args.tokens)
@@ -282,59 +361,199 @@ def run_ours(args, ws, rank, local):
         cfg = cfg.scaled(N=args.experts)
     if args.ffn_dim:
         cfg = cfg.scaled(f=args.ffn_dim, fs=args.ffn_dim if cfg.fs else 0)
-    dev = torch.device("cuda", local)
-    inp = make_inputs(cfg, device=dev)
-    # each rank gets its own batch of the same layer
-    if rank > 0:
-        inp.x = make_x(cfg, device=dev, seed=cfg.seed * 1000 + rank)
-    y_dtype = torch.float32 if args.y_dtype == "f32" else torch.bfloat16
-    layer = B.MoELayer(inp.W_g, inp.W_gate, inp.W_up, inp.W_down, cfg.k, bias=inp.bias,
-                       Ws_gate=inp.Ws_gate, Ws_up=inp.Ws_up, Ws_down=inp.Ws_down,
-                       capacity_factor=cfg.cf, y_dtype=y_dtype, reroute_rounds=args.reroute,
-                       fp8=args.fp8, fp8_down=args.fp8 and args.fp8_down)
-    y = torch.empty((cfg.T, cfg.d), dtype=y_dtype, device=dev)
-    outs = layer.outputs_for(cfg.T, dev)
-    a = layer.args(inp.x, y, outs)
-    wsbuf = layer.workspace(a, dev)
-    stream = torch.cuda.current_stream()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    return cfg
 
-    def step():
-        B.moe_forward(a, wsbuf, stream)
 
-    sampler = ClockSampler(local)
-    sampler.start()
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
+def dtype_name(cfg, fp8, fp8_down):
+    if fp8_down:
+        return "e4m3 experts + bf16"
+    if fp8:
+        return "e4m3 gate/up + bf16"
+    return "bf16" if cfg.dtype == "bf16" else "f32"
 
-    def timed_loop():
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
+
+def config_dict(cfg, ws, fp8=False, fp8_down=False, reroute=0, y_dtype="f32"):
+    """The workload as both arms name it (same keys and values)."""
+    return {"workload": cfg_desc(cfg) + (f", overflow re-routed in {reroute} rounds"
+                                         if reroute else "")
+            + (", gate/up" + (" and down" if fp8_down else "") +
+               " in FP8 E4M3 (per-channel / per-row absmax scales)" if fp8 else ""),
+            "fp8_gate_up": bool(fp8), "fp8_down": bool(fp8_down), "reroute_rounds": reroute,
+            "T": cfg.T, "d": cfg.d, "f": cfg.f, "N": cfg.N, "k": cfg.k, "fs": cfg.fs,
+            "capacity_factor": cfg.cf, "bias_std": cfg.bias_std, "y_dtype": y_dtype,
+            "parallelism": f"replicas x{ws} (no exchange)",
+            "l2": "256 MB L2 flush write between steps, outside the timed events; "
+                  "weights also exceed L2"}
+
+
+class Bench:
+    """One layer set up for timing: inputs, weights, outputs, workspace."""
+
+    def __init__(self, cfg, dev, rank=0, reroute=0, fp8=False, fp8_down=False,
+                 y_dtype=torch.float32):
+        self.cfg = cfg
+        self.inp = make_inputs(cfg, device=dev)
+        if rank > 0:   # each rank gets its own batch of the same layer
+            self.inp.x = make_x(cfg, device=dev, seed=cfg.seed * 1000 + rank)
+        inp = self.inp
+        self.layer = B.MoELayer(inp.W_g, inp.W_gate, inp.W_up, inp.W_down, cfg.k, bias=inp.bias,
+                                Ws_gate=inp.Ws_gate, Ws_up=inp.Ws_up, Ws_down=inp.Ws_down,
+                                capacity_factor=cfg.cf, y_dtype=y_dtype, reroute_rounds=reroute,
+                                fp8=fp8, fp8_down=fp8 and fp8_down)
+        self.y = torch.empty((cfg.T, cfg.d), dtype=y_dtype, device=dev)
+        self.outs = self.layer.outputs_for(cfg.T, dev)
+        self.a = self.layer.args(inp.x, self.y, self.outs)
+        self.wsbuf = self.layer.workspace(self.a, dev)
+
+    def step(self, stream):
+        B.moe_forward(self.a, self.wsbuf, stream)
+
+    def timed(self, steps, stream, flush, ws, ffn_events=False):
+        """`steps` steps between a barrier and a synchronize on both sides, an L2
+        flush before each (outside its events).  Returns the median step time,
+        the median time of the routed expert FFN inside those same steps (CUDA
+        events that moe_forward records around its grouped-GEMM launches; None
+        unless ffn_events), the library launches counted, and the host window."""
+        E = lambda: torch.cuda.Event(enable_timing=True)   # noqa: E731
+        evs = [(E(), E()) for _ in range(steps)]
+        fev = [(E(), E()) for _ in range(steps)] if ffn_events else None
+        for pair in fev or ():
+            pair[0].record(stream)     # creates the events moe_forward will re-record
+            pair[1].record(stream)
         barrier(ws)
         torch.cuda.synchronize()
         l0 = B.moe_launch_counter()
-        for s, e in evs:
-            flush.fill_(1)               # evict L2 between steps (outside the events)
+        t0 = time.perf_counter()
+        for i, (s, e) in enumerate(evs):
+            flush.fill_(1)
+            if fev:
+                self.a.ffn_event_begin = fev[i][0].cuda_event
+                self.a.ffn_event_end = fev[i][1].cuda_event
             s.record(stream)
-            step()
+            self.step(stream)
             e.record(stream)
         torch.cuda.synchronize()
+        t1 = time.perf_counter()
         barrier(ws)
         launches = B.moe_launch_counter() - l0
-        return sum(s.elapsed_time(e) for s, e in evs) / args.steps, launches
+        self.a.ffn_event_begin = self.a.ffn_event_end = None
+        ms = statistics.median(s.elapsed_time(e) for s, e in evs)
+        ffn_ms = statistics.median(s.elapsed_time(e) for s, e in fev) if fev else None
+        return ms, ffn_ms, launches, (t0, t1)
 
-    ms, launches = timed_loop()
-    if args.forward_only:
+    def routing(self):
+        offsets = self.outs["offsets"].cpu()
+        kept = offsets[1:] - offsets[:-1]
+        return dict(A=int(offsets[-1].item()), touched=int((kept > 0).sum().item()),
+                    kept=kept)
+
+    def layer_roofline(self, ms, fp8=False, fp8_down=False):
+        cfg = self.cfg
+        r = self.routing()
+        esz = 2 if cfg.dtype == "bf16" else 4
+        work = RL.layer_work(cfg.T, cfg.d, cfg.f, cfg.N, cfg.k, r["A"], r["touched"], cfg.fs,
+                             esz, fp8_gate_up=fp8, fp8_down=fp8_down)
+        pk = RL.peaks()
+        fp8_flop = ((4.0 if fp8 else 0.0) + (2.0 if fp8_down else 0.0)) * cfg.d * cfg.f * r["A"]
+        t_roof, bound, t_flop, t_bytes = RL.roofline_time_s(work, pk, fp8_flop=fp8_flop)
+        return {"bound": bound, "roofline_ms": round(t_roof * 1e3, 4),
+                "flop_ms": round(t_flop * 1e3, 4), "bytes_ms": round(t_bytes * 1e3, 4),
+                "frac": round(t_roof * 1e3 / ms, 4),
+                "tokens_per_s_at_roofline": round(cfg.T / t_roof, 1),
+                "active_flop": work.flop, "weight_bytes": work.weight_bytes,
+                "activation_bytes": work.activation_bytes,
+                "peaks": f"{pk['source']}: {pk['bf16_tflops']} TFLOP/s bf16, "
+                         f"{pk['hbm_gbs']} GB/s"}
+
+    def free(self):
+        del self.inp, self.layer, self.y, self.outs, self.a, self.wsbuf
+        torch.cuda.empty_cache()
+
+
+def run_workloads(names, local, flush, stream, steps, warmup):
+    """Forward-only, clock-sampled timing of further bf16 workloads (one GPU):
+    median step, tokens/s and the fraction of each layer's roofline."""
+    rec = {}
+    dev = torch.device("cuda", local)
+    for name in names:
+        cfg = CONFIGS[name]
+        bn = Bench(cfg, dev)
+        for _ in range(warmup):
+            bn.step(stream)
+        torch.cuda.synchronize()
+        # enough steps for ~0.3 s of timed work, so the clock record has samples
+        t = time.perf_counter()
+        bn.step(stream)
+        torch.cuda.synchronize()
+        est = max(time.perf_counter() - t, 1e-5)
+        n = int(min(400, max(steps, 0.3 / est)))
+        sampler = ClockSampler(local)
+        sampler.start()
+        ms, _, launches, win = bn.timed(n, stream, flush, 1)
+        sampler.mark(*win)
         clocks = sampler.stop()
-        ms_max = reduce_max(ms, ws)
-        if rank == 0:
-            return {"config": cfg_desc(cfg), "ms_per_step": round(ms_max, 4),
-                    "value": round(ws * cfg.T / (ms_max / 1e3), 1), "unit": "tokens/s",
-                    "gpu_launches": int(launches), "clocks": clocks, "forward_only": True}
-        return None
+        if clocks_rejected(clocks):
+            sampler = ClockSampler(local)
+            sampler.start()
+            ms, _, launches, win = bn.timed(n, stream, flush, 1)
+            sampler.mark(*win)
+            clocks = sampler.stop()
+            clocks["remeasured"] = True
+        r = bn.routing()
+        rec[name] = {"ms_per_step": round(ms, 4), "value": round(cfg.T / (ms / 1e3), 1),
+                     "unit": "tokens/s", "steps": n, "warmup": warmup,
+                     "config": config_dict(cfg, 1), "dtype": dtype_name(cfg, False, False),
+                     "layer_roofline": bn.layer_roofline(ms),
+                     "routing": {"kept_rows": r["A"], "touched_experts": r["touched"],
+                                 "dropped": int(bn.outs["dropped"].item()),
+                                 "max_rows_per_expert": int(r["kept"].max().item()),
+                                 "min_rows_per_expert": int(r["kept"].min().item())},
+                     "gpu_launches": int(launches), "clocks": clocks,
+                     "timing": "moe_forward only, median of CUDA events per step"}
+        bn.free()
+    return rec
 
-    # per-stage times through the stage entry points (same inputs, same stream)
+
+def run_ours(args, ws, rank, local):
+    cfg = resolve_cfg(args)
+    dev = torch.device("cuda", local)
+    fp8, fp8_down = bool(args.fp8), bool(args.fp8 and args.fp8_down)
+    y_dtype = torch.float32 if args.y_dtype == "f32" else torch.bfloat16
+    bn = Bench(cfg, dev, rank, args.reroute, fp8, fp8_down, y_dtype)
+    inp, layer, outs = bn.inp, bn.layer, bn.outs
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    cdict = config_dict(cfg, ws, fp8, fp8_down, args.reroute, args.y_dtype)
+
+    for _ in range(args.warmup):
+        bn.step(stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    ffn_events = not args.forward_only
+    ms, ffn_ms, launches, win = bn.timed(args.steps, stream, flush, ws, ffn_events)
+    sampler.mark(*win)
+    clocks = sampler.stop()
+    if clocks_rejected(clocks):
+        # one re-measurement of the timed loop
+        sampler = ClockSampler(local)
+        sampler.start()
+        ms, ffn_ms, launches, win = bn.timed(args.steps, stream, flush, ws, ffn_events)
+        sampler.mark(*win)
+        clocks = sampler.stop()
+        clocks["remeasured"] = True
+    ms_max = reduce_max(ms, ws)
+    if args.forward_only:
+        if rank != 0:
+            return None
+        return {"metric": METRIC, "value": round(whole_job_value(ws, cfg.T, ms_max), 1),
+                "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(ms_max, 4), "dtype": dtype_name(cfg, fp8, fp8_down),
+                "config": cdict, "layer_roofline": bn.layer_roofline(ms_max, fp8, fp8_down),
+                "gpu_launches": int(launches), "clocks": clocks, "forward_only": True,
+                "timing": "moe_forward only, median of CUDA events per step"}
+
+    # per-stage times through the stage entry points (context: separate legs)
     k, N = cfg.k, cfg.N
     cap = B.moe_capacity(cfg.cf, cfg.T, k, N)
     A_max = cfg.T * k if cap == 0 else min(cfg.T * k, N * cap)
@@ -353,7 +572,7 @@ def run_ours(args, ws, rank, local):
             fn()
             e.record(stream)
         torch.cuda.synchronize()
-        return sum(s.elapsed_time(e) for s, e in evs) / reps
+        return statistics.median(s.elapsed_time(e) for s, e in evs)
 
     reps = max(3, min(args.steps, 20))
     stage_ms = {
@@ -361,38 +580,20 @@ def run_ours(args, ws, rank, local):
                                                             topk_idx=idx, topk_w=w), reps),
         "permute": time_stage(lambda: B.moe_permute(idx, N, x=inp.x, topk_w=w, capacity=cap,
                                                     A_max=A_max), reps),
-        "expert_ffn": time_stage(lambda: B.moe_expert_ffn(perm["x_perm"], perm["offsets"],
-                                                          inp.W_gate, inp.W_up, inp.W_down,
-                                                          row_scale=perm["row_scale"],
-                                                          y_perm=y_perm, A_max=A_max), reps),
-        "combine": time_stage(lambda: B.moe_combine(y_perm, perm["inv_pos"], y=y), reps),
+        "combine": time_stage(lambda: B.moe_combine(y_perm, perm["inv_pos"], y=bn.y), reps),
     }
-    if args.fp8:
-        # the FP8 layer's FFN: E4M3 rows of the permuted tokens, E4M3 gate/up
-        qg, sg, qu, su = layer.fp8[:4]
-        qd, sd = layer.fp8[4:6] if len(layer.fp8) > 4 else (None, None)
-        xq, sx = B.quantize_rows_e4m3(inp.x)
-        A_kept = int(perm["offsets"][-1].item())          # rows past it hold no token
-        xq_perm = torch.zeros((A_max, cfg.d), dtype=torch.uint8, device=dev)
-        xq_perm[:A_kept] = xq[perm["perm_token"][:A_kept].long()]
-        stage_ms["quantize_rows"] = time_stage(lambda: B.quantize_rows_e4m3(inp.x), reps)
-        stage_ms["expert_ffn_bf16"] = stage_ms["expert_ffn"]
-        stage_ms["expert_ffn"] = time_stage(lambda: B.moe_expert_ffn_fp8(
-            xq_perm, sx, perm["perm_token"], perm["offsets"], qg, sg, qu, su,
-            W_down=None if qd is not None else inp.W_down, Wq_down=qd, wscale_down=sd,
-            row_scale=perm["row_scale"], y_perm=y_perm, A_max=A_max), reps)
     if args.reroute > 0:
         cand, cand_w = B.moe_router_topk(inp.x, inp.W_g, k + args.reroute, bias=inp.bias)
         stage_ms["permute_reroute"] = time_stage(
             lambda: B.moe_permute_reroute(cand, cand_w, N, k, cap, x=inp.x), reps)
     # routing diagnostics from the router's logits and the pre-capacity counts
-    lg_buf = torch.empty((cfg.T, N), dtype=torch.float32, device=inp.x.device)
+    lg_buf = torch.empty((cfg.T, N), dtype=torch.float32, device=dev)
     B.moe_router_topk(inp.x, inp.W_g, k, bias=inp.bias, logits=lg_buf)
     stage_ms["routing_stats"] = time_stage(lambda: B.moe_routing_stats(perm["counts"], lg_buf),
                                            reps)
     if cfg.fs > 0:
-        sh_off = torch.tensor([0, cfg.T], dtype=torch.int32, device=inp.x.device)
-        ys = torch.empty((cfg.T, cfg.d), dtype=inp.x.dtype, device=inp.x.device)
+        sh_off = torch.tensor([0, cfg.T], dtype=torch.int32, device=dev)
+        ys = torch.empty((cfg.T, cfg.d), dtype=inp.x.dtype, device=dev)
         stage_ms["shared_ffn"] = time_stage(
             lambda: B.moe_expert_ffn(inp.x, sh_off, inp.Ws_gate[None], inp.Ws_up[None],
                                      inp.Ws_down[None], y_perm=ys), reps)
@@ -401,67 +602,48 @@ def run_ours(args, ws, rank, local):
     x_host = inp.x.cpu().pin_memory()
     y_host = torch.empty((cfg.T, cfg.d), dtype=y_dtype).pin_memory()
     x_stage = torch.empty_like(inp.x)
-    a_h = layer.args(x_stage, y, outs)
-    e2e_serial_ms = time_stage(lambda: B.moe_forward_host_io(a_h, x_host, y_host, wsbuf, stream),
-                               reps)
+    a_h = layer.args(x_stage, bn.y, outs)
+    e2e_serial_ms = time_stage(lambda: B.moe_forward_host_io(a_h, x_host, y_host, bn.wsbuf,
+                                                             stream), reps)
     # the same with the copies overlapped with the layer (token chunks; y only)
-    a_o = layer.args(x_stage, y, {"device_status": outs["device_status"]})
+    a_o = layer.args(x_stage, bn.y, {"device_status": outs["device_status"]})
     chunks = B.moe_forward_overlap_chunks(a_o) if not (cfg.cf > 0 or args.reroute) else 1
     ws_o = layer.workspace(a_o, dev)    # routing outputs live in the workspace here
     e2e_ms = time_stage(lambda: B.moe_forward_host_io_overlapped(a_o, x_host, y_host, ws_o,
                                                                  chunks, stream), reps)
-    clocks = sampler.stop()
-    if any(r in clocks.get("reasons", []) for r in BAD_REASONS):
-        # one re-measurement of the main loop
-        sampler = ClockSampler(local)
-        sampler.start()
-        ms, launches = timed_loop()
-        clocks = sampler.stop()
-        clocks["remeasured"] = True
-
-    ms_max = reduce_max(ms, ws)
     e2e_max = reduce_max(e2e_ms, ws)
+    ffn_max = reduce_max(ffn_ms, ws)
     if rank != 0:
         return None
 
-    # work and roofline
-    counts = outs["counts"].cpu()
-    offsets = outs["offsets"].cpu()
-    kept = (offsets[1:] - offsets[:-1])
-    A = int(offsets[-1].item())
-    touched = int((kept > 0).sum().item())
+    # dominant kernel: the routed grouped expert FFN (gate/up + SwiGLU, down +
+    # gate scale), timed inside the step loop above
+    r = bn.routing()
+    A, touched = r["A"], r["touched"]
     esz = 2 if cfg.dtype == "bf16" else 4
-    fp8_down = args.fp8 and args.fp8_down
-    work = RL.layer_work(cfg.T, cfg.d, cfg.f, N, k, A, touched, cfg.fs, esz,
-                         fp8_gate_up=args.fp8, fp8_down=fp8_down)
+    lr = bn.layer_roofline(ms_max, fp8, fp8_down)
     pk = RL.peaks()
-    fp8_flop = (4.0 if args.fp8 else 0.0) * cfg.d * cfg.f * A + (2.0 if fp8_down else 0.0) * cfg.d * cfg.f * A
-    t_roof, bound, t_flop, t_bytes = RL.roofline_time_s(work, pk, fp8_flop=fp8_flop)
-    value = whole_job_value(ws, cfg.T, ms_max)
-
-    # dominant kernel: the grouped expert FFN (gate/up + SwiGLU, down + gate scale)
-    ffn_ms = stage_ms["expert_ffn"]
     ffn_flop = 6.0 * cfg.d * cfg.f * A
-    ffn_bytes = touched * (RL.expert_params(cfg.d, cfg.f) * esz if not args.fp8
+    ffn_bytes = touched * (RL.expert_params(cfg.d, cfg.f) * esz if not fp8
                            else 2 * cfg.d * cfg.f + 2 * cfg.f * 4 +
                            (cfg.d * cfg.f + cfg.d * 4 if fp8_down else cfg.d * cfg.f * esz))
     # FP8 layers: 2/3 of the FFN FLOPs (gate/up) run at the FP8 rate, so the
     # FFN's peak is the bf16 peak scaled by FLOPs over bf16-equivalent FLOPs
-    fp8_share = (1.0 if fp8_down else 2 / 3) if args.fp8 else 0.0
+    fp8_share = (1.0 if fp8_down else 2 / 3) if fp8 else 0.0
     peak_scale = 1.0 / ((1 - fp8_share) + fp8_share / RL.FP8_OVER_BF16)
-    if bound == "tensor":
-        achieved = ffn_flop / (ffn_ms / 1e3) / 1e12
+    if lr["bound"] == "tensor":
+        achieved = ffn_flop / (ffn_max / 1e3) / 1e12
         peak = round(pk["bf16_tflops"] * peak_scale, 1)
         unit = "TFLOP/s"
     else:
-        achieved = ffn_bytes / (ffn_ms / 1e3) / 1e9
+        achieved = ffn_bytes / (ffn_max / 1e3) / 1e9
         peak = pk["hbm_gbs"]
         unit = "GB/s"
-    traffic, tkernel = traffic_from_profiles(
-        cfg.name + ("_fp8_all" if fp8_down else "_fp8" if args.fp8 else ""))
+    traffic, _ = traffic_from_profiles(
+        cfg.name + ("_fp8_all" if fp8_down else "_fp8" if fp8 else ""))
     line = {
-        "metric": "MoE-layer tokens/s on 1 B300 and % of roofline (active FLOPs vs expert bytes)",
-        "value": round(value, 1),
+        "metric": METRIC,
+        "value": round(whole_job_value(ws, cfg.T, ms_max), 1),
         "unit": "tokens/s",
         "n_gpus": ws,
         "steps": args.steps,
@@ -470,37 +652,23 @@ def run_ours(args, ws, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": ("e4m3 experts + bf16" if fp8_down else "e4m3 gate/up + bf16" if args.fp8 else
-                  "bf16" if cfg.dtype == "bf16" else "f32"),
+        "dtype": dtype_name(cfg, fp8, fp8_down),
         "data": "synthetic (seeded Gaussian x and N(0,1/fan_in) weights of the workload's shape)",
-        "config": {"workload": cfg_desc(cfg) + (f", overflow re-routed in {args.reroute} rounds"
-                                                 if args.reroute else "")
-                   + (", gate/up" + (" and down" if fp8_down else "") +
-                      " in FP8 E4M3 (per-channel / per-row absmax scales)" if args.fp8 else ""),
-                   "fp8_gate_up": bool(args.fp8), "fp8_down": bool(fp8_down),
-                   "reroute_rounds": args.reroute, "T": cfg.T, "d": cfg.d, "f": cfg.f, "N": N,
-                   "k": k, "fs": cfg.fs, "capacity_factor": cfg.cf, "bias_std": cfg.bias_std,
-                   "y_dtype": args.y_dtype, "parallelism": f"replicas x{ws} (no exchange)",
-                   "l2": "256 MB L2 flush write between steps, outside the timed events; "
-                         "weights also exceed L2"},
-        "layer_roofline": {"bound": bound, "roofline_ms": round(t_roof * 1e3, 4),
-                           "flop_ms": round(t_flop * 1e3, 4), "bytes_ms": round(t_bytes * 1e3, 4),
-                           "frac": round(t_roof * 1e3 / ms_max, 4),
-                           "tokens_per_s_at_roofline": round(cfg.T / t_roof, 1),
-                           "active_flop": work.flop, "weight_bytes": work.weight_bytes,
-                           "activation_bytes": work.activation_bytes,
-                           "peaks": f"{pk['source']}: {pk['bf16_tflops']} TFLOP/s bf16, "
-                                    f"{pk['hbm_gbs']} GB/s"},
+        "config": cdict,
+        "timing": "median of per-step CUDA events on the launching stream",
+        "layer_roofline": lr,
         "roofline": {"kernel": "grouped expert FFN (gate/up+SwiGLU and down+gate-scale launches)",
-                     "bound": "tensor" if bound == "tensor" else "hbm",
+                     "bound": "tensor" if lr["bound"] == "tensor" else "hbm",
                      "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "per_launch_ms": round(ffn_ms, 4),
+                     "per_launch_ms": round(ffn_max, 4),
+                     "timed": "inside the timed steps: CUDA events moe_forward records around "
+                              "its routed grouped-GEMM launches (median per step)",
                      "algorithmic": (f"{ffn_flop:.4g} FLOP" if unit == "TFLOP/s"
                                      else f"{ffn_bytes:.4g} B"),
                      "peak_source": f"{pk['source']} (burst)" + (
                          "; gate/up at the bf16 peak x the nominal FP8/bf16 ratio"
-                         if args.fp8 and unit == "TFLOP/s" else ""),
+                         if fp8 and unit == "TFLOP/s" else ""),
                      # context only: the same kernel against the measured sustained
                      # (power-capped) cuBLAS rate; the bench runs back to back for
                      # seconds, so its clocks sit in that regime
@@ -509,10 +677,12 @@ def run_ours(args, ws, rank, local):
                              achieved / (pk["bf16_tflops_sustained"] * peak_scale), 4)}
                         if unit == "TFLOP/s" else {})},
         "stages_ms": {k_: round(v, 4) for k_, v in stage_ms.items()},
+        "stages_note": "stage entry points timed in separate legs after the timed steps "
+                       "(context only)",
         "routing": {"kept_rows": A, "dropped": int(outs["dropped"].item()),
                     "rerouted": int(outs["rerouted"].item()), "reroute_rounds": args.reroute,
-                    "touched_experts": touched, "max_rows_per_expert": int(kept.max().item()),
-                    "min_rows_per_expert": int(kept.min().item())},
+                    "touched_experts": touched, "max_rows_per_expert": int(r["kept"].max().item()),
+                    "min_rows_per_expert": int(r["kept"].min().item())},
         "e2e": {"value": round(ws * cfg.T / (e2e_max / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": cfg.T * cfg.d * esz,
                 "d2h_bytes_per_step": cfg.T * cfg.d * (4 if args.y_dtype == "f32" else 2),
@@ -525,6 +695,14 @@ def run_ours(args, ws, rank, local):
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, inp, args.cpu_seconds)
+    if (ws == 1 and not args.no_workloads and args.config == "mixtral_prefill" and
+            not (args.tokens or args.experts or args.ffn_dim or fp8 or args.reroute)):
+        bn.free()
+        del flush, x_host, y_host, x_stage, y_perm, perm, lg_buf
+        torch.cuda.empty_cache()
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        line["workloads"] = run_workloads(WORKLOADS_ALSO, local, flush, stream,
+                                          steps=30, warmup=max(3, args.warmup))
     return line
 
 
@@ -533,7 +711,7 @@ def run_reference(args, ws, rank):
     if rank != 0:
         return None
     import oracle
-    cfg = CONFIGS[args.config]
+    cfg = resolve_cfg(args)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     dinp = make_inputs(cfg, device=dev)
     per_step = max(0.5, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
@@ -542,22 +720,23 @@ def run_reference(args, ws, rank):
     prefetch(inp, S, fetch)
     for _ in range(args.warmup):
         oracle_sample(inp, S, fetch)
-    t = time.perf_counter()
+    times = []
     for _ in range(args.steps):
+        t = time.perf_counter()
         oracle_sample(inp, S, fetch)
-    dt = (time.perf_counter() - t) / args.steps
+        times.append(time.perf_counter() - t)
+    dt = statistics.median(times)
     v = S / dt
     sample = (f"first {S} of {cfg.T} tokens per step, full fp64 oracle pass "
               f"(router, top-k, grouping, SwiGLU experts, combine)")
     return {
         "impl": "reference",
-        "metric": "MoE-layer tokens/s on 1 B300 and % of roofline (active FLOPs vs expert bytes)",
+        "metric": METRIC,
         "value": round(v, 3), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg_desc(cfg), "T": cfg.T, "d": cfg.d, "f": cfg.f, "N": cfg.N,
-                   "k": cfg.k, "fs": cfg.fs, "capacity_factor": cfg.cf,
-                   "bias_std": cfg.bias_std},
+        "config": config_dict(cfg, ws, bool(args.fp8), bool(args.fp8 and args.fp8_down),
+                              args.reroute, args.y_dtype),
         "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s",
                          "cores": oracle.default_threads(), "kind": "oracle", "sample": sample},
         "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,

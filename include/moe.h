@@ -136,7 +136,9 @@ moe_status_t moe_permute(const int32_t *topk_idx, const float *topk_w,
  *     message (e.g. T <= 65536 tokens for N = 256 experts);
  *   - allocates nothing; the first call on each device looks up the array's
  *     device address (with that device current), so make that first call
- *     before any stream capture;
+ *     before any stream capture.  The address is kept for later calls, which
+ *     assumes the device's context is not reset (cudaDeviceReset) while the
+ *     library stays loaded;
  *   - every call shares the one array: calls that overlap on the GPU race;
  *     order them on one stream.  Nothing in it needs clearing between calls. */
 moe_status_t moe_permute_noalloc(const int32_t *topk_idx, const float *topk_w,
@@ -227,10 +229,11 @@ moe_status_t moe_expert_ffn(const void *x_perm, const int32_t *offsets,
  *   g = (xq . Wq_gate[e][j]) * x_scale * wscale_gate[e][j], u likewise,
  *   h = SiLU(g) * u rounded to bf16, y_perm = row_scale * (h W_down) as in
  *   moe_expert_ffn.  With Wq_down ([N,d,f] codes, wscale_down [N,d]; W_down
- *   may be NULL) the down projection is E4M3 too: each kept row of h is
- *   quantised like x (one scale per row, f % 16 == 0) and
- *   y_perm[p][m] = row_scale[p] * (hq . Wq_down[e][m]) * h_scale[p] *
- *   wscale_down[e][m].  Workspace: moe_expert_ffn_fp8_workspace_size.
+ *   may be NULL) the down projection is E4M3 too: h is kept in fp32 and each
+ *   kept row quantised from those values like x (one scale per row,
+ *   f % 16 == 0), and y_perm[p][m] = row_scale[p] * (hq . Wq_down[e][m]) *
+ *   h_scale[p] * wscale_down[e][m].  Workspace:
+ *   moe_expert_ffn_fp8_workspace_size.
  * ------------------------------------------------------------------------- */
 size_t moe_expert_ffn_fp8_workspace_size(int A_max, int d, int f, int N,
                                          int fp8_down);
@@ -305,6 +308,14 @@ typedef struct moe_forward_args {
                                  [N,d,f] (W_down may then be NULL); h is
                                  quantised per row before it               */
   const float *wscale_down;   /* [N,d]                                       */
+  /* Timing hooks (optional, NULL = none): two cudaEvent_t (as void*) that
+   * moe_forward records on its stream right before the routed experts' first
+   * grouped-GEMM launch and right after their last one, so a caller can time
+   * the expert FFN inside the same step it times the layer.  Recording them
+   * orders the FFN's first launch after the dispatch's completion (no early
+   * launch across the event), which costs a few microseconds per step.     */
+  void *ffn_event_begin;
+  void *ffn_event_end;
 } moe_forward_args;
 
 size_t moe_forward_workspace_size(const moe_forward_args *args);

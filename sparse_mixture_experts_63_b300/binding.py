@@ -56,7 +56,8 @@ class moe_forward_args(ctypes.Structure):
                 ("rerouted", ctypes.c_void_p), ("Wq_gate", ctypes.c_void_p),
                 ("wscale_gate", ctypes.c_void_p), ("Wq_up", ctypes.c_void_p),
                 ("wscale_up", ctypes.c_void_p), ("Wq_down", ctypes.c_void_p),
-                ("wscale_down", ctypes.c_void_p)]
+                ("wscale_down", ctypes.c_void_p), ("ffn_event_begin", ctypes.c_void_p),
+                ("ffn_event_end", ctypes.c_void_p)]
 
 
 _lib = None

@@ -562,6 +562,10 @@ moe_status_t moe_forward(const moe_forward_args *a, void *workspace, size_t work
     s = launch_copy_rows_e4m3(a->x, L.inv_pos, a->T, a->d, a->k,
                               static_cast<uint8_t *>(L.x_perm), L.xs, stream);
     if (s != MOE_OK) return s;
+  }
+  if (a->ffn_event_begin)
+    MOE_CUDA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(a->ffn_event_begin), stream));
+  if (fp8) {
     s = launch_ffn_tc_fp8(L.x_perm, L.xs, L.perm_token, L.offsets, L.row_scale, A_max, a->d,
                           a->f, a->N, cap, a->Wq_gate, a->wscale_gate, a->Wq_up, a->wscale_up,
                           a->W_down, a->Wq_down, a->wscale_down, L.ffn_ws, L.y_perm,
@@ -572,6 +576,8 @@ moe_status_t moe_forward(const moe_forward_args *a, void *workspace, size_t work
                           L.ffn_ws, stream);
   }
   if (s != MOE_OK) return s;
+  if (a->ffn_event_end)
+    MOE_CUDA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(a->ffn_event_end), stream));
   if (a->fs > 0) {
     MOE_CUDA_TRY(launch_pdl(set_shared_offsets, dim3(1), dim3(1), 0, stream, L.sh_offsets, a->T));
     MOE_LAUNCH_CHECK();
@@ -654,6 +660,7 @@ moe_status_t moe_forward_host_io_overlapped(const moe_forward_args *a, const voi
     ac.T = (int)tc;
     ac.x = static_cast<const char *>(a->x) + t0 * xr;
     ac.y = static_cast<char *>(a->y) + t0 * yr;
+    ac.ffn_event_begin = ac.ffn_event_end = nullptr;   // one layer call spans several chunks
     MOE_CUDA_TRY(cudaStreamWaitEvent(stream, ev[1 + c], 0));
     s = moe_forward(&ac, workspace, workspace_bytes, stream_);
     if (s != MOE_OK) return s;

@@ -187,3 +187,24 @@ def test_overlap_chunks_rule(lib):
     assert lib.moe_forward_overlap_chunks(ctypes.byref(pre)) == 7
     assert lib.moe_forward_overlap_chunks(ctypes.byref(ds)) == 1
     assert lib.moe_forward_overlap_chunks(ctypes.byref(dec)) == 1
+
+
+def test_forward_args_layout_matches_header(tmp_path):
+    """The binding's ctypes mirror of moe_forward_args has the C struct's
+    field offsets and size (a C program compiled against include/moe.h
+    prints them)."""
+    fields = [f[0] for f in B.moe_forward_args._fields_]
+    prog = ["#include <stdio.h>", "#include <stddef.h>", '#include "moe.h"', "int main(void) {",
+            '  printf("%zu\\n", sizeof(moe_forward_args));']
+    prog += [f'  printf("%zu\\n", offsetof(moe_forward_args, {n}));' for n in fields]
+    prog += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(prog) + "\n")
+    exe = tmp_path / "layout"
+    import subprocess
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)],
+                   check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(B.moe_forward_args)
+    assert got[1:] == [getattr(B.moe_forward_args, n).offset for n in fields]
