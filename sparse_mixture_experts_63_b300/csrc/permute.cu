@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(256) permute_copy_rows(const VecT *__restrict_
 
 size_t permute_workspace_bytes(int T, int N, int k) {
   (void)k;
-  size_t nchunks = (size_t)(T + kChunkTokens - 1) / kChunkTokens;
+  size_t nchunks = ((size_t)T + kChunkTokens - 1) / kChunkTokens;
   return align_up(nchunks * (size_t)N * sizeof(int32_t), 256);
 }
 

@@ -72,7 +72,7 @@ extern "C" moe_status_t moe_permute_noalloc(const int32_t *topk_idx, const float
     set_error("moe_permute_noalloc: bad sizes T=%d N=%d k=%d", T, N, k);
     return MOE_ERR_INVALID_ARG;
   }
-  const long need = (long)((T + 255) / 256) * N;
+  const long need = (((long)T + 255) / 256) * (long)N;   // no int overflow near INT_MAX
   if (need > kNoAllocHistEntries) {
     set_error("moe_permute_noalloc: ceil(T/256)*N = %ld histogram entries exceeds the fixed "
               "scratch of %d (use moe_permute with a workspace)",

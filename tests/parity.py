@@ -241,6 +241,19 @@ def _fp8_fetch(inp, qw):
     return fetch
 
 
+_QCACHE = {}
+
+
+def oracle_codes(cfg, name, W):
+    """The oracle's E4M3 codes and channel scales of one weight tensor of a
+    seeded layer, computed once per (layer, tensor) in this process (the
+    inputs of a config and seed are always the same tensors)."""
+    key = (cfg, name)
+    if key not in _QCACHE:
+        _QCACHE[key] = oracle.quantize_weights_e4m3(W.cpu())
+    return _QCACHE[key]
+
+
 def check_layer_fp8(cfg, inp, rows=None, down=False):
     """moe_forward with E4M3 gate/up (and down, with `down`) against the
     oracle's fp64 layer on its own E4M3 codes of x and of the weights; the
@@ -254,9 +267,9 @@ def check_layer_fp8(cfg, inp, rows=None, down=False):
     out = layer.last
     assert int(out["device_status"].item()) == 0
     # the layer's quantised weights are the oracle's, byte for byte
-    qw = [oracle.quantize_weights_e4m3(inp.W_gate.cpu()), oracle.quantize_weights_e4m3(inp.W_up.cpu())]
+    qw = [oracle_codes(cfg, "W_gate", inp.W_gate), oracle_codes(cfg, "W_up", inp.W_up)]
     if down:
-        qw.append(oracle.quantize_weights_e4m3(inp.W_down.cpu()))
+        qw.append(oracle_codes(cfg, "W_down", inp.W_down))
     for (qo, so), i in zip(qw, (0, 2, 4)):
         np.testing.assert_array_equal(layer.fp8[i].cpu().numpy(), qo)
         np.testing.assert_array_equal(layer.fp8[i + 1].cpu().numpy(), so)

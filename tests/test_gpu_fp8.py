@@ -1,9 +1,11 @@
-"""GPU parity of the FP8 (E4M3) gate/up path against the fp64 oracle.
+"""GPU parity of the FP8 (E4M3) expert path against the fp64 oracle.
 
 Quantisation is byte work: the codes and scales must match the oracle's bit
 for bit.  The FFN and the layer are compared with the oracle's fp64 layer on
 the same E4M3 values (its own quantisation of the inputs), within the bf16
-layer tolerance (h is rounded to bf16 between the GEMMs, as in the bf16 path).
+layer tolerance: with a bf16 down projection h is rounded to bf16 between the
+GEMMs, as in the bf16 path; with an E4M3 down projection the oracle quantises
+its exact h per row and the kernels quantise their fp32 h.
 """
 import numpy as np
 import pytest
@@ -110,13 +112,19 @@ def test_layer_fp8_reduced(name, down):
 
 
 @pytest.mark.parametrize("down", [False, True], ids=["bf16_down", "fp8_down"])
-@pytest.mark.parametrize("name,rows", [("mixtral_decode", None), ("capacity", 256)])
+@pytest.mark.parametrize("name,rows", [("mixtral_decode", None), ("capacity", None),
+                                       ("mixtral_prefill", 512), ("deepseek", 512)])
 def test_layer_fp8_full_size(name, rows, down):
+    """The FP8 layer at the sizes the benchmark times: codes and scales of
+    every weight bit-exact, routing and the output of sampled rows (all rows
+    on the decode and capacity layers; 512 seeded rows with the first and last
+    token on the prefill and DeepSeek layers) against the oracle."""
     cfg = CONFIGS[name]
     inp = make_inputs(cfg, device=torch.device("cuda"))
     sel = None
     if rows is not None:
         sel = np.sort(np.random.default_rng(cfg.seed).choice(cfg.T, size=rows, replace=False))
+        sel[0], sel[-1] = 0, cfg.T - 1
     print(name, down, parity.check_layer_fp8(cfg, inp, sel, down=down))
     del inp
     torch.cuda.empty_cache()

@@ -66,3 +66,8 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
                                None, None, None, None)
     assert rc == 2
     assert "65536" in L.moe_last_error().decode()
+    # a token count near INT_MAX: the entry count is formed without overflow
+    rc = L.moe_permute_noalloc(fake, None, None, 1, 2 ** 31 - 100, 64, 1, 1, 0, fake, fake, fake,
+                               None, fake, None, None, None, None)
+    assert rc == 2
+    assert "65536" in L.moe_last_error().decode()
