@@ -104,31 +104,57 @@ class ClockSampler:
         self._thread = None
         self._proc = None
         self.source = "unsampled"
+        self.nvml_error = None
 
-    def _nvml_handle(self):
-        import pynvml
-        pynvml.nvmlInit()
+    def _nvml(self):
+        """Read-only NVML calls through ctypes on the library nvidia-smi uses:
+        returns (SM clock, max SM clock, clock-event reason bits) readers."""
+        import ctypes
+        L = ctypes.CDLL("libnvidia-ml.so.1")
+        if L.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        h = ctypes.c_void_p()
         uuid = None
         try:
             uuid = str(torch.cuda.get_device_properties(self.torch_index).uuid)
-        except Exception:
+        except Exception:   # noqa: BLE001 -- older torch: no uuid, match by index
             pass
+        rc = 1
         if uuid:
             u = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
-            try:
-                return pynvml, pynvml.nvmlDeviceGetHandleByUUID(u)
-            except Exception:
-                pass
-        return pynvml, pynvml.nvmlDeviceGetHandleByIndex(self.torch_index)
+            rc = L.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h))
+        if rc != 0 and L.nvmlDeviceGetHandleByIndex_v2(self.torch_index, ctypes.byref(h)) != 0:
+            raise RuntimeError("no NVML handle for the device")
+        NVML_CLOCK_SM = 1
+        get_reasons = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            L.nvmlDeviceGetCurrentClocksThrottleReasons
+
+        def clock():
+            c = ctypes.c_uint()
+            if L.nvmlDeviceGetClockInfo(h, NVML_CLOCK_SM, ctypes.byref(c)) != 0:
+                raise RuntimeError("nvmlDeviceGetClockInfo failed")
+            return float(c.value)
+
+        def max_clock():
+            c = ctypes.c_uint()
+            if L.nvmlDeviceGetMaxClockInfo(h, NVML_CLOCK_SM, ctypes.byref(c)) != 0:
+                raise RuntimeError("nvmlDeviceGetMaxClockInfo failed")
+            return float(c.value)
+
+        def reasons():
+            r = ctypes.c_ulonglong()
+            if get_reasons(h, ctypes.byref(r)) != 0:
+                raise RuntimeError("clock-event reasons unavailable")
+            return int(r.value)
+        clock(), reasons()   # both readable, or fall back
+        return clock, max_clock(), reasons
 
     def start(self):
         import threading
         try:
-            nv, h = self._nvml_handle()
-            smax = float(nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM))
-            get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons",
-                                  None) or nv.nvmlDeviceGetCurrentClocksThrottleReasons
-        except Exception:
+            clock, smax, reasons = self._nvml()
+        except Exception as exc:   # noqa: BLE001 -- any NVML failure: use nvidia-smi
+            self.nvml_error = f"{type(exc).__name__}: {exc}"[:200]
             return self._start_smi()
         self.source = f"nvml every {self.period * 1e3:.0f} ms"
         self._stop = threading.Event()
@@ -136,10 +162,8 @@ class ClockSampler:
         def run():
             while not self._stop.is_set():
                 try:
-                    self.samples.append((time.perf_counter(),
-                                         float(nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)),
-                                         smax, int(get_reasons(h))))
-                except Exception:
+                    self.samples.append((time.perf_counter(), clock(), smax, reasons()))
+                except Exception:   # noqa: BLE001 -- a failed read drops one sample
                     pass
                 self._stop.wait(self.period)
         self._thread = threading.Thread(target=run, daemon=True)
@@ -196,7 +220,8 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"],
                     "source": self.source}
         counts = {n: sum(1 for r in inside if r[3] & b) for n, b in self.BITS.items()}
-        return {"sm_mhz": statistics.median(r[1] for r in inside),
+        extra = {"nvml_error": self.nvml_error} if self.nvml_error else {}
+        return {**extra, "sm_mhz": statistics.median(r[1] for r in inside),
                 "sm_max_mhz": max(r[2] for r in inside),
                 "sm_min_mhz": min(r[1] for r in inside),
                 "samples": len(inside), "reasons": sorted(n for n, c in counts.items() if c),
