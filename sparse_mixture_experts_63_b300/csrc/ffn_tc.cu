@@ -120,6 +120,8 @@ struct TcParams {
   int tile_cap;            // token rows per tile: 64, 128, 256, or 320 (wide)
   int wide;                // 1: tiles over 256 rows run as two sub-tiles
   int stages;              // pipeline stages (kStageRegion / stage_bytes)
+  int kgroup;              // stages per barrier pair (1 or 2; divides stages): selects
+                           // the kernel instance
   int stage_bytes;         // kABytes + token rows of a stage (both sub-tiles)
   // FP8 (E4M3 weights and rows, K-major): D is multiplied by the output
   // channel's scale and the row's scale before the epilogue's math
@@ -354,7 +356,7 @@ __device__ __forceinline__ void scale_chunk(const TcParams &p, int row0, int val
 // stage (the same 128-byte rows as 64 bf16), kind::f8f6f4 MMAs, and the
 // channel x row scales applied to D before SwiGLU (GEMM1) or the gate-weight
 // scale (GEMM2).
-template <bool FP8>
+template <bool FP8, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
@@ -428,7 +430,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       unsigned char *stage0 = smem + Smem::stages;
       // the even CTA's full barriers, in cluster address space (contiguous, 8 B apart)
       const uint32_t full_leader0 = tc::mapa_shared(&full[0], 0);
-      int s = 0;
+      const int ngroups = p.stages / G;          // G: stages per barrier pair
+      const int bbytes = p.stage_bytes - kABytes;   // token part of a stage
+      int g = 0;            // barrier group: stages g*G .. g*G+G-1
       uint32_t ph = 0;
       uint32_t issued = 0;
       bool ok = true;
@@ -447,34 +451,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m1 = p.gemm1 ? m0 : m0 + 64;
         const int brow0 = ti.row0 + (int)rank * (n0 / 2);
         const int brow1 = ti.row0 + ti.rows0 + (int)rank * (n1 / 2);
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!tc::mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, kTimeoutNs)) {
+        // K steps go in groups of G (the last group of a tile may be shorter),
+        // one full and one empty barrier per group
+        for (int kb = 0; kb < kblocks; kb += G) {
+          const int nk = min(G, kblocks - kb);
+          if (!tc::mbar_wait_bounded(&empty[g], ph ^ 1, abort_flag, kTimeoutNs)) {
             ok = false;
             break;
           }
-          unsigned char *st = stage0 + s * kABytes;                     // weight part
-          unsigned char *stb =                                            // token part
-              stage0 + p.stages * kABytes + s * (p.stage_bytes - kABytes);
-          if (rank == 0) tc::mbar_arrive_expect_tx(&full[s], tx);
-          const uint32_t fb = full_leader0 + 8u * s;
-          const int kc = kb * kKStage;
-          if (FP8) {   // K-major weights W[N][M][K]: coordinates (k, m, e)
-            tc::tma_load_3d_pair(st, &tmA0, fb, kc, m0, ti.e, pol_w);
-            tc::tma_load_3d_pair(st + kAChunkBytes, &tmA1, fb, kc, m1, ti.e, pol_w);
-          } else {     // MN-major weights W[N][K][M]: coordinates (m, k, e)
-            tc::tma_load_3d_pair(st, &tmA0, fb, m0, kc, ti.e, pol_w);
-            tc::tma_load_3d_pair(st + kAChunkBytes, &tmA1, fb, m1, kc, ti.e, pol_w);
+          if (rank == 0) tc::mbar_arrive_expect_tx(&full[g], tx * (uint32_t)nk);
+          const uint32_t fb = full_leader0 + 8u * g;
+          for (int h = 0; h < nk; ++h) {
+            const int slot = g * G + h;
+            unsigned char *st = stage0 + slot * kABytes;                  // weight part
+            unsigned char *stb = stage0 + p.stages * kABytes + slot * bbytes;   // token part
+            const int kc = (kb + h) * kKStage;
+            if (FP8) {   // K-major weights W[N][M][K]: coordinates (k, m, e)
+              tc::tma_load_3d_pair(st, &tmA0, fb, kc, m0, ti.e, pol_w);
+              tc::tma_load_3d_pair(st + kAChunkBytes, &tmA1, fb, kc, m1, ti.e, pol_w);
+            } else {     // MN-major weights W[N][K][M]: coordinates (m, k, e)
+              tc::tma_load_3d_pair(st, &tmA0, fb, m0, kc, ti.e, pol_w);
+              tc::tma_load_3d_pair(st + kAChunkBytes, &tmA1, fb, m1, kc, ti.e, pol_w);
+            }
+            tc::tma_load_2d_pair(stb, tb0, fb, kc, brow0, pol_x);
+            if (n1) tc::tma_load_2d_pair(stb + kSubBytes, tb1, fb, kc, brow1, pol_x);
           }
-          tc::tma_load_2d_pair(stb, tb0, fb, kc, brow0, pol_x);
-          if (n1) tc::tma_load_2d_pair(stb + kSubBytes, tb1, fb, kc, brow1, pol_x);
           ++issued;
-          if (++s == p.stages) { s = 0; ph ^= 1; }
+          if (++g == ngroups) { g = 0; ph ^= 1; }
         }
       }
       if (!ok && rank == 0) {
-        // Drain: wait (bounded) for every stage still being filled (both CTAs'
+        // Drain: wait (bounded) for every group still being filled (both CTAs'
         // bytes complete on these barriers).
-        const uint32_t ns = (uint32_t)p.stages;
+        const uint32_t ns = (uint32_t)ngroups;
         const uint32_t first = issued >= ns ? issued - ns : 0;
         for (uint32_t q = first; q < issued; ++q) {
           volatile int dummy = 0;
@@ -496,7 +505,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    : tc::sdesc_sw128(stage0, kAChunkBytes, 1024);
       const uint64_t b_desc0 =
           tc::sdesc_sw128(stage0 + (uint32_t)(p.stages * kABytes), 16, 1024);   // K-major B
-      int s = 0;
+      const int ngroups = p.stages / G;
+      const int bbytes = p.stage_bytes - kABytes;
+      int g = 0;            // barrier group, as in the producer
       uint32_t ph = 0;
       int pos = 0;              // tensor-memory ring position (chunks)
       uint32_t cuse = 0;        // bit c: parity of chunk c's uses so far
@@ -532,44 +543,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d0 = tmem_base + (uint32_t)(c0 * 32);
         const uint32_t d1 = tmem_base + (uint32_t)(c1 * 32);
         tc::tc_fence_after();
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!tc::mbar_wait_bounded(&full[s], ph, abort_flag, kTimeoutNs)) {
+        for (int kb = 0; kb < kblocks; kb += G) {
+          const int nk = min(G, kblocks - kb);
+          if (!tc::mbar_wait_bounded(&full[g], ph, abort_flag, kTimeoutNs)) {
             ok = false;
             break;
           }
           tc::tc_fence_after();
-          const uint64_t ad = a_desc0 + (uint64_t)((s * kABytes) >> 4);
-          const uint64_t bd = b_desc0 + (uint64_t)((s * (p.stage_bytes - kABytes)) >> 4);
-          if (FP8) {
-            // both K-major: 32 k of 8 bits = 32 B further inside the 128-B rows (+2)
-            tc::mma_f8_pair(d0, ad, bd, idesc0, kb > 0 ? 1u : 0u);
-            tc::mma_f8_pair(d0, ad + 2, bd + 2, idesc0, 1u);
-            tc::mma_f8_pair(d0, ad + 4, bd + 4, idesc0, 1u);
-            tc::mma_f8_pair(d0, ad + 6, bd + 6, idesc0, 1u);
-            if (two) {
-              const uint64_t bd1 = bd + (kSubBytes >> 4);
-              tc::mma_f8_pair(d1, ad, bd1, idesc1, kb > 0 ? 1u : 0u);
-              tc::mma_f8_pair(d1, ad + 2, bd1 + 2, idesc1, 1u);
-              tc::mma_f8_pair(d1, ad + 4, bd1 + 4, idesc1, 1u);
-              tc::mma_f8_pair(d1, ad + 6, bd1 + 6, idesc1, 1u);
-            }
-          } else {
-            // A MN-major: 16 k-rows = two 1024-B atoms further (+128 in 16-B units);
-            // B K-major: 16 k = 32 B further inside the 128-B swizzled row (+2).
-            tc::mma_f16_pair(d0, ad, bd, idesc0, kb > 0 ? 1u : 0u);
-            tc::mma_f16_pair(d0, ad + 128, bd + 2, idesc0, 1u);
-            tc::mma_f16_pair(d0, ad + 256, bd + 4, idesc0, 1u);
-            tc::mma_f16_pair(d0, ad + 384, bd + 6, idesc0, 1u);
-            if (two) {
-              const uint64_t bd1 = bd + (kSubBytes >> 4);   // second sub-tile's token rows
-              tc::mma_f16_pair(d1, ad, bd1, idesc1, kb > 0 ? 1u : 0u);
-              tc::mma_f16_pair(d1, ad + 128, bd1 + 2, idesc1, 1u);
-              tc::mma_f16_pair(d1, ad + 256, bd1 + 4, idesc1, 1u);
-              tc::mma_f16_pair(d1, ad + 384, bd1 + 6, idesc1, 1u);
+          for (int h = 0; h < nk; ++h) {
+            const int slot = g * G + h;
+            const uint64_t ad = a_desc0 + (uint64_t)((slot * kABytes) >> 4);
+            const uint64_t bd = b_desc0 + (uint64_t)((slot * bbytes) >> 4);
+            const uint32_t acc = (kb + h) > 0 ? 1u : 0u;   // the tile's first K step overwrites
+            if (FP8) {
+              // both K-major: 32 k of 8 bits = 32 B further inside the 128-B rows (+2)
+              tc::mma_f8_pair(d0, ad, bd, idesc0, acc);
+              tc::mma_f8_pair(d0, ad + 2, bd + 2, idesc0, 1u);
+              tc::mma_f8_pair(d0, ad + 4, bd + 4, idesc0, 1u);
+              tc::mma_f8_pair(d0, ad + 6, bd + 6, idesc0, 1u);
+              if (two) {
+                const uint64_t bd1 = bd + (kSubBytes >> 4);
+                tc::mma_f8_pair(d1, ad, bd1, idesc1, acc);
+                tc::mma_f8_pair(d1, ad + 2, bd1 + 2, idesc1, 1u);
+                tc::mma_f8_pair(d1, ad + 4, bd1 + 4, idesc1, 1u);
+                tc::mma_f8_pair(d1, ad + 6, bd1 + 6, idesc1, 1u);
+              }
+            } else {
+              // A MN-major: 16 k-rows = two 1024-B atoms further (+128 in 16-B units);
+              // B K-major: 16 k = 32 B further inside the 128-B swizzled row (+2).
+              tc::mma_f16_pair(d0, ad, bd, idesc0, acc);
+              tc::mma_f16_pair(d0, ad + 128, bd + 2, idesc0, 1u);
+              tc::mma_f16_pair(d0, ad + 256, bd + 4, idesc0, 1u);
+              tc::mma_f16_pair(d0, ad + 384, bd + 6, idesc0, 1u);
+              if (two) {
+                const uint64_t bd1 = bd + (kSubBytes >> 4);   // second sub-tile's token rows
+                tc::mma_f16_pair(d1, ad, bd1, idesc1, acc);
+                tc::mma_f16_pair(d1, ad + 128, bd1 + 2, idesc1, 1u);
+                tc::mma_f16_pair(d1, ad + 256, bd1 + 4, idesc1, 1u);
+                tc::mma_f16_pair(d1, ad + 384, bd1 + 6, idesc1, 1u);
+              }
             }
           }
-          tc::mma_commit_pair(&empty[s], 0x3);  // frees the stage in both CTAs
-          if (++s == p.stages) { s = 0; ph ^= 1; }
+          tc::mma_commit_pair(&empty[g], 0x3);  // frees the group's stages in both CTAs
+          if (++g == ngroups) { g = 0; ph ^= 1; }
         }
         if (!ok) break;
         tc::mma_commit_pair(&acc_full[k % kAccRing], 0x3);
@@ -765,7 +781,7 @@ int max_pairs() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int c = 0;
-  if (cudaOccupancyMaxActiveClusters(&c, grouped_gemm_tc<false>, &cfg) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveClusters(&c, grouped_gemm_tc<false, 1>, &cfg) != cudaSuccess ||
       c <= 0) {
     cudaGetLastError();
     c = sms / 2;
@@ -781,9 +797,13 @@ moe_status_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUt
   static bool attr_set[kMaxDevicesCached] = {};
   const int dev = current_device();
   if (dev >= kMaxDevicesCached || !attr_set[dev]) {
-    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc<FP8>,
+    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc<FP8, 1>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
-    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc<FP8>,
+    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc<FP8, 1>,
+                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 0));
+    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc<FP8, 2>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc<FP8, 2>,
                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 0));
     if (dev < kMaxDevicesCached) attr_set[dev] = true;
   }
@@ -801,8 +821,12 @@ moe_status_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUt
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  MOE_CUDA_TRY(
-      cudaLaunchKernelEx(&cfg, grouped_gemm_tc<FP8>, a0, a1, b[0], b[1], b[2], b[3], p));
+  if (p.kgroup == 2)
+    MOE_CUDA_TRY(
+        cudaLaunchKernelEx(&cfg, grouped_gemm_tc<FP8, 2>, a0, a1, b[0], b[1], b[2], b[3], p));
+  else
+    MOE_CUDA_TRY(
+        cudaLaunchKernelEx(&cfg, grouped_gemm_tc<FP8, 1>, a0, a1, b[0], b[1], b[2], b[3], p));
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
@@ -812,7 +836,7 @@ moe_status_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUt
 namespace {
 
 struct TileCfg {
-  int tile_cap, wide, stages, stage_bytes;
+  int tile_cap, wide, stages, stage_bytes, kgroup;
 };
 
 // Token tile width: the expected largest expert (1.25x the average rows, or
@@ -830,6 +854,14 @@ TileCfg tile_config(int A_max, int N, int capacity) {
   c.stage_bytes = c.wide ? kABytes + 2 * kSubBytes : kABytes + (c.tile_cap / 2) * kBK * 2;
   c.stages = kStageRegion / c.stage_bytes;
   if (c.stages > kMaxStages) c.stages = kMaxStages;
+  // Every barrier wait and commit in the MMA issuer's loop costs about as much
+  // as issuing an MMA.  Where an expert spans many token tiles (the weights
+  // come from L2 and the tensor pipe is the limit) two stages share one
+  // barrier pair: one wait and one commit per 128 K (measured: prefill 2%
+  // faster).  Where the weights stream from DRAM the finer release of one
+  // pair per stage measured faster (DeepSeek-shaped, capacity layers).
+  const long tiles = (exp_rows + c.tile_cap - 1) / c.tile_cap;
+  c.kgroup = (tiles > 2 && c.stages % 2 == 0) ? 2 : 1;
   return c;
 }
 
@@ -859,7 +891,7 @@ moe_status_t launch_down(const int32_t *offsets, const float *row_scale, int A_m
   }
   TcParams p2{offsets, N, f, d, (d + 255) / 256, 0, static_cast<__nv_bfloat16 *>(y_perm), d,
               row_scale, device_status, raster_group(f), tc_.tile_cap, tc_.wide, tc_.stages,
-              tc_.stage_bytes};
+              tc_.kgroup, tc_.stage_bytes};
   return launch_gemm<false>(wd, wd, bh, p2, stream);
 }
 
@@ -884,7 +916,7 @@ moe_status_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, const flo
   }
   const TileCfg c = tile_config(A_max, N, capacity);
   TcParams p1{offsets, N, d, f, (f + 127) / 128, 1, static_cast<__nv_bfloat16 *>(h), f, nullptr,
-              device_status, raster_group(d), c.tile_cap, c.wide, c.stages, c.stage_bytes};
+              device_status, raster_group(d), c.tile_cap, c.wide, c.stages, c.kgroup, c.stage_bytes};
   s = launch_gemm<false>(wg, wu, bx, p1, stream);
   if (s != MOE_OK) return s;
   return launch_down(offsets, row_scale, A_max, d, f, N, c, W_down, h, y_perm, device_status,
@@ -939,7 +971,7 @@ moe_status_t launch_ffn_tc_fp8(const void *xq_perm, const float *x_scale,
   }
   const TileCfg c = tile_config(A_max, N, capacity);
   TcParams p1{offsets, N, d, f, (f + 127) / 128, 1, static_cast<__nv_bfloat16 *>(h), f, nullptr,
-              device_status, raster_group(d), c.tile_cap, c.wide, c.stages, c.stage_bytes,
+              device_status, raster_group(d), c.tile_cap, c.wide, c.stages, c.kgroup, c.stage_bytes,
               sw_gate, sw_up, x_scale, perm_token, h_f32 ? 1 : 0};
   s = launch_gemm<true>(wg, wu, bx, p1, stream);
   if (s != MOE_OK) return s;
@@ -950,7 +982,7 @@ moe_status_t launch_ffn_tc_fp8(const void *xq_perm, const float *x_scale,
   if (s != MOE_OK) return s;
   TcParams p2{offsets, N, f, d, (d + 255) / 256, 0, static_cast<__nv_bfloat16 *>(y_perm), d,
               row_scale, device_status, raster_group(f), c.tile_cap, c.wide, c.stages,
-              c.stage_bytes, sw_down, nullptr, hs, nullptr};
+              c.kgroup, c.stage_bytes, sw_down, nullptr, hs, nullptr};
   return launch_gemm<true>(wd, wd, bh, p2, stream);
 }
 
