@@ -113,12 +113,13 @@ def test_layer_fp8_reduced(name, down):
 
 @pytest.mark.parametrize("down", [False, True], ids=["bf16_down", "fp8_down"])
 @pytest.mark.parametrize("name,rows", [("mixtral_decode", None), ("capacity", None),
-                                       ("mixtral_prefill", 512), ("deepseek", 512)])
+                                       ("mixtral_prefill", 512), ("deepseek", 256)])
 def test_layer_fp8_full_size(name, rows, down):
     """The FP8 layer at the sizes the benchmark times: codes and scales of
     every weight bit-exact, routing and the output of sampled rows (all rows
-    on the decode and capacity layers; 512 seeded rows with the first and last
-    token on the prefill and DeepSeek layers) against the oracle."""
+    on the decode and capacity layers; seeded rows with the first and last
+    token on the prefill (512) and DeepSeek (256: 2048 routed rows, every
+    expert touched) layers) against the oracle."""
     cfg = CONFIGS[name]
     inp = make_inputs(cfg, device=torch.device("cuda"))
     sel = None
