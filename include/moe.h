@@ -70,6 +70,7 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
 #define MOE_DEV_NAN_LOGIT 0x2     /* a router logit was NaN (ranked last)           */
 #define MOE_DEV_TIMEOUT 0x4       /* a bounded on-chip wait gave up; output invalid */
 #define MOE_DEV_BAD_TILE 0x8      /* grouped-GEMM tile outside the expert layout     */
+#define MOE_DEV_BAD_COUNTS 0x10   /* expert-parallel counts do not add up to the rows */
 
 const char *moe_status_string(moe_status_t s);
 const char *moe_last_error(void);
@@ -354,6 +355,46 @@ moe_status_t moe_forward_host_io_overlapped(const moe_forward_args *args,
                                             size_t workspace_bytes, int chunks,
                                             void *stream, void *h2d_stream,
                                             void *d2h_stream);
+
+/* ---------------------------------------------------------------------------
+ * Expert parallelism: the device steps around the two all-to-all exchanges.
+ * Source: "MoE 分片：混合專家模型的平行化策略", sections 專家平行化詳解 (the N
+ * experts split over G GPUs) and 動態 token 路由 steps 3-5 (rows go to the
+ * GPU holding their expert, are computed there and come back);
+ * "MoE稀疏激活原理与工程实践", 2.2 (one all-to-all per routing step).
+ *
+ * Rank r holds experts [r*Ne, (r+1)*Ne), N = G*Ne.  Its moe_permute over all
+ * N experts orders its rows by expert, so the rows for rank q are the
+ * contiguous range x_perm[offsets[q*Ne] : offsets[(q+1)*Ne]) and need no
+ * packing.  The caller exchanges, with its own collective library, each
+ * rank's kept counts per expert and then those row ranges (and their
+ * row_scale values); rank r then holds, from each source s in turn, the rows
+ * of each of its experts e: block (s, e), recv_counts[s*Ne + e] rows.
+ *
+ * moe_ep_regroup: moves block (s, e) to expert e's range, after the blocks of
+ *   sources 0..s-1 (stable), so the grouped GEMM sees each expert's rows
+ *   together:
+ *   recv_counts [G*Ne] device int32; x_recv [R,d] (dtype) and row_scale_recv
+ *   [R] fp32 (or NULL) in received order, R = sum of recv_counts.
+ *   Outputs: x_local [R,d], row_scale_local [R] (if row_scale_recv),
+ *   offsets_local [Ne+1] (moe_expert_ffn's offsets over the local experts),
+ *   dest [R] int32: where received row i went.  If the counts do not add up
+ *   to R nothing is copied and MOE_DEV_BAD_COUNTS is set.
+ * moe_ep_return: y_back[i] = y_local[dest[i]], the expert outputs put back in
+ *   received order, ready for the return exchange; afterwards the source
+ *   rank's rows are in its own x_perm order and moe_combine finishes the layer.
+ * Requirements: 1 <= G, 1 <= Ne, G*Ne <= 4096, d*sizeof(dtype) % 16 == 0,
+ * 16-byte aligned rows.  No workspace; asynchronous on `stream`.
+ * ------------------------------------------------------------------------- */
+moe_status_t moe_ep_regroup(const int32_t *recv_counts, int G, int Ne,
+                            const void *x_recv, const float *row_scale_recv,
+                            int R, int d, moe_dtype_t dtype, void *x_local,
+                            float *row_scale_local, int32_t *offsets_local,
+                            int32_t *dest, int32_t *device_status,
+                            void *stream);
+moe_status_t moe_ep_return(const void *y_local, const int32_t *dest, int R,
+                           int d, moe_dtype_t dtype, void *y_back,
+                           void *stream);
 
 /* ---------------------------------------------------------------------------
  * Routing diagnostics (forward only): how evenly the router spreads the load.

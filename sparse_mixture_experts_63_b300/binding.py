@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(_PKG, "libmoe.so")
 
 MOE_F32, MOE_BF16 = 0, 1
 MOE_DEV_BAD_EXPERT_ID, MOE_DEV_NAN_LOGIT, MOE_DEV_TIMEOUT, MOE_DEV_BAD_TILE = 1, 2, 4, 8
+MOE_DEV_BAD_COUNTS = 16
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE"}
 
@@ -30,7 +31,8 @@ EXPORTS = ("moe_status_string", "moe_last_error", "moe_version", "moe_launch_cou
            "moe_routing_stats_workspace_size", "moe_routing_stats",
            "moe_permute_reroute_workspace_size", "moe_permute_reroute",
            "moe_quantize_weights_e4m3", "moe_quantize_rows_e4m3",
-           "moe_expert_ffn_fp8_workspace_size", "moe_expert_ffn_fp8")
+           "moe_expert_ffn_fp8_workspace_size", "moe_expert_ffn_fp8",
+           "moe_ep_regroup", "moe_ep_return")
 
 
 class MoEError(RuntimeError):
@@ -112,7 +114,10 @@ def lib():
         L.moe_expert_ffn_fp8_workspace_size.restype = sz
         L.moe_expert_ffn_fp8.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, vp, vp, vp, vp, vp,
                                          vp, vp, vp, vp, vp, sz, vp]
+        L.moe_ep_regroup.argtypes = [vp, ci, ci, vp, vp, ci, ci, ci, vp, vp, vp, vp, vp, vp]
+        L.moe_ep_return.argtypes = [vp, vp, ci, ci, ci, vp, vp]
         for n in ("moe_router_topk", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn",
+                  "moe_ep_regroup", "moe_ep_return",
                   "moe_quantize_weights_e4m3", "moe_quantize_rows_e4m3", "moe_expert_ffn_fp8",
                   "moe_combine", "moe_routing_stats", "moe_permute_reroute",
                   "moe_forward", "moe_forward_host_io", "moe_forward_host_io_overlapped"):
@@ -379,6 +384,38 @@ def moe_combine(y_perm, inv_pos, shared_y=None, y=None, y_dtype=torch.float32, s
         _p(y_perm), _dt(y_perm), _p(inv_pos), T, k, d, _p(shared_y), _p(y), _dt(y),
         _stream(stream)))
     return y
+
+
+def moe_ep_regroup(recv_counts, Ne, x_recv, row_scale_recv=None, device_status=None,
+                   stream=None):
+    """Rows received from G source ranks (block (s, e) = recv_counts[s*Ne + e]
+    rows, in (s, e) order) regrouped by local expert.  Returns dict x_local,
+    row_scale_local (or None), offsets_local [Ne+1], dest [R]."""
+    _cuda(recv_counts, x_recv, row_scale_recv)
+    G = recv_counts.numel() // Ne
+    R, d = x_recv.shape
+    dev = x_recv.device
+    out = dict(x_local=torch.empty((max(R, 1), d), dtype=x_recv.dtype, device=dev),
+               row_scale_local=(torch.empty(max(R, 1), dtype=torch.float32, device=dev)
+                                if row_scale_recv is not None else None),
+               offsets_local=torch.empty(Ne + 1, dtype=torch.int32, device=dev),
+               dest=torch.empty(max(R, 1), dtype=torch.int32, device=dev))
+    _check("moe_ep_regroup", lib().moe_ep_regroup(
+        _p(recv_counts), G, Ne, _p(x_recv), _p(row_scale_recv), R, d, _dt(x_recv),
+        _p(out["x_local"]), _p(out["row_scale_local"]), _p(out["offsets_local"]),
+        _p(out["dest"]), _p(device_status), _stream(stream)))
+    return out
+
+
+def moe_ep_return(y_local, dest, R, y_back=None, stream=None):
+    """y_back[i] = y_local[dest[i]] for the R received rows."""
+    _cuda(y_local, dest, y_back)
+    d = y_local.shape[1]
+    if y_back is None:
+        y_back = torch.empty((max(R, 1), d), dtype=y_local.dtype, device=y_local.device)
+    _check("moe_ep_return", lib().moe_ep_return(
+        _p(y_local), _p(dest), R, d, _dt(y_local), _p(y_back), _stream(stream)))
+    return y_back
 
 
 def make_forward_args(x, W_g, W_gate, W_up, W_down, k, y, bias=None, Ws_gate=None,

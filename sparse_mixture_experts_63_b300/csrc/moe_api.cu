@@ -466,6 +466,41 @@ moe_status_t moe_combine(const void *y_perm, moe_dtype_t y_perm_dtype, const int
                         static_cast<cudaStream_t>(stream));
 }
 
+moe_status_t moe_ep_regroup(const int32_t *recv_counts, int G, int Ne, const void *x_recv,
+                            const float *row_scale_recv, int R, int d, moe_dtype_t dtype,
+                            void *x_local, float *row_scale_local, int32_t *offsets_local,
+                            int32_t *dest, int32_t *device_status, void *stream) {
+  CHECK_ARG(dtype_ok(dtype), "bad dtype");
+  CHECK_ARG(G >= 1 && Ne >= 1 && R >= 0 && d >= 1, "bad sizes G=%d Ne=%d R=%d d=%d", G, Ne, R, d);
+  if ((long)G * Ne > ep_max_blocks()) {
+    set_error("moe_ep_regroup: G*Ne = %ld exceeds %d", (long)G * Ne, ep_max_blocks());
+    return MOE_ERR_UNSUPPORTED;
+  }
+  CHECK_ARG(((size_t)d * esize(dtype)) % 16 == 0, "rows must be a multiple of 16 bytes (d=%d)", d);
+  CHECK_ARG(recv_counts && offsets_local && (R == 0 || (x_recv && x_local && dest)),
+            "required pointer is NULL");
+  CHECK_ARG(!row_scale_recv || row_scale_local || R == 0, "row_scale_local is NULL");
+  CHECK_ARG(aligned16(x_recv) && aligned16(x_local), "tensors must be 16-byte aligned");
+  moe_status_t s = check_device();
+  if (s != MOE_OK) return s;
+  return launch_ep_regroup(recv_counts, G, Ne, x_recv, row_scale_recv, R,
+                           (size_t)d * esize(dtype), x_local, row_scale_local, offsets_local,
+                           dest, device_status, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_ep_return(const void *y_local, const int32_t *dest, int R, int d,
+                           moe_dtype_t dtype, void *y_back, void *stream) {
+  CHECK_ARG(dtype_ok(dtype), "bad dtype");
+  CHECK_ARG(R >= 0 && d >= 1, "bad sizes R=%d d=%d", R, d);
+  CHECK_ARG(((size_t)d * esize(dtype)) % 16 == 0, "rows must be a multiple of 16 bytes (d=%d)", d);
+  CHECK_ARG(R == 0 || (y_local && dest && y_back), "required pointer is NULL");
+  CHECK_ARG(aligned16(y_local) && aligned16(y_back), "tensors must be 16-byte aligned");
+  moe_status_t s = check_device();
+  if (s != MOE_OK) return s;
+  return launch_ep_return(y_local, dest, R, (size_t)d * esize(dtype), y_back,
+                          static_cast<cudaStream_t>(stream));
+}
+
 static moe_status_t validate_forward(const moe_forward_args *a) {
   CHECK_ARG(a, "args is NULL");
   CHECK_ARG(dtype_ok(a->dtype) && dtype_ok(a->y_dtype), "bad dtype");

@@ -201,4 +201,14 @@ moe_status_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, const flo
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Expert parallelism (ep.cu): regroup received rows by local expert, and put
+// the expert outputs back in received order.
+int ep_max_blocks();
+moe_status_t launch_ep_regroup(const int32_t *recv_counts, int G, int Ne, const void *x_recv,
+                               const float *row_scale_recv, int R, size_t row_bytes,
+                               void *x_local, float *row_scale_local, int32_t *offsets_local,
+                               int32_t *dest, int32_t *device_status, cudaStream_t stream);
+moe_status_t launch_ep_return(const void *y_local, const int32_t *dest, int R, size_t row_bytes,
+                              void *y_back, cudaStream_t stream);
+
 }  // namespace moe

@@ -208,3 +208,22 @@ def test_forward_args_layout_matches_header(tmp_path):
                                           check=True).stdout.split()]
     assert got[0] == ctypes.sizeof(B.moe_forward_args)
     assert got[1:] == [getattr(B.moe_forward_args, n).offset for n in fields]
+
+
+def test_ep_argument_errors(lib):
+    """moe_ep_regroup / moe_ep_return reject bad sizes on the host, before any launch."""
+    fake = ctypes.c_void_p(4096)
+    # G * Ne beyond the supported 4096 blocks
+    assert lib.moe_ep_regroup(fake, 64, 65, fake, None, 10, 64, B.MOE_BF16, fake, None, fake, fake,
+                              None, None) == 2
+    # rows that are not a multiple of 16 bytes (bf16, d = 4)
+    assert lib.moe_ep_regroup(fake, 2, 2, fake, None, 10, 4, B.MOE_BF16, fake, None, fake, fake,
+                              None, None) == 1
+    # missing destination map
+    assert lib.moe_ep_regroup(fake, 2, 2, fake, None, 10, 64, B.MOE_BF16, fake, None, fake, None,
+                              None, None) == 1
+    # a row scale in without one out
+    assert lib.moe_ep_regroup(fake, 2, 2, fake, fake, 10, 64, B.MOE_BF16, fake, None, fake, fake,
+                              None, None) == 1
+    assert lib.moe_ep_return(fake, None, 10, 64, B.MOE_BF16, fake, None) == 1
+    assert lib.moe_ep_return(fake, fake, -1, 64, B.MOE_BF16, fake, None) == 1
