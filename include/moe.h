@@ -341,8 +341,8 @@ moe_status_t moe_forward_host_io(const moe_forward_args *args,
  * depends on that token alone, so y equals moe_forward_host_io's -- except
  * under a capacity limit or re-routing, whose drops depend on the whole
  * batch: there chunks is taken as 1.  chunks <= 0: moe_forward_overlap_chunks
- * (as many as keep each batch's tensor work at least twice the time to
- * stream its weights again, at most one per 2048 tokens, 16 in all).  The
+ * (as many as keep each batch's tensor work at least four times the time
+ * to stream its weights again, at most one per 2048 tokens, 16 in all).  The
  * call returns y only: the routing outputs of args must be NULL.  Three
  * distinct streams; workspace: moe_forward_workspace_size(args).  Pinned
  * host memory makes the copies asynchronous.  The first call on a host thread

@@ -169,16 +169,18 @@ moe_status_t validate_ffn(const void *x_perm, const int32_t *offsets, int A_max,
 constexpr int kMaxChunks = 16;
 
 // Chunks for the overlapped host-buffer call: as many as keep each chunk's
-// tensor work at least twice its weight streaming (every chunk reads every
+// tensor work at least four times its weight streaming (every chunk reads every
 // touched expert's weights again), at most one per 2048 tokens and 16 in all;
-// estimated with 274 FLOP per byte (dense bf16 rate over copy bandwidth).
+// estimated with 274 FLOP per byte (dense bf16 rate over copy bandwidth).  On
+// the prefill layer that is 3 chunks: measured best among 1-16 (10.8 ms;
+// 7 chunks, from a factor of two, took 11.1-11.4 ms).
 int auto_chunks(const moe_forward_args *a) {
   const double kFlopPerByte = 274.0;
   const double rows = (double)a->T * a->k;
   const double flop = 6.0 * rows * a->d * a->f + 6.0 * (double)a->T * a->d * a->fs;
   const double touched = rows < a->N ? rows : a->N;
   const double bytes = esize(a->dtype) * (3.0 * a->d * a->f * touched + 3.0 * (double)a->d * a->fs);
-  int n = (int)(flop / (2.0 * bytes * kFlopPerByte));
+  int n = (int)(flop / (4.0 * bytes * kFlopPerByte));
   const int by_tokens = a->T / 2048;
   if (n > by_tokens) n = by_tokens;
   if (n > kMaxChunks) n = kMaxChunks;
