@@ -76,7 +76,11 @@ constexpr int kNumBoxes = 4;                             // B box heights 32/64/
 constexpr int kChunks = 16;                              // 32-column chunks of tensor memory
 constexpr int kAccRing = 16;                             // acc_full barriers (sub-tile ring)
 constexpr int kEpiThreads = 128;
-constexpr int kThreads = 64 + kEpiThreads;
+// Warps: 0 TMA producer, 1 MMA issuer (and tensor-memory allocator), with two
+// MMA issuers (wide layers) 2 the second issuer; then 4 epilogue warps.
+constexpr int epi_warp0(bool dual) { return dual ? 3 : 2; }
+constexpr int threads_for(bool dual) { return 32 * epi_warp0(dual) + kEpiThreads; }
+constexpr int kMaxThreads = threads_for(true);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kMaxExperts = 1024;
@@ -95,7 +99,7 @@ struct Smem {
   static constexpr int x = kStageRegion;
   static constexpr int out = x + kXBytes;
   static constexpr int bars = out + kOutBytes;                    // 8-byte aligned
-  static constexpr int nbars = 2 * kMaxStages + kAccRing + kChunks + 1;
+  static constexpr int nbars = 2 * kMaxStages + kAccRing + kChunks + 2;
   static constexpr int tmem_slot = bars + nbars * 8;
   static constexpr int abort_flag = tmem_slot + 4;
   static constexpr int epi_ok = abort_flag + 4;
@@ -356,8 +360,8 @@ __device__ __forceinline__ void scale_chunk(const TcParams &p, int row0, int val
 // stage (the same 128-byte rows as 64 bf16), kind::f8f6f4 MMAs, and the
 // channel x row scales applied to D before SwiGLU (GEMM1) or the gate-weight
 // scale (GEMM2).
-template <bool FP8, int G>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool FP8, int G, bool DUAL>
+__global__ void __launch_bounds__(kMaxThreads, 1)
     grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
                     const __grid_constant__ CUtensorMap tmB0,
@@ -376,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *acc_full = bars + 2 * kMaxStages;   // [kAccRing] sub-tile accumulated
   uint64_t *col_free = acc_full + kAccRing;     // [kChunks]  chunk loaded by the epilogue
                                                 //            (used in the even CTA)
-  uint64_t *drain = col_free + kChunks;         // [1]
+  uint64_t *drain = col_free + kChunks;         // [2] one per MMA issuer
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::tmem_slot);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Smem::abort_flag);
   int *prefix = reinterpret_cast<int *>(smem + Smem::tile_prefix);
@@ -388,11 +392,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
       tc::mbar_init(&full[s], 1);
-      tc::mbar_init(&empty[s], 1);
+      tc::mbar_init(&empty[s], DUAL ? 2 : 1);   // each MMA issuer commits every group
     }
     for (int b = 0; b < kAccRing; ++b) tc::mbar_init(&acc_full[b], 1);
     for (int c = 0; c < kChunks; ++c) tc::mbar_init(&col_free[c], 2 * kEpiThreads / 32);
-    tc::mbar_init(drain, 1);
+    tc::mbar_init(&drain[0], 1);
+    tc::mbar_init(&drain[1], 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
     tc::fence_proxy_async();
@@ -492,11 +497,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer --
-    // Even CTA only.  Lane 0 runs a tight loop: the gap between the last MMA of
-    // one stage and the first of the next must stay shorter than the work the
-    // tensor pipe still has queued, or it idles.
+  } else if (warp == 1 || (DUAL && warp == 2)) {
+    // --------------------------------------------------------- MMA issuers --
+    // Even CTA only.  Lane 0 of warp 1 issues the first token sub-tile's MMAs,
+    // lane 0 of warp 2 the second's (wide layers): one tcgen05.mma takes ~72
+    // cycles to issue whatever its N, so one thread issuing both sub-tiles'
+    // eight MMAs per K step fell behind the tensor pipe.  Both walk the same
+    // tiles and stages, wait on every full barrier and commit every stage
+    // group (the empty barriers count two arrivals), and both track every
+    // tensor-memory chunk's uses, waiting only for their own sub-tile's.
+    // Each loop stays tight: the gap between the last MMA of one stage and the
+    // first of the next must stay shorter than the work the tensor pipe still
+    // has queued, or it idles.
+    // Layers without wide tiles have one token sub-tile per tile: their kernel
+    // instance has the first issuer only (DUAL false, one arrival per stage).
+    const int role = warp - 1;   // 0: sub-tile 0, 1: sub-tile 1
     if (rank == 0 && lane == 0) {
       const uint32_t stage0 = tc::smem_u32(smem + Smem::stages);
       // descriptors of stage 0; stage s adds (s * stage_bytes) >> 4 to the start field
@@ -528,14 +543,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // since its previous use
         const int e0 = c0 + (n0 + 31) / 32;
         for (int c = c0; c < e0 && ok; ++c) {
-          ok = tc::mbar_wait_bounded(&col_free[c], ((cuse >> c) & 1) ^ 1, abort_flag, kTimeoutNs);
+          if (role == 0)
+            ok = tc::mbar_wait_bounded(&col_free[c], ((cuse >> c) & 1) ^ 1, abort_flag,
+                                       kTimeoutNs);
           cuse ^= 1u << c;
         }
         if (two) {
           const int e1 = c1 + (n1 + 31) / 32;
           for (int c = c1; c < e1 && ok; ++c) {
-            ok = tc::mbar_wait_bounded(&col_free[c], ((cuse >> c) & 1) ^ 1, abort_flag,
-                                       kTimeoutNs);
+            if (role == 1)
+              ok = tc::mbar_wait_bounded(&col_free[c], ((cuse >> c) & 1) ^ 1, abort_flag,
+                                         kTimeoutNs);
             cuse ^= 1u << c;
           }
         }
@@ -557,11 +575,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t acc = (kb + h) > 0 ? 1u : 0u;   // the tile's first K step overwrites
             if (FP8) {
               // both K-major: 32 k of 8 bits = 32 B further inside the 128-B rows (+2)
-              tc::mma_f8_pair(d0, ad, bd, idesc0, acc);
-              tc::mma_f8_pair(d0, ad + 2, bd + 2, idesc0, 1u);
-              tc::mma_f8_pair(d0, ad + 4, bd + 4, idesc0, 1u);
-              tc::mma_f8_pair(d0, ad + 6, bd + 6, idesc0, 1u);
-              if (two) {
+              if (role == 0) {
+                tc::mma_f8_pair(d0, ad, bd, idesc0, acc);
+                tc::mma_f8_pair(d0, ad + 2, bd + 2, idesc0, 1u);
+                tc::mma_f8_pair(d0, ad + 4, bd + 4, idesc0, 1u);
+                tc::mma_f8_pair(d0, ad + 6, bd + 6, idesc0, 1u);
+              } else if (two) {
                 const uint64_t bd1 = bd + (kSubBytes >> 4);
                 tc::mma_f8_pair(d1, ad, bd1, idesc1, acc);
                 tc::mma_f8_pair(d1, ad + 2, bd1 + 2, idesc1, 1u);
@@ -571,11 +590,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
               // A MN-major: 16 k-rows = two 1024-B atoms further (+128 in 16-B units);
               // B K-major: 16 k = 32 B further inside the 128-B swizzled row (+2).
-              tc::mma_f16_pair(d0, ad, bd, idesc0, acc);
-              tc::mma_f16_pair(d0, ad + 128, bd + 2, idesc0, 1u);
-              tc::mma_f16_pair(d0, ad + 256, bd + 4, idesc0, 1u);
-              tc::mma_f16_pair(d0, ad + 384, bd + 6, idesc0, 1u);
-              if (two) {
+              if (role == 0) {
+                tc::mma_f16_pair(d0, ad, bd, idesc0, acc);
+                tc::mma_f16_pair(d0, ad + 128, bd + 2, idesc0, 1u);
+                tc::mma_f16_pair(d0, ad + 256, bd + 4, idesc0, 1u);
+                tc::mma_f16_pair(d0, ad + 384, bd + 6, idesc0, 1u);
+              } else if (two) {
                 const uint64_t bd1 = bd + (kSubBytes >> 4);   // second sub-tile's token rows
                 tc::mma_f16_pair(d1, ad, bd1, idesc1, acc);
                 tc::mma_f16_pair(d1, ad + 128, bd1 + 2, idesc1, 1u);
@@ -588,20 +608,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++g == ngroups) { g = 0; ph ^= 1; }
         }
         if (!ok) break;
-        tc::mma_commit_pair(&acc_full[k % kAccRing], 0x3);
-        if (two) tc::mma_commit_pair(&acc_full[(k + 1) % kAccRing], 0x3);
+        if (role == 0) tc::mma_commit_pair(&acc_full[k % kAccRing], 0x3);
+        if (two && role == 1) tc::mma_commit_pair(&acc_full[(k + 1) % kAccRing], 0x3);
         k += two ? 2 : 1;
       }
-      // Drain: make sure no MMA is still reading shared or writing tensor memory.
-      tc::mma_commit_pair(drain, 0x1);
+      // Drain: make sure none of this issuer's MMAs is still reading shared or
+      // writing tensor memory.
+      tc::mma_commit_pair(&drain[role], 0x1);
       volatile int dummy = 0;
-      tc::mbar_wait_bounded(drain, 0, &dummy, kTimeoutNs);
+      tc::mbar_wait_bounded(&drain[role], 0, &dummy, kTimeoutNs);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue --
     const int lane_grp = warp % 4;           // TMEM lanes 32*lane_grp .. +31
-    const int etid = threadIdx.x - 64;       // 0..127
+    const int etid = threadIdx.x - 32 * epi_warp0(DUAL);   // 0..127
     volatile int *epi_ok = reinterpret_cast<volatile int *>(smem + Smem::epi_ok);
     float *xbuf = reinterpret_cast<float *>(smem + Smem::x);
     __nv_bfloat16 *obuf = reinterpret_cast<__nv_bfloat16 *>(smem + Smem::out);
@@ -776,12 +797,12 @@ int max_pairs() {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(2 * (sms / 2));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kMaxThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int c = 0;
-  if (cudaOccupancyMaxActiveClusters(&c, grouped_gemm_tc<false, 1>, &cfg) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveClusters(&c, grouped_gemm_tc<false, 1, true>, &cfg) != cudaSuccess ||
       c <= 0) {
     cudaGetLastError();
     c = sms / 2;
@@ -797,14 +818,12 @@ moe_status_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUt
   static bool attr_set[kMaxDevicesCached] = {};
   const int dev = current_device();
   if (dev >= kMaxDevicesCached || !attr_set[dev]) {
-    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc<FP8, 1>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
-    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc<FP8, 1>,
-                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 0));
-    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc<FP8, 2>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
-    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_tc<FP8, 2>,
-                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 0));
+    for (auto fn : {grouped_gemm_tc<FP8, 1, false>, grouped_gemm_tc<FP8, 2, false>,
+                    grouped_gemm_tc<FP8, 1, true>}) {
+      MOE_CUDA_TRY(
+          cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+      MOE_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 0));
+    }
     if (dev < kMaxDevicesCached) attr_set[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
@@ -816,17 +835,15 @@ moe_status_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUt
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_begin
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(2 * max_pairs());
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads_for(p.wide != 0));
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (p.kgroup == 2)
-    MOE_CUDA_TRY(
-        cudaLaunchKernelEx(&cfg, grouped_gemm_tc<FP8, 2>, a0, a1, b[0], b[1], b[2], b[3], p));
-  else
-    MOE_CUDA_TRY(
-        cudaLaunchKernelEx(&cfg, grouped_gemm_tc<FP8, 1>, a0, a1, b[0], b[1], b[2], b[3], p));
+  // wide layers: one barrier pair per stage, two MMA issuers
+  auto fn = p.wide ? grouped_gemm_tc<FP8, 1, true>
+          : p.kgroup == 2 ? grouped_gemm_tc<FP8, 2, false> : grouped_gemm_tc<FP8, 1, false>;
+  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, fn, a0, a1, b[0], b[1], b[2], b[3], p));
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
