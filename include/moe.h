@@ -334,7 +334,9 @@ moe_status_t moe_forward_host_io(const moe_forward_args *args,
                                  void *stream);
 
 /* The host-buffer call with the copies overlapped with the layer: the T
- * tokens run as `chunks` consecutive batches on `stream`; every chunk's x
+ * tokens run as `chunks` consecutive batches on `stream` (with three or more,
+ * the first and the last half the size of the others: their copy in and copy
+ * out are what no compute hides); every chunk's x
  * rows go host->device on h2d_stream (all issued at once, each batch waits
  * for its own), and each batch's y rows go back on d2h_stream as soon as it
  * is done; `stream` then waits for the last copy.  Each token's output row

@@ -172,8 +172,7 @@ constexpr int kMaxChunks = 16;
 // tensor work at least four times its weight streaming (every chunk reads every
 // touched expert's weights again), at most one per 2048 tokens and 16 in all;
 // estimated with 274 FLOP per byte (dense bf16 rate over copy bandwidth).  On
-// the prefill layer that is 3 chunks: measured best among 1-16 (10.8 ms;
-// 7 chunks, from a factor of two, took 11.1-11.4 ms).
+// the prefill layer that is 3 chunks, measured best among 1-16.
 int auto_chunks(const moe_forward_args *a) {
   const double kFlopPerByte = 274.0;
   const double rows = (double)a->T * a->k;
@@ -678,21 +677,39 @@ moe_status_t moe_forward_host_io_overlapped(const moe_forward_args *a, const voi
   cudaEvent_t *ev = nullptr;
   if ((s = chunk_events(&ev)) != MOE_OK) return s;   // [0] start, [1..n] h2d, [n+1..2n] layer
   const size_t xr = (size_t)a->d * esize(a->dtype), yr = (size_t)a->d * esize(a->y_dtype);
-  const int Tc = (a->T + n - 1) / n;
-  n = (a->T + Tc - 1) / Tc;                    // no empty last chunk
+  // Chunk c covers tokens [start[c], start[c+1]).  With three or more chunks
+  // the first and the last are half the size of the others: the first one's
+  // copy in and the last one's copy out are the parts no compute hides.
+  int start[kMaxChunks + 1];
+  {
+    const double wsum = n >= 3 ? (double)(n - 1) : (double)n;   // 0.5 + (n-2) + 0.5
+    double acc = 0.0;
+    start[0] = 0;
+    for (int c = 0; c < n; ++c) {
+      acc += (n >= 3 && (c == 0 || c == n - 1)) ? 0.5 : 1.0;
+      start[c + 1] = c + 1 == n ? a->T : (int)((double)a->T * acc / wsum + 0.5);
+    }
+    bool empty = false;
+    for (int c = 0; c < n; ++c) empty = empty || start[c + 1] <= start[c];
+    if (empty) {                               // tiny batches: equal chunks, none empty
+      const int Tc = (a->T + n - 1) / n;
+      n = (a->T + Tc - 1) / Tc;
+      for (int c = 0; c <= n; ++c) start[c] = c * Tc < a->T ? c * Tc : a->T;
+    }
+  }
   // the copies start after the caller's earlier work on `stream`
   MOE_CUDA_TRY(cudaEventRecord(ev[0], stream));
   MOE_CUDA_TRY(cudaStreamWaitEvent(h2d, ev[0], 0));
   MOE_CUDA_TRY(cudaStreamWaitEvent(d2h, ev[0], 0));
   for (int c = 0; c < n; ++c) {
-    const size_t t0 = (size_t)c * Tc, tc = (size_t)(a->T - (int)t0 < Tc ? a->T - (int)t0 : Tc);
+    const size_t t0 = (size_t)start[c], tc = (size_t)(start[c + 1] - start[c]);
     MOE_CUDA_TRY(cudaMemcpyAsync(static_cast<char *>(const_cast<void *>(a->x)) + t0 * xr,
                                  static_cast<const char *>(x_host) + t0 * xr, tc * xr,
                                  cudaMemcpyHostToDevice, h2d));
     MOE_CUDA_TRY(cudaEventRecord(ev[1 + c], h2d));
   }
   for (int c = 0; c < n; ++c) {
-    const size_t t0 = (size_t)c * Tc, tc = (size_t)(a->T - (int)t0 < Tc ? a->T - (int)t0 : Tc);
+    const size_t t0 = (size_t)start[c], tc = (size_t)(start[c + 1] - start[c]);
     moe_forward_args ac = *a;
     ac.T = (int)tc;
     ac.x = static_cast<const char *>(a->x) + t0 * xr;
