@@ -17,7 +17,8 @@ One forward, per rank:
      put back in received order (moe_ep_return);
   5. the reverse exchange of the output rows, which land in the source rank's
      own x_perm order;
-  6. combine (moe_combine) into y.
+  6. combine (moe_combine) into y, with the optional always-on shared expert
+     (replicated: each rank runs it on its own tokens with moe_expert_ffn).
 Every step on the device is a libmoe kernel; this module only computes the
 split sizes and calls the exchange.  The exchange is an object with one
 method, all_to_all(out, inp, out_splits, in_splits), with the semantics of
@@ -90,19 +91,22 @@ class EPState:
     send_rows: List[int]
     recv_counts: Optional[torch.Tensor] = None   # [G*Ne] on the device
     recv_rows: Optional[List[int]] = None
+    shared_y: Optional[torch.Tensor] = None      # [T,d] shared expert output, if any
 
 
 class ExpertParallelMoE:
     """One rank's part of an expert-parallel layer.
 
-    W_g [d,N] and bias [N] are replicated; W_gate_local / W_up_local [Ne,d,f]
-    and W_down_local [Ne,f,d] are this rank's experts [rank*Ne, (rank+1)*Ne).
+    W_g [d,N], bias [N] and the shared expert (Ws_gate, Ws_up [d,fs], Ws_down
+    [fs,d], optional) are replicated; W_gate_local / W_up_local [Ne,d,f] and
+    W_down_local [Ne,f,d] are this rank's experts [rank*Ne, (rank+1)*Ne).
     `forward(x)` runs the whole layer with `exchange`; the step methods
     (dispatch, post_counts, experts, combine) let a caller drive several ranks
     in one process with its own exchange."""
 
     def __init__(self, W_g, W_gate_local, W_up_local, W_down_local, k, rank, world, exchange=None,
-                 bias=None, capacity_factor=0.0, y_dtype=torch.float32):
+                 bias=None, capacity_factor=0.0, y_dtype=torch.float32, Ws_gate=None, Ws_up=None,
+                 Ws_down=None):
         self.W_g, self.bias, self.k = W_g, bias, k
         self.Wg, self.Wu, self.Wd = W_gate_local, W_up_local, W_down_local
         self.rank, self.G = rank, world
@@ -110,6 +114,7 @@ class ExpertParallelMoE:
         self.N = W_g.shape[1]
         assert self.N == self.G * self.Ne, "N must equal world * local experts"
         self.cf, self.y_dtype = capacity_factor, y_dtype
+        self.Ws = None if Ws_gate is None else (Ws_gate, Ws_up, Ws_down)
         self.exchange = exchange if exchange is not None else TorchDistExchange()
         self.status = torch.zeros(1, dtype=torch.int32, device=W_g.device)
 
@@ -122,7 +127,12 @@ class ExpertParallelMoE:
         perm = B.moe_permute(idx, self.N, x=x, topk_w=w, capacity=cap,
                              device_status=self.status)
         counts, send_rows = plan_from_offsets(perm["offsets"].cpu(), self.G, self.Ne)
-        return EPState(T=T, A=sum(send_rows), perm=perm, counts=counts, send_rows=send_rows)
+        st = EPState(T=T, A=sum(send_rows), perm=perm, counts=counts, send_rows=send_rows)
+        if self.Ws is not None:   # the shared expert on this rank's own tokens, weight 1
+            off = torch.tensor([0, T], dtype=torch.int32, device=x.device)
+            st.shared_y = B.moe_expert_ffn(x, off, self.Ws[0][None], self.Ws[1][None],
+                                           self.Ws[2][None], device_status=self.status)
+        return st
 
     # after the counts exchange: the received counts (device) and row splits
     def post_counts(self, st: EPState, recv_counts):
@@ -142,7 +152,8 @@ class ExpertParallelMoE:
 
     # step 6: the output rows, back in this rank's x_perm order, combined
     def combine(self, st: EPState, y_perm):
-        return B.moe_combine(y_perm, st.perm["inv_pos"], y_dtype=self.y_dtype)
+        return B.moe_combine(y_perm, st.perm["inv_pos"], shared_y=st.shared_y,
+                             y_dtype=self.y_dtype)
 
     def forward(self, x):
         ex = self.exchange
@@ -155,3 +166,36 @@ class ExpertParallelMoE:
         return self.combine(st, y_perm)
 
     __call__ = forward
+
+
+def _split(t, sizes):
+    out, p = [], 0
+    for n in sizes:
+        out.append(t[p:p + n])
+        p += n
+    return out
+
+
+def _loopback(parts):
+    """out[r] = the parts every source s sends to r, in source order."""
+    G = len(parts)
+    return [torch.cat([parts[s][r] for s in range(G)]) for r in range(G)]
+
+
+def run_ranks_in_one_process(layers, xs):
+    """Drives G ranks' layers (rank r's ExpertParallelMoE and its tokens xs[r])
+    in one process on one device, doing each exchange as plain device copies:
+    the data movement an all-to-all performs, with no kernel waiting on another
+    rank's.  For checking the expert-parallel path on a single GPU.  Returns
+    each rank's y."""
+    G = len(layers)
+    Ne = layers[0].Ne
+    sts = [layers[r].dispatch(xs[r]) for r in range(G)]
+    recv = _loopback([list(torch.split(st.counts.to(xs[0].device), Ne)) for st in sts])
+    for r in range(G):
+        layers[r].post_counts(sts[r], recv[r])
+    x_recv = _loopback([_split(st.perm["x_perm"], st.send_rows) for st in sts])
+    s_recv = _loopback([_split(st.perm["row_scale"], st.send_rows) for st in sts])
+    y_back = [layers[r].experts(sts[r], x_recv[r], s_recv[r]) for r in range(G)]
+    y_perm = _loopback([_split(y_back[r], sts[r].recv_rows) for r in range(G)])
+    return [layers[r].combine(sts[r], y_perm[r]) for r in range(G)]

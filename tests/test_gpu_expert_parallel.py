@@ -73,37 +73,16 @@ def test_regroup_flags_counts_that_do_not_add_up():
     assert int(st.item()) & B.MOE_DEV_BAD_COUNTS
 
 
-def _loopback(parts_per_rank):
-    """out[r] = concatenation over sources s of the part s sends to r."""
-    G = len(parts_per_rank)
-    return [torch.cat([parts_per_rank[s][r] for s in range(G)]) for r in range(G)]
-
-
-def _split(t, sizes):
-    out, p = [], 0
-    for n in sizes:
-        out.append(t[p:p + n])
-        p += n
-    return out
-
-
 def _emulated_ep(cfg, G, seeds):
     inp = make_inputs(cfg, device=torch.device("cuda"))
     Ne = cfg.N // G
     layers = [EP.ExpertParallelMoE(inp.W_g, inp.W_gate[r * Ne:(r + 1) * Ne],
                                    inp.W_up[r * Ne:(r + 1) * Ne], inp.W_down[r * Ne:(r + 1) * Ne],
-                                   cfg.k, r, G, bias=inp.bias, capacity_factor=cfg.cf)
+                                   cfg.k, r, G, bias=inp.bias, capacity_factor=cfg.cf,
+                                   Ws_gate=inp.Ws_gate, Ws_up=inp.Ws_up, Ws_down=inp.Ws_down)
               for r in range(G)]
     xs = [make_x(cfg, device=torch.device("cuda"), seed=s) for s in seeds]
-    sts = [layers[r].dispatch(xs[r]) for r in range(G)]
-    rc = _loopback([list(torch.split(st.counts.cuda(), Ne)) for st in sts])
-    for r in range(G):
-        layers[r].post_counts(sts[r], rc[r])
-    xr = _loopback([_split(st.perm["x_perm"], st.send_rows) for st in sts])
-    sr = _loopback([_split(st.perm["row_scale"], st.send_rows) for st in sts])
-    yb = [layers[r].experts(sts[r], xr[r], sr[r]) for r in range(G)]
-    yp = _loopback([_split(yb[r], sts[r].recv_rows) for r in range(G)])
-    ys = [layers[r].combine(sts[r], yp[r]) for r in range(G)]
+    ys = EP.run_ranks_in_one_process(layers, xs)
     torch.cuda.synchronize()
     for L in layers:
         assert int(L.status.item()) == 0
@@ -115,13 +94,15 @@ def _emulated_ep(cfg, G, seeds):
     MoEConfig("ep_fine", T=300, d=256, f=256, N=16, k=4, seed=81),
     MoEConfig("ep_capacity", T=512, d=256, f=192, N=32, k=2, cf=1.25, bias_std=1.0, seed=82),
     MoEConfig("ep_f32", T=100, d=64, f=96, N=8, k=2, dtype="f32", seed=83),
+    MoEConfig("ep_shared", T=200, d=256, f=256, N=32, k=8, fs=256, seed=84),
 ], ids=lambda c: c.name)
 def test_expert_parallel_layer_emulated_ranks(cfg, G):
     seeds = [cfg.seed * 10 + r for r in range(G)]
     inp, xs, ys = _emulated_ep(cfg, G, seeds)
     single = B.MoELayer(inp.W_g, inp.W_gate, inp.W_up, inp.W_down, cfg.k, bias=inp.bias,
-                        capacity_factor=cfg.cf)
-    shared = None
+                        capacity_factor=cfg.cf, Ws_gate=inp.Ws_gate, Ws_up=inp.Ws_up,
+                        Ws_down=inp.Ws_down)
+    shared = None if not cfg.fs else (inp.Ws_gate.cpu(), inp.Ws_up.cpu(), inp.Ws_down.cpu())
     for r in range(G):
         x = xs[r]
         # the single-GPU layer on the same tokens: same kernels, same per-row math
