@@ -24,6 +24,10 @@ the host cores, on a bounded sample of the same workload per step.
 roofline (E4M3 bytes, FP8 FLOPs at twice the measured bf16 rate).  `e2e` is
 the same layer through the host-buffer call with pinned x in and y out, the
 copies overlapped with token chunks of the layer where that cannot change y.
+
+--ffn-vs-cublas R times only the routed expert FFN of the workload's expert
+shape on exactly R rows per expert, against cuBLAS batched GEMMs of the same
+shapes (context: what the library reaches on this power-capped chip).
 """
 import argparse
 import json
@@ -77,6 +81,11 @@ def parse():
                     help="with --fp8: the down projection in FP8 E4M3 too (h quantised per row)")
     ap.add_argument("--forward-only", action="store_true",
                     help="time moe_forward only (no stage, end-to-end or CPU legs)")
+    ap.add_argument("--ffn-vs-cublas", type=int, default=0, metavar="R",
+                    help="time only the routed expert FFN of the layer's expert shape with "
+                         "exactly R rows per expert, against cuBLAS batched GEMMs (torch.bmm) "
+                         "of the same shapes with the SwiGLU in torch (context for the chip's "
+                         "power-capped GEMM rate; one JSON line)")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the forward-only timing of the other bf16 workloads that the "
                          "default (prefill) run appends as `workloads`")
@@ -769,8 +778,93 @@ def run_reference(args, ws, rank):
     }
 
 
+def run_ffn_vs_cublas(args, local):
+    """The routed FFN (both grouped-GEMM launches, SwiGLU and gate scale fused)
+    on N experts of exactly R rows each, against the same FFN as cuBLAS
+    batched GEMMs: x_e [N,R,d] x [W_gate|W_up] [N,d,2f], SiLU(gate)*up in
+    torch, then h [N,R,f] x W_down [N,f,d]; and the two cuBLAS GEMMs alone.
+    Rounds of `steps` back-to-back calls per leg, the order rotated; medians
+    of CUDA events.  Useful FLOP 6*N*R*d*f in every leg."""
+    cfg = resolve_cfg(args)
+    dev = torch.device("cuda", local)
+    inp = make_inputs(cfg, device=dev)
+    N, d, f, R = cfg.N, cfg.d, cfg.f, args.ffn_vs_cublas
+    A = N * R
+    gen = torch.Generator(device=dev).manual_seed(cfg.seed)
+    x = torch.randn(A, d, device=dev, generator=gen).to(torch.bfloat16)
+    off = torch.arange(0, A + 1, R, dtype=torch.int32, device=dev)
+    y = torch.empty(A, d, dtype=torch.bfloat16, device=dev)
+    Wgu = torch.cat([inp.W_gate, inp.W_up], dim=2)
+    xe = x.view(N, R, d)
+    g = torch.empty(N, R, 2 * f, dtype=torch.bfloat16, device=dev)
+    h = torch.empty(N, R, f, dtype=torch.bfloat16, device=dev)
+    y2 = torch.empty(N, R, d, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    launches0 = B.moe_launch_counter()
+
+    def ours():
+        B.moe_expert_ffn(x, off, inp.W_gate, inp.W_up, inp.W_down, y_perm=y)
+
+    def cublas_gemms():
+        torch.bmm(xe, Wgu, out=g)
+        torch.bmm(h, inp.W_down, out=y2)
+
+    def cublas():
+        torch.bmm(xe, Wgu, out=g)
+        torch.mul(torch.nn.functional.silu(g[..., :f]), g[..., f:], out=h)
+        torch.bmm(h, inp.W_down, out=y2)
+
+    def timed(fn):
+        E = lambda: torch.cuda.Event(enable_timing=True)   # noqa: E731
+        evs = [(E(), E()) for _ in range(args.steps)]
+        for s, e in evs:
+            s.record(stream)
+            fn()
+            e.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(s.elapsed_time(e) for s, e in evs)
+
+    for _ in range(args.warmup):
+        ours()
+        cublas()
+    torch.cuda.synchronize()
+    rel = ((y.float() - y2.view(A, d).float()).norm() / y2.float().norm()).item()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t0 = time.perf_counter()
+    legs = (ours, cublas, cublas_gemms)
+    rounds = []
+    for r in range(3):   # each round starts with a different leg
+        t = {}
+        for j in range(3):
+            fn = legs[(r + j) % 3]
+            t[fn.__name__] = timed(fn)
+        rounds.append(t)
+    sampler.mark(t0, time.perf_counter())
+    clocks = sampler.stop()
+    flop = 6.0 * A * d * f
+    med = {k: statistics.median(t[k] for t in rounds) for k in rounds[0]}
+    return {"metric": "routed expert FFN TFLOP/s, ours vs cuBLAS batched GEMMs",
+            "workload": f"{cfg.name} expert shape: N={N} experts x {R} rows, d={d}, f={f}, bf16",
+            "ours_ms": round(med["ours"], 4), "ours_tflops": round(flop / med["ours"] / 1e9, 1),
+            "cublas_ms": round(med["cublas"], 4),
+            "cublas_tflops": round(flop / med["cublas"] / 1e9, 1),
+            "cublas_gemms_only_ms": round(med["cublas_gemms"], 4),
+            "cublas_gemms_only_tflops": round(flop / med["cublas_gemms"] / 1e9, 1),
+            "rounds_ms": [{k: round(v, 4) for k, v in t.items()} for t in rounds],
+            "rel_frobenius_ours_vs_cublas": float(f"{rel:.3g}"),
+            "gpu_launches": int(B.moe_launch_counter() - launches0), "clocks": clocks,
+            "timing": f"3 rounds of {args.steps} back-to-back calls per leg, the leg order "
+                      "rotated each round; median of CUDA events; weights larger than L2",
+            "legs": "ours = moe_expert_ffn (SwiGLU fused); cublas = two torch.bmm + SiLU(gate)*up "
+                    "in torch; cublas_gemms = the two torch.bmm alone (no SwiGLU: h is stale)"}
+
+
 def main():
     args = parse()
+    if args.ffn_vs_cublas > 0:
+        print(json.dumps(run_ffn_vs_cublas(args, 0)), flush=True)
+        return
     ws, rank, local = dist_setup(args)
     if args.impl == "reference":
         line = run_reference(args, ws, rank)
