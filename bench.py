@@ -220,6 +220,11 @@ class ClockSampler:
                         continue
         else:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return self.summary(rows)
+
+    def summary(self, rows):
+        """Summary of (host time or None, SM MHz, max SM MHz, reason bits)
+        samples: those inside the timed window when the rows carry host times."""
         if self.window is not None and rows and rows[0][0] is not None:
             t0, t1 = self.window
             inside = [r for r in rows if t0 <= r[0] <= t1]
@@ -238,8 +243,19 @@ class ClockSampler:
                 "source": self.source + ", timed window only"}
 
 
+STUCK_LOW = 0.75   # median SM clock under this fraction of max, with no reason: a clock lock
+
+
 def clocks_rejected(clocks):
-    return any(r in clocks.get("reasons", []) for r in BAD_REASONS)
+    """A run to measure again: the GPU slowed itself down (hardware or thermal
+    slowdown), or its SM clock sat well below its maximum with no clock-event
+    reason at all (a clock lock left by someone else).  A power cap alone
+    (`sw_power_cap`) is kept."""
+    reasons = clocks.get("reasons") or []
+    if any(r in reasons for r in BAD_REASONS):
+        return True
+    mhz, top = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    return bool(mhz and top and mhz < STUCK_LOW * top and not reasons)
 
 
 # --------------------------------------------------------------- helpers ----
