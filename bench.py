@@ -28,6 +28,10 @@ copies overlapped with token chunks of the layer where that cannot change y.
 --ffn-vs-cublas R times only the routed expert FFN of the workload's expert
 shape on exactly R rows per expert, against cuBLAS batched GEMMs of the same
 shapes (context: what the library reaches on this power-capped chip).
+
+--ep-emulate G times the expert-parallel layer over G ranks emulated on this
+one GPU (the all-to-alls as device copies) against the one-GPU layer on the
+same tokens: the device-side cost of the expert-parallel path.
 """
 import argparse
 import json
@@ -86,6 +90,11 @@ def parse():
                          "exactly R rows per expert, against cuBLAS batched GEMMs (torch.bmm) "
                          "of the same shapes with the SwiGLU in torch (context for the chip's "
                          "power-capped GEMM rate; one JSON line)")
+    ap.add_argument("--ep-emulate", type=int, default=0, metavar="G",
+                    help="time the expert-parallel layer over G ranks emulated on this one GPU "
+                         "(every rank's layer and batch in one process, the all-to-alls as "
+                         "device copies) against the one-GPU layer on the same tokens "
+                         "(a context line)")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the forward-only timing of the other bf16 workloads that the "
                          "default (prefill) run appends as `workloads`")
@@ -876,8 +885,90 @@ def run_ffn_vs_cublas(args, local):
                     "in torch; cublas_gemms = the two torch.bmm alone (no SwiGLU: h is stale)"}
 
 
+def run_ep_emulated(args, local):
+    """Expert parallelism over G ranks, emulated on one GPU: every rank's
+    ExpertParallelMoE (its N/G experts) with its own batch of T tokens, the
+    exchanges done as device copies (the bytes an all-to-all moves, at copy
+    speed rather than a link's).  Timed against moe_forward of the one-GPU
+    layer on the same G*T tokens.  Both run on one GPU, so the ratio is the
+    expert-parallel path's device-side cost (regroup, return, G sets of
+    launches, the host reads of the split sizes), not a multi-GPU time."""
+    from sparse_mixture_experts_63_b300 import expert_parallel as EP
+    cfg = resolve_cfg(args)
+    G = args.ep_emulate
+    if cfg.N % G or cfg.cf:
+        raise SystemExit("--ep-emulate needs N divisible by G and no capacity limit "
+                         "(a capacity applies per rank's batch)")
+    dev = torch.device("cuda", local)
+    inp = make_inputs(cfg, device=dev)
+    Ne = cfg.N // G
+    layers = [EP.ExpertParallelMoE(inp.W_g, inp.W_gate[r * Ne:(r + 1) * Ne],
+                                   inp.W_up[r * Ne:(r + 1) * Ne], inp.W_down[r * Ne:(r + 1) * Ne],
+                                   cfg.k, r, G, bias=inp.bias, Ws_gate=inp.Ws_gate,
+                                   Ws_up=inp.Ws_up, Ws_down=inp.Ws_down)
+              for r in range(G)]
+    xs = [make_x(cfg, device=dev, seed=cfg.seed * 1000 + r + 1) for r in range(G)]
+    x_all = torch.cat(xs)
+    one = B.MoELayer(inp.W_g, inp.W_gate, inp.W_up, inp.W_down, cfg.k, bias=inp.bias,
+                     Ws_gate=inp.Ws_gate, Ws_up=inp.Ws_up, Ws_down=inp.Ws_down)
+    y_all = torch.empty((G * cfg.T, cfg.d), dtype=torch.float32, device=dev)
+    outs = one.outputs_for(G * cfg.T, dev)
+    a = one.args(x_all, y_all, outs)
+    wsb = one.workspace(a, dev)
+    stream = torch.cuda.current_stream()
+    launches0 = B.moe_launch_counter()
+    state = {}
+
+    def ep():
+        state["ys"] = EP.run_ranks_in_one_process(layers, xs)
+
+    def single():
+        B.moe_forward(a, wsb, stream)
+
+    def timed(fn):
+        E = lambda: torch.cuda.Event(enable_timing=True)   # noqa: E731
+        evs = [(E(), E()) for _ in range(args.steps)]
+        for s_, e_ in evs:
+            s_.record(stream)
+            fn()
+            e_.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(s_.elapsed_time(e_) for s_, e_ in evs)
+
+    for _ in range(args.warmup):
+        ep()
+        single()
+    torch.cuda.synchronize()
+    diff = max(float((state["ys"][r] - y_all[r * cfg.T:(r + 1) * cfg.T]).abs().max())
+               for r in range(G))
+    # rows each rank sent to other ranks, one forward (x rows + gate weights out, y rows back)
+    sent = 0
+    for L, x in zip(layers, xs):
+        st = L.dispatch(x)
+        sent += sum(n for q, n in enumerate(st.send_rows) if q != L.rank)
+    esize = 2 if cfg.dtype == "bf16" else 4
+    rounds = [(timed(ep), timed(single)) for _ in range(3)]
+    ep_ms = statistics.median(r[0] for r in rounds)
+    one_ms = statistics.median(r[1] for r in rounds)
+    return {"metric": "expert-parallel layer emulated on one GPU (all-to-alls as device copies)",
+            "workload": f"{cfg_desc(cfg)}; {G} ranks x {cfg.T} tokens, {Ne} experts per rank",
+            "value": round(G * cfg.T / (ep_ms / 1e3), 1), "unit": "tokens/s",
+            "ep_ms": round(ep_ms, 4), "one_gpu_layer_ms": round(one_ms, 4),
+            "ep_over_one_gpu": round(ep_ms / one_ms, 4),
+            "rows_exchanged_per_step": int(sent),
+            "bytes_exchanged_per_step": int(sent * (2 * cfg.d * esize + 4)),
+            "max_abs_ep_vs_one_gpu": diff,
+            "rounds_ms": [[round(x, 4), round(y, 4)] for x, y in rounds],
+            "gpu_launches": int(B.moe_launch_counter() - launches0),
+            "timing": f"3 rounds of {args.steps} back-to-back forwards per leg, medians of CUDA "
+                      "events; both legs on one GPU: not a multi-GPU time"}
+
+
 def main():
     args = parse()
+    if args.ep_emulate > 0:
+        print(json.dumps(run_ep_emulated(args, 0)), flush=True)
+        return
     if args.ffn_vs_cublas > 0:
         print(json.dumps(run_ffn_vs_cublas(args, 0)), flush=True)
         return
