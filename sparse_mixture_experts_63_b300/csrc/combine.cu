@@ -8,13 +8,45 @@
 // in fp32, slots in ascending order, then the shared output: deterministic.
 //
 // HBM-bound: one thread per 8 output elements, 16-byte loads of bf16 rows
-// (32-byte of fp32), coalesced along d.
+// (32-byte of fp32), coalesced along d.  A thread reads the token's slot
+// positions for up to KB slots at once and issues all of their row loads
+// before adding any: KB loads in flight per thread instead of one at a time
+// behind its position load (the sums are taken in the same slot order).
 #include "moe_internal.cuh"
 
 namespace moe {
 namespace {
 
-template <typename TI, typename TO>
+// 8 consecutive elements of a row, as loaded (bf16: 16 bytes; fp32: 32 bytes)
+template <typename TI> struct Raw8;
+template <> struct Raw8<__nv_bfloat16> {
+  uint4 q;
+  __device__ __forceinline__ void load(const __nv_bfloat16 *p) {
+    q = *reinterpret_cast<const uint4 *>(p);
+  }
+  __device__ __forceinline__ void add_to(float (&acc)[8]) const {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&q);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      acc[2 * i] += f.x;
+      acc[2 * i + 1] += f.y;
+    }
+  }
+};
+template <> struct Raw8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float *p) {
+    a = *reinterpret_cast<const float4 *>(p);
+    b = *reinterpret_cast<const float4 *>(p + 4);
+  }
+  __device__ __forceinline__ void add_to(float (&acc)[8]) const {
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+  }
+};
+
+template <typename TI, typename TO, int KB>
 __global__ void __launch_bounds__(256) combine_kernel(const TI *__restrict__ y_perm,
                                                       const int32_t *__restrict__ inv_pos, int T,
                                                       int k, int d, const TI *__restrict__ shared,
@@ -29,19 +61,23 @@ __global__ void __launch_bounds__(256) combine_kernel(const TI *__restrict__ y_p
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int p = __ldg(inv_pos + (size_t)t * k + j);
-      if (p < 0) continue;
-      float v[8];
-      load8(y_perm + (size_t)p * d + c, v);
+    for (int j0 = 0; j0 < k; j0 += KB) {
+      int pos[KB];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] += v[i];
+      for (int j = 0; j < KB; ++j)
+        pos[j] = j0 + j < k ? __ldg(inv_pos + (size_t)t * k + j0 + j) : -1;
+      Raw8<TI> r[KB];
+#pragma unroll
+      for (int j = 0; j < KB; ++j)
+        if (pos[j] >= 0) r[j].load(y_perm + (size_t)pos[j] * d + c);
+#pragma unroll
+      for (int j = 0; j < KB; ++j)   // slot order, dropped slots skipped
+        if (pos[j] >= 0) r[j].add_to(acc);
     }
     if (shared) {
-      float v[8];
-      load8(shared + (size_t)t * d + c, v);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] += v[i];
+      Raw8<TI> r;
+      r.load(shared + (size_t)t * d + c);
+      r.add_to(acc);
     }
     TO *dst = y + (size_t)t * d + c;
     if constexpr (sizeof(TO) == 4) {
@@ -64,7 +100,10 @@ moe_status_t launch_typed(const void *y_perm, const int32_t *inv_pos, int T, int
   if (total == 0) return MOE_OK;
   long grid = (total + 255) / 256;
   if (grid > 148L * 32) grid = 148L * 32;
-  MOE_CUDA_TRY(launch_pdl(combine_kernel<TI, TO>, dim3((int)grid), dim3(256), 0, stream,
+  // slots batched 2, 4 or 8 at a time (larger k in batches of 8)
+  auto fn = k <= 2 ? combine_kernel<TI, TO, 2> : k <= 4 ? combine_kernel<TI, TO, 4>
+                                                        : combine_kernel<TI, TO, 8>;
+  MOE_CUDA_TRY(launch_pdl(fn, dim3((int)grid), dim3(256), 0, stream,
       static_cast<const TI *>(y_perm), inv_pos, T, k, d, static_cast<const TI *>(shared_y),
       static_cast<TO *>(y)));
   MOE_LAUNCH_CHECK();
