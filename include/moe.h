@@ -267,6 +267,11 @@ moe_status_t moe_combine(const void *y_perm, moe_dtype_t y_perm_dtype,
 /* ---------------------------------------------------------------------------
  * The whole layer in one call: steps 1-6 plus the optional shared expert.
  * Optional outputs may be NULL (then workspace holds them).
+ *   Sizes: T >= 1 and 1 <= k <= N; d, f and fs multiples of 8 (d of 16 with
+ *   E4M3 gate/up, f of 16 with an E4M3 down projection); T*k < 2^31; every
+ *   tensor 16-byte aligned; re-routing needs a capacity and k + rounds <= N.
+ *   Otherwise MOE_ERR_INVALID_ARG (moe_forward_workspace_size returns 0).
+ *   N > 256, or k (+ reroute_rounds) > 32: MOE_ERR_UNSUPPORTED.
  * ------------------------------------------------------------------------- */
 typedef struct moe_forward_args {
   int T, d, f, N, k;
