@@ -71,6 +71,7 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
 #define MOE_DEV_TIMEOUT 0x4       /* a bounded on-chip wait gave up; output invalid */
 #define MOE_DEV_BAD_TILE 0x8      /* grouped-GEMM tile outside the expert layout     */
 #define MOE_DEV_BAD_COUNTS 0x10   /* expert-parallel counts do not add up to the rows */
+#define MOE_DEV_BAD_ROW 0x20      /* an output-row index outside the output rows      */
 
 const char *moe_status_string(moe_status_t s);
 const char *moe_last_error(void);
@@ -206,6 +207,23 @@ moe_status_t moe_expert_ffn(const void *x_perm, const int32_t *offsets,
                             const void *W_up, const void *W_down, void *y_perm,
                             int32_t *device_status, void *workspace,
                             size_t workspace_bytes, void *stream);
+
+/* The same FFN storing each output row at a caller-given row: y[out_row[p]]
+ * = row_scale[p] * SwiGLU_e(x_perm[p]) for every p < offsets[N].  out_row
+ * [A_max] device int32, indices into y [rows_out, d] (dtype); an index
+ * outside [0, rows_out) stores nothing and sets MOE_DEV_BAD_ROW in
+ * device_status.  Rows of y no p maps to are left as they are.  The
+ * expert-parallel layer passes moe_ep_regroup's `dest`, so the outputs land
+ * in received order without a moe_ep_return copy.  Same workspace as
+ * moe_expert_ffn; argument errors as there, plus NULL out_row or rows_out < 0
+ * (MOE_ERR_INVALID_ARG). */
+moe_status_t moe_expert_ffn_to_rows(const void *x_perm, const int32_t *offsets,
+                                    const float *row_scale, const int32_t *out_row,
+                                    int A_max, int d, int f, int N, moe_dtype_t dtype,
+                                    const void *W_gate, const void *W_up,
+                                    const void *W_down, void *y, int rows_out,
+                                    int32_t *device_status, void *workspace,
+                                    size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
  * Low-precision expert weights: FP8 E4M3 with absmax scales.
@@ -385,7 +403,9 @@ moe_status_t moe_forward_host_io_overlapped(const moe_forward_args *args,
  *   [R] fp32 (or NULL) in received order, R = sum of recv_counts.
  *   Outputs: x_local [R,d], row_scale_local [R] (if row_scale_recv),
  *   offsets_local [Ne+1] (moe_expert_ffn's offsets over the local experts),
- *   dest [R] int32: where received row i went.  If the counts do not add up
+ *   dest [R] int32: where received row i went; src [R] int32 or NULL: the
+ *   inverse, src[dest[i]] = i (moe_expert_ffn_to_rows's out_row, so the
+ *   outputs land in received order directly).  If the counts do not add up
  *   to R nothing is copied and MOE_DEV_BAD_COUNTS is set.
  * moe_ep_return: y_back[i] = y_local[dest[i]], the expert outputs put back in
  *   received order, ready for the return exchange; afterwards the source
@@ -397,8 +417,8 @@ moe_status_t moe_ep_regroup(const int32_t *recv_counts, int G, int Ne,
                             const void *x_recv, const float *row_scale_recv,
                             int R, int d, moe_dtype_t dtype, void *x_local,
                             float *row_scale_local, int32_t *offsets_local,
-                            int32_t *dest, int32_t *device_status,
-                            void *stream);
+                            int32_t *dest, int32_t *src,
+                            int32_t *device_status, void *stream);
 moe_status_t moe_ep_return(const void *y_local, const int32_t *dest, int R,
                            int d, moe_dtype_t dtype, void *y_back,
                            void *stream);

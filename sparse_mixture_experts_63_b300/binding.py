@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(_PKG, "libmoe.so")
 
 MOE_F32, MOE_BF16 = 0, 1
 MOE_DEV_BAD_EXPERT_ID, MOE_DEV_NAN_LOGIT, MOE_DEV_TIMEOUT, MOE_DEV_BAD_TILE = 1, 2, 4, 8
-MOE_DEV_BAD_COUNTS = 16
+MOE_DEV_BAD_COUNTS, MOE_DEV_BAD_ROW = 16, 32
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE"}
 
@@ -25,7 +25,8 @@ EXPORTS = ("moe_status_string", "moe_last_error", "moe_version", "moe_launch_cou
            "moe_capacity",
            "moe_router_topk", "moe_permute_workspace_size", "moe_permute",
            "moe_permute_noalloc",
-           "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
+           "moe_expert_ffn_workspace_size", "moe_expert_ffn", "moe_expert_ffn_to_rows",
+           "moe_combine",
            "moe_forward_workspace_size", "moe_forward", "moe_forward_host_io",
            "moe_forward_overlap_chunks", "moe_forward_host_io_overlapped",
            "moe_routing_stats_workspace_size", "moe_routing_stats",
@@ -92,6 +93,8 @@ def lib():
         L.moe_expert_ffn_workspace_size.restype = sz
         L.moe_expert_ffn.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp,
                                      sz, vp]
+        L.moe_expert_ffn_to_rows.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, vp, vp, vp, vp,
+                                             ci, vp, vp, sz, vp]
         L.moe_combine.argtypes = [vp, ci, vp, ci, ci, ci, vp, vp, ci, vp]
         L.moe_forward_workspace_size.argtypes = [ctypes.POINTER(moe_forward_args)]
         L.moe_forward_workspace_size.restype = sz
@@ -114,7 +117,7 @@ def lib():
         L.moe_expert_ffn_fp8_workspace_size.restype = sz
         L.moe_expert_ffn_fp8.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, vp, vp, vp, vp, vp,
                                          vp, vp, vp, vp, vp, sz, vp]
-        L.moe_ep_regroup.argtypes = [vp, ci, ci, vp, vp, ci, ci, ci, vp, vp, vp, vp, vp, vp]
+        L.moe_ep_regroup.argtypes = [vp, ci, ci, vp, vp, ci, ci, ci, vp, vp, vp, vp, vp, vp, vp]
         L.moe_ep_return.argtypes = [vp, vp, ci, ci, ci, vp, vp]
         for n in ("moe_router_topk", "moe_permute", "moe_permute_noalloc", "moe_expert_ffn",
                   "moe_ep_regroup", "moe_ep_return",
@@ -237,16 +240,25 @@ def moe_permute_noalloc(topk_idx, N, x=None, topk_w=None, capacity=0, gather=Tru
 
 
 def moe_expert_ffn(x_perm, offsets, W_gate, W_up, W_down, row_scale=None, y_perm=None,
-                   device_status=None, stream=None, A_max=None):
-    """y_perm [A_max,d] = row_scale * SwiGLU_e(x_perm) for each expert's rows."""
-    _cuda(x_perm, offsets, W_gate, W_up, W_down, row_scale, y_perm)
+                   device_status=None, stream=None, A_max=None, out_row=None, rows_out=None):
+    """y_perm [A_max,d] = row_scale * SwiGLU_e(x_perm) for each expert's rows.
+    With out_row (int32 [A_max]): moe_expert_ffn_to_rows, row p stored at
+    y_perm row out_row[p] of rows_out rows."""
+    _cuda(x_perm, offsets, W_gate, W_up, W_down, row_scale, y_perm, out_row)
     A = x_perm.shape[0] if A_max is None else A_max
     d = x_perm.shape[1]
     N, _, f = W_gate.shape
+    rows = A if out_row is None else (A if rows_out is None else rows_out)
     if y_perm is None:
-        y_perm = torch.empty((max(A, 1), d), dtype=x_perm.dtype, device=x_perm.device)
+        y_perm = torch.empty((max(rows, 1), d), dtype=x_perm.dtype, device=x_perm.device)
     ws_bytes = lib().moe_expert_ffn_workspace_size(A, d, f, N, _dt(x_perm))
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=x_perm.device)
+    if out_row is not None:
+        _check("moe_expert_ffn_to_rows", lib().moe_expert_ffn_to_rows(
+            _p(x_perm), _p(offsets), _p(row_scale), _p(out_row), A, d, f, N, _dt(x_perm),
+            _p(W_gate), _p(W_up), _p(W_down), _p(y_perm), rows, _p(device_status), _p(ws),
+            ws_bytes, _stream(stream)))
+        return y_perm
     _check("moe_expert_ffn", lib().moe_expert_ffn(
         _p(x_perm), _p(offsets), _p(row_scale), A, d, f, N, _dt(x_perm), _p(W_gate),
         _p(W_up), _p(W_down), _p(y_perm), _p(device_status), _p(ws), ws_bytes,
@@ -390,7 +402,8 @@ def moe_ep_regroup(recv_counts, Ne, x_recv, row_scale_recv=None, device_status=N
                    stream=None):
     """Rows received from G source ranks (block (s, e) = recv_counts[s*Ne + e]
     rows, in (s, e) order) regrouped by local expert.  Returns dict x_local,
-    row_scale_local (or None), offsets_local [Ne+1], dest [R]."""
+    row_scale_local (or None), offsets_local [Ne+1], dest [R] (where received
+    row i went) and src [R] (its inverse: the received row of local row p)."""
     _cuda(recv_counts, x_recv, row_scale_recv)
     G = recv_counts.numel() // Ne
     R, d = x_recv.shape
@@ -399,11 +412,12 @@ def moe_ep_regroup(recv_counts, Ne, x_recv, row_scale_recv=None, device_status=N
                row_scale_local=(torch.empty(max(R, 1), dtype=torch.float32, device=dev)
                                 if row_scale_recv is not None else None),
                offsets_local=torch.empty(Ne + 1, dtype=torch.int32, device=dev),
-               dest=torch.empty(max(R, 1), dtype=torch.int32, device=dev))
+               dest=torch.empty(max(R, 1), dtype=torch.int32, device=dev),
+               src=torch.empty(max(R, 1), dtype=torch.int32, device=dev))
     _check("moe_ep_regroup", lib().moe_ep_regroup(
         _p(recv_counts), G, Ne, _p(x_recv), _p(row_scale_recv), R, d, _dt(x_recv),
         _p(out["x_local"]), _p(out["row_scale_local"]), _p(out["offsets_local"]),
-        _p(out["dest"]), _p(device_status), _stream(stream)))
+        _p(out["dest"]), _p(out["src"]), _p(device_status), _stream(stream)))
     return out
 
 

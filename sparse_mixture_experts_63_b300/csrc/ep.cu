@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kEpThreads) ep_regroup_kernel(
     const int32_t *__restrict__ counts, int G, int Ne, const uint4 *__restrict__ x_recv,
     const float *__restrict__ rs_recv, int R, int vecs, uint4 *__restrict__ x_local,
     float *__restrict__ rs_local, int32_t *__restrict__ offsets_local,
-    int32_t *__restrict__ dest, int32_t *device_status) {
+    int32_t *__restrict__ dest, int32_t *__restrict__ src_row, int32_t *device_status) {
   pdl_begin();
   __shared__ EpScan sc;
   ep_scan(counts, G, Ne, sc, blockIdx.x == 0 ? offsets_local : nullptr);
@@ -94,6 +94,7 @@ __global__ void __launch_bounds__(kEpThreads) ep_regroup_kernel(
     for (int v = lane; v < vecs; v += 32) dst[v] = src[v];
     if (lane == 0) {
       dest[i] = to;
+      if (src_row) src_row[to] = (int32_t)i;
       if (rs_recv) rs_local[to] = rs_recv[i];
     }
   }
@@ -129,11 +130,12 @@ int ep_max_blocks() { return kEpMaxBlocks; }
 moe_status_t launch_ep_regroup(const int32_t *recv_counts, int G, int Ne, const void *x_recv,
                                const float *row_scale_recv, int R, size_t row_bytes,
                                void *x_local, float *row_scale_local, int32_t *offsets_local,
-                               int32_t *dest, int32_t *device_status, cudaStream_t stream) {
+                               int32_t *dest, int32_t *src_row, int32_t *device_status,
+                               cudaStream_t stream) {
   MOE_CUDA_TRY(launch_pdl(ep_regroup_kernel, dim3(ep_grid(R)), dim3(kEpThreads), 0, stream,
                           recv_counts, G, Ne, static_cast<const uint4 *>(x_recv), row_scale_recv,
                           R, (int)(row_bytes / 16), static_cast<uint4 *>(x_local),
-                          row_scale_local, offsets_local, dest, device_status));
+                          row_scale_local, offsets_local, dest, src_row, device_status));
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

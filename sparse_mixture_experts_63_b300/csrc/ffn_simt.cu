@@ -64,7 +64,9 @@ __device__ int find_expert_tile(const int32_t *offsets, int N, int tile, int &ro
   return s_e;
 }
 
-// DUAL: out = SiLU(A B0) * (A B1); else out = row_scale * (A B0).
+// DUAL: out = SiLU(A B0) * (A B1); else out = row_scale * (A B0), row p
+// stored at out_row[p] when out_row is set (an index outside [0, rows_out)
+// stores nothing and sets MOE_DEV_BAD_ROW).
 template <typename T, bool DUAL>
 __global__ void __launch_bounds__(256) grouped_gemm_simt(const T *__restrict__ A,
                                                          const int32_t *__restrict__ offsets,
@@ -72,7 +74,9 @@ __global__ void __launch_bounds__(256) grouped_gemm_simt(const T *__restrict__ A
                                                          const T *__restrict__ B0,
                                                          const T *__restrict__ B1,
                                                          const float *__restrict__ row_scale,
-                                                         T *__restrict__ out) {
+                                                         T *__restrict__ out,
+                                                         const int32_t *__restrict__ out_row,
+                                                         int rows_out, int32_t *status) {
   __shared__ float as[kBM][kKC + 1];
   __shared__ float b0s[kKC][kBN];
   __shared__ float b1s[DUAL ? kKC : 1][kBN];
@@ -124,6 +128,15 @@ __global__ void __launch_bounds__(256) grouped_gemm_simt(const T *__restrict__ A
   for (int i = 0; i < 4; ++i) {
     int p = row0 + ty + 8 * i;
     if (p >= row1) continue;
+    size_t orow = (size_t)p;
+    if (!DUAL && out_row) {
+      const int o = out_row[p];
+      if (o < 0 || o >= rows_out) {
+        report(status, MOE_DEV_BAD_ROW);
+        continue;
+      }
+      orow = (size_t)o;
+    }
     float s = (!DUAL && row_scale) ? row_scale[p] : 1.f;
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -136,7 +149,7 @@ __global__ void __launch_bounds__(256) grouped_gemm_simt(const T *__restrict__ A
       } else {
         v = acc0[i][j] * s;
       }
-      out[(size_t)p * Ncols + c] = from_f32<T>(v);
+      out[orow * Ncols + c] = from_f32<T>(v);
     }
   }
 }
@@ -145,6 +158,7 @@ template <typename T>
 moe_status_t launch_simt_typed(const void *x_perm, const int32_t *offsets, const float *row_scale,
                                int A_max, int d, int f, int N, const void *W_gate,
                                const void *W_up, const void *W_down, void *h, void *y_perm,
+                               const int32_t *out_row, int rows_out, int32_t *status,
                                cudaStream_t stream) {
   if (A_max == 0) return MOE_OK;
   // Upper bound on row tiles: each expert adds at most one partial tile.
@@ -152,12 +166,12 @@ moe_status_t launch_simt_typed(const void *x_perm, const int32_t *offsets, const
   dim3 g1(max_tiles, (f + kBN - 1) / kBN);
   grouped_gemm_simt<T, true><<<g1, 256, 0, stream>>>(
       static_cast<const T *>(x_perm), offsets, N, d, f, static_cast<const T *>(W_gate),
-      static_cast<const T *>(W_up), nullptr, static_cast<T *>(h));
+      static_cast<const T *>(W_up), nullptr, static_cast<T *>(h), nullptr, 0, status);
   MOE_LAUNCH_CHECK();
   dim3 g2(max_tiles, (d + kBN - 1) / kBN);
   grouped_gemm_simt<T, false><<<g2, 256, 0, stream>>>(
       static_cast<const T *>(h), offsets, N, f, d, static_cast<const T *>(W_down), nullptr,
-      row_scale, static_cast<T *>(y_perm));
+      row_scale, static_cast<T *>(y_perm), out_row, rows_out, status);
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
@@ -167,13 +181,14 @@ moe_status_t launch_simt_typed(const void *x_perm, const int32_t *offsets, const
 moe_status_t launch_ffn_simt(const void *x_perm, const int32_t *offsets, const float *row_scale,
                              int A_max, int d, int f, int N, moe_dtype_t dtype,
                              const void *W_gate, const void *W_up, const void *W_down, void *h,
-                             void *y_perm, int32_t *device_status, cudaStream_t stream) {
-  (void)device_status;
+                             void *y_perm, int32_t *device_status, cudaStream_t stream,
+                             const int32_t *out_row, int rows_out) {
   if (dtype == MOE_BF16)
     return launch_simt_typed<__nv_bfloat16>(x_perm, offsets, row_scale, A_max, d, f, N, W_gate,
-                                            W_up, W_down, h, y_perm, stream);
+                                            W_up, W_down, h, y_perm, out_row, rows_out,
+                                            device_status, stream);
   return launch_simt_typed<float>(x_perm, offsets, row_scale, A_max, d, f, N, W_gate, W_up,
-                                  W_down, h, y_perm, stream);
+                                  W_down, h, y_perm, out_row, rows_out, device_status, stream);
 }
 
 }  // namespace moe

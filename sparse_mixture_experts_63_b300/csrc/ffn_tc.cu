@@ -134,6 +134,10 @@ struct TcParams {
   const float *xscale;     // row scales: [T] by token (GEMM1) or [A] by permuted row (GEMM2)
   const int32_t *perm_token;  // [A] token of each permuted row (GEMM1), else null
   int out_f32;             // GEMM1: h written in fp32 (out holds floats), else bf16
+  // GEMM2: row p of the result goes to out row out_row[p] (null: row p); an
+  // index outside [0, rows_out) stores nothing and sets MOE_DEV_BAD_ROW
+  const int32_t *out_row;
+  int rows_out;
 };
 
 // Token sub-tiles of a tile: rows [row0, row0 + rows0) and, for a wide tile
@@ -336,9 +340,16 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams &p, const TileInfo
     for (int q = etid; q < ncols * 16; q += kEpiThreads) {
       const int c = q / 16, v = q % 16;
       if (v < vec_valid) {
+        int orow = srow0 + cc * 32 + c;
+        if (p.out_row) {
+          orow = p.out_row[orow];
+          if (orow < 0 || orow >= p.rows_out) {
+            if (v == 0) report(p.status, MOE_DEV_BAD_ROW);
+            continue;
+          }
+        }
         const uint4 val = *reinterpret_cast<const uint4 *>(ob + c * 128 + v * 8);
-        *reinterpret_cast<uint4 *>(p.out + (size_t)(srow0 + cc * 32 + c) * p.out_ld + m0 +
-                                   v * 8) = val;
+        *reinterpret_cast<uint4 *>(p.out + (size_t)orow * p.out_ld + m0 + v * 8) = val;
       }
     }
   }
@@ -897,7 +908,8 @@ moe_status_t check_ffn_launch(int N) {
 // GEMM2 (down projection + gate scale) of either form: h [A_max, f] bf16.
 moe_status_t launch_down(const int32_t *offsets, const float *row_scale, int A_max, int d,
                          int f, int N, const TileCfg &tc_, const void *W_down, void *h,
-                         void *y_perm, int32_t *device_status, cudaStream_t stream) {
+                         void *y_perm, int32_t *device_status, cudaStream_t stream,
+                         const int32_t *out_row = nullptr, int rows_out = 0) {
   CUtensorMap wd, bh[kNumBoxes];
   bool ok = make_weight_map(&wd, W_down, N, f, d);
   const int box_rows[kNumBoxes] = {32, 64, 80, 128};
@@ -909,6 +921,8 @@ moe_status_t launch_down(const int32_t *offsets, const float *row_scale, int A_m
   TcParams p2{offsets, N, f, d, (d + 255) / 256, 0, static_cast<__nv_bfloat16 *>(y_perm), d,
               row_scale, device_status, raster_group(f), tc_.tile_cap, tc_.wide, tc_.stages,
               tc_.kgroup, tc_.stage_bytes};
+  p2.out_row = out_row;
+  p2.rows_out = rows_out;
   return launch_gemm<false>(wd, wd, bh, p2, stream);
 }
 
@@ -918,7 +932,8 @@ moe_status_t launch_down(const int32_t *offsets, const float *row_scale, int A_m
 moe_status_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, const float *row_scale,
                            int A_max, int d, int f, int N, int capacity, const void *W_gate,
                            const void *W_up, const void *W_down, void *h, void *y_perm,
-                           int32_t *device_status, cudaStream_t stream) {
+                           int32_t *device_status, cudaStream_t stream,
+                           const int32_t *out_row, int rows_out) {
   if (A_max == 0) return MOE_OK;
   moe_status_t s = check_ffn_launch(N);
   if (s != MOE_OK) return s;
@@ -937,7 +952,7 @@ moe_status_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, const flo
   s = launch_gemm<false>(wg, wu, bx, p1, stream);
   if (s != MOE_OK) return s;
   return launch_down(offsets, row_scale, A_max, d, f, N, c, W_down, h, y_perm, device_status,
-                     stream);
+                     stream, out_row, rows_out);
 }
 
 // h in bf16 (bf16 down projection), or in fp32 followed by its E4M3 codes

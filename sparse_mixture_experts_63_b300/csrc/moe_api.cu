@@ -219,13 +219,13 @@ moe_status_t launch_expert_ffn(const void *x_perm, const int32_t *offsets, const
                                int A_max, int d, int f, int N, int capacity, moe_dtype_t dtype,
                                const void *W_gate, const void *W_up, const void *W_down,
                                void *y_perm, int32_t *device_status, void *workspace,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, const int32_t *out_row, int rows_out) {
   void *h = workspace;
   if (dtype == MOE_BF16)
     return launch_ffn_tc(x_perm, offsets, row_scale, A_max, d, f, N, capacity, W_gate, W_up,
-                         W_down, h, y_perm, device_status, stream);
+                         W_down, h, y_perm, device_status, stream, out_row, rows_out);
   return launch_ffn_simt(x_perm, offsets, row_scale, A_max, d, f, N, dtype, W_gate, W_up,
-                         W_down, h, y_perm, device_status, stream);
+                         W_down, h, y_perm, device_status, stream, out_row, rows_out);
 }
 
 }  // namespace moe
@@ -327,6 +327,28 @@ moe_status_t moe_expert_ffn(const void *x_perm, const int32_t *offsets, const fl
   return launch_expert_ffn(x_perm, offsets, row_scale, A_max, d, f, N, 0, dtype, W_gate, W_up,
                            W_down, y_perm, device_status, workspace,
                            static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_expert_ffn_to_rows(const void *x_perm, const int32_t *offsets,
+                                    const float *row_scale, const int32_t *out_row, int A_max,
+                                    int d, int f, int N, moe_dtype_t dtype, const void *W_gate,
+                                    const void *W_up, const void *W_down, void *y, int rows_out,
+                                    int32_t *device_status, void *workspace,
+                                    size_t workspace_bytes, void *stream) {
+  moe_status_t s = validate_ffn(x_perm, offsets, A_max, d, f, N, dtype, W_gate, W_up, W_down,
+                                y);
+  if (s != MOE_OK) return s;
+  CHECK_ARG(rows_out >= 0, "rows_out=%d must be >= 0", rows_out);
+  CHECK_ARG(A_max == 0 || out_row, "out_row is NULL");
+  size_t need = ffn_workspace_bytes(A_max, d, f, N, dtype);
+  if (need > 0 && (!workspace || workspace_bytes < need)) {
+    set_error("moe_expert_ffn_to_rows: workspace %zu bytes, needs %zu", workspace_bytes, need);
+    return MOE_ERR_WORKSPACE;
+  }
+  if ((s = check_device()) != MOE_OK) return s;
+  return launch_expert_ffn(x_perm, offsets, row_scale, A_max, d, f, N, 0, dtype, W_gate, W_up,
+                           W_down, y, device_status, workspace,
+                           static_cast<cudaStream_t>(stream), out_row, rows_out);
 }
 
 moe_status_t moe_quantize_weights_e4m3(const void *W, int N, int d, int f, uint8_t *Wq,
@@ -470,7 +492,7 @@ moe_status_t moe_combine(const void *y_perm, moe_dtype_t y_perm_dtype, const int
 moe_status_t moe_ep_regroup(const int32_t *recv_counts, int G, int Ne, const void *x_recv,
                             const float *row_scale_recv, int R, int d, moe_dtype_t dtype,
                             void *x_local, float *row_scale_local, int32_t *offsets_local,
-                            int32_t *dest, int32_t *device_status, void *stream) {
+                            int32_t *dest, int32_t *src, int32_t *device_status, void *stream) {
   CHECK_ARG(dtype_ok(dtype), "bad dtype");
   CHECK_ARG(G >= 1 && Ne >= 1 && R >= 0 && d >= 1, "bad sizes G=%d Ne=%d R=%d d=%d", G, Ne, R, d);
   if ((long)G * Ne > ep_max_blocks()) {
@@ -486,7 +508,7 @@ moe_status_t moe_ep_regroup(const int32_t *recv_counts, int G, int Ne, const voi
   if (s != MOE_OK) return s;
   return launch_ep_regroup(recv_counts, G, Ne, x_recv, row_scale_recv, R,
                            (size_t)d * esize(dtype), x_local, row_scale_local, offsets_local,
-                           dest, device_status, static_cast<cudaStream_t>(stream));
+                           dest, src, device_status, static_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_ep_return(const void *y_local, const int32_t *dest, int R, int d,

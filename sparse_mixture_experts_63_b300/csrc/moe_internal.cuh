@@ -157,11 +157,13 @@ moe_status_t launch_ffn_tc_fp8(const void *xq_perm, const float *x_scale,
 size_t ffn_workspace_bytes(int A_max, int d, int f, int N, moe_dtype_t dtype);
 // capacity: rows per expert the dispatch kept at most (0 = unknown/none); a
 // tiling hint only.
+// out_row (nullable): output row p goes to y_perm row out_row[p] (< rows_out).
 moe_status_t launch_expert_ffn(const void *x_perm, const int32_t *offsets,
                                const float *row_scale, int A_max, int d, int f, int N,
                                int capacity, moe_dtype_t dtype, const void *W_gate,
                                const void *W_up, const void *W_down, void *y_perm,
-                               int32_t *device_status, void *workspace, cudaStream_t stream);
+                               int32_t *device_status, void *workspace, cudaStream_t stream,
+                               const int32_t *out_row = nullptr, int rows_out = 0);
 
 size_t reroute_workspace_bytes(int T, int N, int k);
 moe_status_t launch_permute_reroute(const int32_t *cand, const float *cand_w, const void *x,
@@ -186,7 +188,8 @@ moe_status_t launch_ffn_simt(const void *x_perm, const int32_t *offsets,
                              const float *row_scale, int A_max, int d, int f, int N,
                              moe_dtype_t dtype, const void *W_gate, const void *W_up,
                              const void *W_down, void *h, void *y_perm,
-                             int32_t *device_status, cudaStream_t stream);
+                             int32_t *device_status, cudaStream_t stream,
+                             const int32_t *out_row = nullptr, int rows_out = 0);
 
 // bf16 tcgen05 router (returns MOE_ERR_UNSUPPORTED when N does not suit it).
 moe_status_t launch_router_tc(const void *x, const void *W_g, const float *bias, int T, int d,
@@ -194,10 +197,13 @@ moe_status_t launch_router_tc(const void *x, const void *W_g, const float *bias,
                               int32_t *device_status, cudaStream_t stream);
 
 // bf16 tcgen05 grouped SwiGLU FFN (the bf16 layer's path).
+// out_row (nullable): output row p goes to y_perm row out_row[p], checked
+// against rows_out (MOE_DEV_BAD_ROW).
 moe_status_t launch_ffn_tc(const void *x_perm, const int32_t *offsets, const float *row_scale,
                            int A_max, int d, int f, int N, int capacity, const void *W_gate,
                            const void *W_up, const void *W_down, void *h, void *y_perm,
-                           int32_t *device_status, cudaStream_t stream);
+                           int32_t *device_status, cudaStream_t stream,
+                           const int32_t *out_row = nullptr, int rows_out = 0);
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -207,7 +213,8 @@ int ep_max_blocks();
 moe_status_t launch_ep_regroup(const int32_t *recv_counts, int G, int Ne, const void *x_recv,
                                const float *row_scale_recv, int R, size_t row_bytes,
                                void *x_local, float *row_scale_local, int32_t *offsets_local,
-                               int32_t *dest, int32_t *device_status, cudaStream_t stream);
+                               int32_t *dest, int32_t *src_row, int32_t *device_status,
+                               cudaStream_t stream);
 moe_status_t launch_ep_return(const void *y_local, const int32_t *dest, int R, size_t row_bytes,
                               void *y_back, cudaStream_t stream);
 

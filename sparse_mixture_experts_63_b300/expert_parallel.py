@@ -12,9 +12,10 @@ One forward, per rank:
      are one contiguous range of it;
   2. exchange of the kept counts per expert (G*Ne int32: Ne to each rank);
   3. exchange of the rows and their gate weights (row_scale);
-  4. regroup by local expert (moe_ep_regroup), the local grouped SwiGLU FFN
-     (moe_expert_ffn, gate weight applied in its epilogue), and the outputs
-     put back in received order (moe_ep_return);
+  4. regroup by local expert (moe_ep_regroup), then the local grouped SwiGLU
+     FFN (gate weight applied in its epilogue) storing each output row at its
+     received position (moe_expert_ffn_to_rows with the regroup's inverse
+     map), ready for the return exchange;
   5. the reverse exchange of the output rows, which land in the source rank's
      own x_perm order;
   6. combine (moe_combine) into y, with the optional always-on shared expert
@@ -145,10 +146,9 @@ class ExpertParallelMoE:
         R = sum(st.recv_rows)
         g = B.moe_ep_regroup(st.recv_counts, self.Ne, x_recv[:R], rs_recv[:R],
                              device_status=self.status)
-        y_local = B.moe_expert_ffn(g["x_local"], g["offsets_local"], self.Wg, self.Wu, self.Wd,
-                                   row_scale=g["row_scale_local"], device_status=self.status,
-                                   A_max=R)
-        return B.moe_ep_return(y_local, g["dest"], R)
+        return B.moe_expert_ffn(g["x_local"], g["offsets_local"], self.Wg, self.Wu, self.Wd,
+                                row_scale=g["row_scale_local"], device_status=self.status,
+                                A_max=R, out_row=g["src"], rows_out=R)
 
     # step 6: the output rows, back in this rank's x_perm order, combined
     def combine(self, st: EPState, y_perm):

@@ -216,15 +216,21 @@ def test_ep_argument_errors(lib):
     fake = ctypes.c_void_p(4096)
     # G * Ne beyond the supported 4096 blocks
     assert lib.moe_ep_regroup(fake, 64, 65, fake, None, 10, 64, B.MOE_BF16, fake, None, fake, fake,
-                              None, None) == 2
+                              None, None, None) == 2
     # rows that are not a multiple of 16 bytes (bf16, d = 4)
     assert lib.moe_ep_regroup(fake, 2, 2, fake, None, 10, 4, B.MOE_BF16, fake, None, fake, fake,
-                              None, None) == 1
+                              None, None, None) == 1
     # missing destination map
     assert lib.moe_ep_regroup(fake, 2, 2, fake, None, 10, 64, B.MOE_BF16, fake, None, fake, None,
-                              None, None) == 1
+                              None, None, None) == 1
     # a row scale in without one out
     assert lib.moe_ep_regroup(fake, 2, 2, fake, fake, 10, 64, B.MOE_BF16, fake, None, fake, fake,
-                              None, None) == 1
+                              None, None, None) == 1
     assert lib.moe_ep_return(fake, None, 10, 64, B.MOE_BF16, fake, None) == 1
+    # the FFN with an output-row map: the map is required, rows_out >= 0
+    ws = ctypes.c_void_p(4096)
+    assert lib.moe_expert_ffn_to_rows(fake, fake, None, None, 10, 64, 64, 2, B.MOE_BF16, fake,
+                                      fake, fake, fake, 10, None, ws, 1 << 30, None) == 1
+    assert lib.moe_expert_ffn_to_rows(fake, fake, None, fake, 10, 64, 64, 2, B.MOE_BF16, fake,
+                                      fake, fake, fake, -1, None, ws, 1 << 30, None) == 1
     assert lib.moe_ep_return(fake, fake, -1, 64, B.MOE_BF16, fake, None) == 1

@@ -59,9 +59,54 @@ def test_regroup_and_return_bit_exact(G, Ne, dtype, seed):
     assert int(st.item()) == 0
     assert out["offsets_local"].cpu().tolist() == off
     assert torch.equal(out["dest"][:R].cpu().long(), dest)
+    src = out["src"][:R].cpu().long()                  # the inverse map: src[dest[i]] = i
+    assert torch.equal(src[dest], torch.arange(R))
     assert torch.equal(out["x_local"][:R].cpu(), xr)
     assert torch.equal(out["row_scale_local"][:R].cpu(), rsr)
     assert torch.equal(y[:R].cpu(), x)                   # the return undoes the regroup
+
+
+@pytest.mark.parametrize("counts,dtype", [
+    pytest.param([0, 1, 160, 161, 300, 7], torch.bfloat16, id="bf16-256-row-tiles"),
+    pytest.param([257, 290, 203, 313], torch.bfloat16, id="bf16-wide-tiles"),
+    pytest.param([5, 0, 40, 13], torch.float32, id="fp32")])
+def test_expert_ffn_to_rows_equals_ffn_then_scatter(counts, dtype):
+    """moe_expert_ffn_to_rows = moe_expert_ffn followed by y[out_row[p]] = y_perm[p],
+    bit for bit (bf16 on the tensor cores, one-sub-tile and wide tiles; fp32 on the
+    CUDA cores); rows no p maps to keep their contents; an out-of-range row stores
+    nothing and sets MOE_DEV_BAD_ROW."""
+    g = torch.Generator().manual_seed(sum(counts) + len(counts))
+    N, d, f = len(counts), 128, 256
+    A = sum(counts)
+    x = torch.randn((A, d), generator=g).to(dtype).cuda()
+    Wg = (torch.randn((N, d, f), generator=g) / d ** 0.5).to(dtype).cuda()
+    Wu = (torch.randn((N, d, f), generator=g) / d ** 0.5).to(dtype).cuda()
+    Wd = (torch.randn((N, f, d), generator=g) / f ** 0.5).to(dtype).cuda()
+    rs = torch.rand(A, generator=g).cuda()
+    off = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int32).cuda()
+    rows_out = A + 5
+    perm = torch.randperm(rows_out, generator=g)[:A]
+    out_row = perm.to(torch.int32).cuda()
+    y_ref = B.moe_expert_ffn(x, off, Wg, Wu, Wd, row_scale=rs)
+    y = torch.full((rows_out, d), 7.0, dtype=dtype, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.moe_expert_ffn(x, off, Wg, Wu, Wd, row_scale=rs, out_row=out_row, rows_out=rows_out,
+                     y_perm=y, device_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(y[perm.cuda()], y_ref[:A])
+    untouched = torch.ones(rows_out, dtype=torch.bool)
+    untouched[perm] = False
+    assert bool((y[untouched.cuda()] == 7.0).all())
+    bad = out_row.clone()
+    bad[A // 2] = rows_out                                    # outside the output
+    y2 = torch.full((rows_out, d), 7.0, dtype=dtype, device="cuda")
+    B.moe_expert_ffn(x, off, Wg, Wu, Wd, row_scale=rs, out_row=bad, rows_out=rows_out,
+                     y_perm=y2, device_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & B.MOE_DEV_BAD_ROW
+    keep = torch.arange(A) != A // 2
+    assert torch.equal(y2[perm[keep].cuda()], y_ref[:A][keep.cuda()])
 
 
 def test_regroup_flags_counts_that_do_not_add_up():
